@@ -1,0 +1,599 @@
+// C-ABI entry points of include/bst.h: argument validation, TMA tensor-map
+// construction, tile/grid selection and kernel launch.  No entry point
+// allocates memory or synchronises (except bst_check_async).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/bst.h"
+#include "internal.h"
+
+namespace bst {
+
+// Per-device error word: [0] flags (kErr*), [1] block, [2] where, [3] spare.
+__device__ uint32_t g_err_word[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    uint32_t sms = 0;
+    uint32_t max_smem = 0;
+    uint32_t* err = nullptr;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+thread_local uint64_t t_timeout_ns = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bst_status device_info(DeviceInfo& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BST_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return BST_ERR_CUDA;
+        void* err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) return BST_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sms = static_cast<uint32_t>(sms);
+        d.max_smem = static_cast<uint32_t>(smem);
+        d.err = static_cast<uint32_t*>(err);
+        d.ready = true;
+    }
+    out = d;
+    return d.supported ? BST_OK : BST_ERR_UNSUPPORTED;
+}
+
+bool encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+uint32_t dtype_bytes(bst_dtype t) {
+    switch (t) {
+        case BST_F16: case BST_BF16: return 2;
+        case BST_E4M3: case BST_S8: return 1;
+        case BST_F32: case BST_S32: return 4;
+    }
+    return 0;
+}
+
+bool out_code(bst_dtype t, uint32_t& code) {
+    if (t == BST_F16) code = kOutF16;
+    else if (t == BST_BF16) code = kOutBF16;
+    else if (t == BST_F32) code = kOutF32;
+    else return false;
+    return true;
+}
+
+uint64_t timeout_ns() { return t_timeout_ns ? t_timeout_ns : kDefaultTimeoutNs; }
+
+struct Sched {
+    uint32_t offset = 1, dir = 0, tile_n = 0, num_ctas = 0;
+    uint32_t* trace = nullptr;
+};
+
+bst_status read_sched(const bst_sched* s, Sched& out) {
+    if (!s) return BST_OK;
+    if (s->swizzle_offset < 1 || s->swizzle_direction > 1) return BST_ERR_INVALID_ARG;
+    if (s->tile_n != 0 && s->tile_n != 64 && s->tile_n != 128 && s->tile_n != 256) return BST_ERR_INVALID_ARG;
+    out.offset = s->swizzle_offset;
+    out.dir = s->swizzle_direction;
+    out.tile_n = s->tile_n;
+    out.num_ctas = s->num_ctas;
+    out.trace = s->trace;
+    return BST_OK;
+}
+
+// Operand of a GEMM as the kernel sees it: which index is contiguous, and
+// whether TMA can fetch it (16-byte aligned base, pitch and batch stride).
+struct OperandSpec {
+    const void* ptr;
+    uint32_t esize;
+    uint64_t mn;          // rows of A (M) or columns of B (N) -- the MN extent
+    uint64_t k;           // K
+    int64_t ld;
+    int64_t batch_stride;
+    uint64_t batch;       // 1 for 2-D
+    bool mn_major;
+};
+
+bool tma_ok(const OperandSpec& o) {
+    const uintptr_t p = reinterpret_cast<uintptr_t>(o.ptr);
+    if (p % 16) return false;
+    if ((static_cast<uint64_t>(o.ld) * o.esize) % 16) return false;
+    if (o.batch > 1 && (static_cast<uint64_t>(o.batch_stride) * o.esize) % 16) return false;
+    if (o.batch > 1 && static_cast<uint64_t>(o.batch_stride) * o.esize >= (1ull << 40)) return false;
+    if (static_cast<uint64_t>(o.ld) * o.esize >= (1ull << 40)) return false;
+    return true;
+}
+
+uint32_t plain_vec(const OperandSpec& o) {
+    uint32_t v = 16;
+    const uint64_t p = reinterpret_cast<uintptr_t>(o.ptr);
+    while (v > o.esize && (p % v || (static_cast<uint64_t>(o.ld) * o.esize) % v ||
+                           (o.batch > 1 && (static_cast<uint64_t>(o.batch_stride) * o.esize) % v)))
+        v >>= 1;
+    return v;
+}
+
+bst_status encode(CUtensorMap* map, const OperandSpec& o, uint32_t tile_mn, CUtensorMapDataType dt) {
+    if (!encoder()) return BST_ERR_CUDA;
+    const uint32_t bk = kLine / o.esize;   // elements per 128-byte line
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (!o.mn_major) {
+        dims[0] = o.k; dims[1] = o.mn;
+        box[0] = bk; box[1] = tile_mn;
+    } else {
+        dims[0] = o.mn; dims[1] = o.k;
+        box[0] = bk; box[1] = bk;
+    }
+    strides[0] = static_cast<cuuint64_t>(o.ld) * o.esize;
+    uint32_t rank = 2;
+    if (o.batch > 1 && o.batch_stride != 0) {
+        dims[2] = o.batch;
+        strides[1] = static_cast<cuuint64_t>(o.batch_stride) * o.esize;
+        box[2] = 1;
+        rank = 3;
+    }
+    CUresult r = g_encode(map, dt, rank, const_cast<void*>(o.ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BST_OK : BST_ERR_ALIGNMENT;
+}
+
+bst_status fill_operand(OperandDesc& d, CUtensorMap* map, const OperandSpec& o, uint32_t tile_mn,
+                        CUtensorMapDataType dt, bool require_tma) {
+    d.ptr = static_cast<const uint8_t*>(o.ptr);
+    d.ld = o.ld;
+    d.batch_stride = o.batch_stride;
+    d.mn_major = o.mn_major ? 1u : 0u;
+    d.use_tma = tma_ok(o) ? 1u : 0u;
+    d.vec_bytes = plain_vec(o);
+    // a batch stride of 0 broadcasts one matrix to every batch: 2-D map, z ignored
+    d.tma_rank = (o.batch > 1 && o.batch_stride != 0) ? 3u : 2u;
+    if (!d.use_tma) {
+        if (require_tma) return BST_ERR_ALIGNMENT;
+        std::memset(map, 0, sizeof(*map));
+        return BST_OK;
+    }
+    return encode(map, o, tile_mn, dt);
+}
+
+// Picks the tile width by a small cost model: tiles per SM wave times the
+// per-tile time, with narrow tiles derated because tcgen05 reads more
+// shared-memory bytes per flop for them.
+uint32_t choose_bn(uint64_t loops_m_total, uint64_t N, uint32_t sms, bool allow64) {
+    static const uint32_t cand[3] = {256, 128, 64};
+    static const double eff[3] = {1.0, 0.9, 0.67};
+    uint32_t best = 256;
+    double best_cost = 1e300;
+    for (int i = 0; i < 3; ++i) {
+        if (cand[i] == 64 && !allow64) continue;
+        const uint64_t tiles = loops_m_total * ((N + cand[i] - 1) / cand[i]);
+        const uint64_t waves = (tiles + sms - 1) / sms;
+        const double cost = static_cast<double>(waves) * cand[i] / eff[i];
+        if (cost < best_cost * 0.999) { best_cost = cost; best = cand[i]; }
+    }
+    return best;
+}
+
+CUtensorMapDataType tmap_type(bst_dtype t) {
+    if (t == BST_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (t == BST_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+}
+
+bst_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BST_OK : BST_ERR_CUDA; }
+
+constexpr uint64_t kMaxDim = (1ull << 31) - 1;
+
+// A [M,K] / B [K,N] logical -> operand specs.  Row-major A is K-contiguous;
+// row-major B is N-contiguous (MN-major).
+bst_status make_specs(uint64_t M, uint64_t N, uint64_t K, const void* A, bst_layout la, int64_t lda, int64_t sa,
+                      const void* B, bst_layout lb, int64_t ldb, int64_t sb, uint32_t esize, uint64_t batch,
+                      OperandSpec& a, OperandSpec& b) {
+    if (la != BST_ROW_MAJOR && la != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
+    if (lb != BST_ROW_MAJOR && lb != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
+    a = OperandSpec{A, esize, M, K, lda, sa, batch, la == BST_COL_MAJOR};
+    b = OperandSpec{B, esize, N, K, ldb, sb, batch, lb == BST_ROW_MAJOR};
+    const uint64_t a_contig = a.mn_major ? M : K;
+    const uint64_t b_contig = b.mn_major ? N : K;
+    if (lda < 1 || static_cast<uint64_t>(lda) < a_contig) return BST_ERR_INVALID_ARG;
+    if (ldb < 1 || static_cast<uint64_t>(ldb) < b_contig) return BST_ERR_INVALID_ARG;
+    return BST_OK;
+}
+
+bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void* A, bst_dtype at, bst_layout la,
+                     int64_t lda, int64_t sa, const void* B, bst_dtype bt, bst_layout lb, int64_t ldb, int64_t sb,
+                     void* C, bst_dtype ct, int64_t ldc, int64_t sc, int64_t batch, const bst_sched* sched_in,
+                     void* stream_v) {
+    if (M < 0 || N < 0 || K < 0 || batch < 1) return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(M) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(K) > kMaxDim || static_cast<uint64_t>(batch) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    if (at != bt || (at != BST_F16 && at != BST_BF16)) return BST_ERR_UNSUPPORTED;
+    uint32_t c_code;
+    if (!out_code(ct, c_code)) return BST_ERR_UNSUPPORTED;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
+    if (mode == kModeBatched && (sa < 0 || sb < 0 || sc < 0)) return BST_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BST_OK;
+    if (!C || (K > 0 && (!A || !B))) return BST_ERR_INVALID_ARG;
+    OperandSpec a, b;
+    if (bst_status s = make_specs(M, N, K, A, la, lda, sa, B, lb, ldb, sb, 2, static_cast<uint64_t>(batch), a, b))
+        return s;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const uint32_t csize = dtype_bytes(ct);
+    if (K == 0)
+        return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, sc, M, N, batch, csize, dev.sms, stream));
+
+    const uint64_t loops_m = (M + kBM - 1) / kBM;
+    const uint32_t bn = sch.tile_n ? sch.tile_n : choose_bn(loops_m * batch, N, dev.sms, true);
+    const uint64_t tiles = loops_m * ((N + bn - 1) / bn) * batch;
+    if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    if (smem_dense(bn, 0) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, tmap_type(at), false)) return s;
+    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, bn, tmap_type(bt), false)) return s;
+    p.M = M; p.N = N; p.K = K;
+    p.batch = batch;
+    p.mode = mode;
+    p.ab_fmt = at == BST_BF16 ? 1u : 0u;
+    p.esize = 2;
+    p.swz_offset = sch.offset;
+    p.swz_dir = sch.dir;
+    p.num_kb = (K + 63) / 64;
+    p.chunk_kb = p.num_kb;
+    p.total_tiles = static_cast<uint32_t>(tiles);
+    p.C = static_cast<uint8_t*>(C);
+    p.ldc = ldc;
+    p.c_batch_stride = sc;
+    p.c_type = c_code;
+    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0) &&
+              (mode != kModeBatched || (sc * csize) % 16 == 0);
+    p.trace = sch.trace;
+    p.trace_cap = static_cast<uint32_t>(tiles);
+    p.err = dev.err;
+    p.timeout_ns = timeout_ns();
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
+    return cuda_status(launch_dense(p, bn, grid, stream));
+}
+
+bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout la, int64_t lda, const void* B,
+                    bst_layout lb, int64_t ldb, void* C, bst_dtype ct, int64_t ldc, const uint8_t* sfa,
+                    const uint8_t* sfb, const bst_sched* sched_in, void* stream_v) {
+    if (M < 0 || N < 0 || K < 0) return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(M) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(K) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    uint32_t c_code;
+    if (!out_code(ct, c_code)) return BST_ERR_UNSUPPORTED;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (la != BST_ROW_MAJOR || lb != BST_COL_MAJOR) return BST_ERR_UNSUPPORTED;
+    if (K % 128) return BST_ERR_UNSUPPORTED;
+    if (sch.tile_n == 64) return BST_ERR_UNSUPPORTED;
+    if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BST_OK;
+    if (!C || (K > 0 && (!A || !B || !sfa || !sfb))) return BST_ERR_INVALID_ARG;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(sfa) | reinterpret_cast<uintptr_t>(sfb)) % 4))
+        return BST_ERR_ALIGNMENT;
+    OperandSpec a, b;
+    if (bst_status s = make_specs(M, N, K, A, la, lda, 0, B, lb, ldb, 0, 1, 1, a, b)) return s;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const uint32_t csize = dtype_bytes(ct);
+    if (K == 0) return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, M, N, 1, csize, dev.sms, stream));
+    const uint64_t loops_m = (M + kBM - 1) / kBM;
+    const uint32_t bn = sch.tile_n ? sch.tile_n : choose_bn(loops_m, N, dev.sms, false);
+    const uint64_t tiles = loops_m * ((N + bn - 1) / bn);
+    if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    if (smem_mxf8(bn) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
+    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, bn, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
+    p.M = M; p.N = N; p.K = K;
+    p.batch = 1;
+    p.mode = kModePlain;
+    p.esize = 1;
+    p.swz_offset = sch.offset;
+    p.swz_dir = sch.dir;
+    p.num_kb = K / 128;
+    p.chunk_kb = p.num_kb;
+    p.total_tiles = static_cast<uint32_t>(tiles);
+    p.C = static_cast<uint8_t*>(C);
+    p.ldc = ldc;
+    p.c_type = c_code;
+    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
+    p.sfa = sfa;
+    p.sfb = sfb;
+    p.sf_ld = static_cast<uint32_t>(K / 32);
+    p.trace = sch.trace;
+    p.trace_cap = static_cast<uint32_t>(tiles);
+    p.err = dev.err;
+    p.timeout_ns = timeout_ns();
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
+    return cuda_status(launch_mxf8(p, bn, grid, stream));
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace bst
+
+using namespace bst;
+
+extern "C" {
+
+bst_status bst_gemm(int64_t M, int64_t N, int64_t K, const void* A, bst_dtype a_type, bst_layout a_layout,
+                    int64_t lda, const void* B, bst_dtype b_type, bst_layout b_layout, int64_t ldb, void* C,
+                    bst_dtype c_type, int64_t ldc, const uint8_t* scale_a, const uint8_t* scale_b,
+                    const bst_sched* sched, void* stream) {
+    if (a_type == BST_E4M3 || b_type == BST_E4M3) {
+        if (a_type != b_type) return BST_ERR_UNSUPPORTED;
+        return run_mxf8(M, N, K, A, a_layout, lda, B, b_layout, ldb, C, c_type, ldc, scale_a, scale_b, sched, stream);
+    }
+    if (scale_a || scale_b) return BST_ERR_INVALID_ARG;
+    return run_dense(kModePlain, M, N, K, A, a_type, a_layout, lda, 0, B, b_type, b_layout, ldb, 0, C, c_type, ldc,
+                     0, 1, sched, stream);
+}
+
+bst_status bst_gemm_batched(int64_t M, int64_t N, int64_t K, const void* A, bst_dtype a_type, bst_layout a_layout,
+                            int64_t lda, int64_t stride_a, const void* B, bst_dtype b_type, bst_layout b_layout,
+                            int64_t ldb, int64_t stride_b, void* C, bst_dtype c_type, int64_t ldc, int64_t stride_c,
+                            int64_t batch, const bst_sched* sched, void* stream) {
+    return run_dense(batch > 1 ? kModeBatched : kModePlain, M, N, K, A, a_type, a_layout, lda, stride_a, B, b_type,
+                     b_layout, ldb, stride_b, C, c_type, ldc, stride_c, batch, sched, stream);
+}
+
+bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, int64_t N, int64_t K, const void* A,
+                            int64_t lda, const void* B, bst_layout b_layout, int64_t ldb, int64_t stride_b, void* C,
+                            int64_t ldc, bst_dtype ab_type, bst_dtype c_type, const bst_sched* sched_in,
+                            void* stream_v) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups || total_m < 0 || N < 0 || K < 0 || stride_b < 0)
+        return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(total_m) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(K) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    if (ab_type != BST_F16 && ab_type != BST_BF16) return BST_ERR_UNSUPPORTED;
+    uint32_t c_code;
+    if (!out_code(c_type, c_code)) return BST_ERR_UNSUPPORTED;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
+    if (total_m == 0 || N == 0) return BST_OK;
+    if (!group_m || !C || (K > 0 && (!A || !B))) return BST_ERR_INVALID_ARG;
+    OperandSpec a, b;
+    if (bst_status s = make_specs(total_m, N, K, A, BST_ROW_MAJOR, lda, 0, B, b_layout, ldb, stride_b, 2, 1, a, b))
+        return s;
+    b.batch = static_cast<uint64_t>(G);
+    if (G > 1 && stride_b < 1) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const uint32_t csize = dtype_bytes(c_type);
+    if (K == 0)
+        return cuda_status(
+            launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, total_m, N, 1, csize, dev.sms, stream));
+    // an upper bound of the tile count: sum ceil(M_g/128) <= total_m/128 + G
+    const uint64_t loops_m_bound = (total_m + kBM - 1) / kBM + G;
+    const uint32_t bn = sch.tile_n ? sch.tile_n : choose_bn(loops_m_bound, N, dev.sms, true);
+    const uint64_t tiles_bound = loops_m_bound * ((N + bn - 1) / bn);
+    if (tiles_bound >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    if (smem_dense(bn, G) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, tmap_type(ab_type), false)) return s;
+    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, bn, tmap_type(ab_type), false)) return s;
+    p.M = 0; p.N = N; p.K = K;
+    p.batch = 1;
+    p.mode = kModeGrouped;
+    p.ab_fmt = ab_type == BST_BF16 ? 1u : 0u;
+    p.esize = 2;
+    p.swz_offset = sch.offset;
+    p.swz_dir = sch.dir;
+    p.num_kb = (K + 63) / 64;
+    p.chunk_kb = p.num_kb;
+    p.group_m = group_m;
+    p.G = static_cast<uint32_t>(G);
+    p.total_m = static_cast<uint32_t>(total_m);
+    p.C = static_cast<uint8_t*>(C);
+    p.ldc = ldc;
+    p.c_type = c_code;
+    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
+    p.trace = sch.trace;
+    p.trace_cap = static_cast<uint32_t>(tiles_bound);
+    p.err = dev.err;
+    p.timeout_ns = timeout_ns();
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles_bound));
+    return cuda_status(launch_dense(p, bn, grid, stream));
+}
+
+size_t bst_gemm_quant_per_token_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return 0;
+    const size_t kp = static_cast<size_t>((K + 7) / 8 * 8);
+    const size_t np = static_cast<size_t>((N + 7) / 8 * 8);
+    const size_t a = static_cast<size_t>(M) * kp * 2;
+    const size_t b = std::max(static_cast<size_t>(N) * kp, static_cast<size_t>(K) * np) * 2;
+    return round256(a) + round256(b);
+}
+
+bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda, const int8_t* B,
+                                    bst_layout b_layout, int64_t ldb, const float* scale_a, const float* scale_b,
+                                    void* C, int64_t ldc, int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                                    const bst_sched* sched_in, void* stream_v) {
+    if (M < 0 || N < 0 || K < 0) return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(M) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(K) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    if (b_layout != BST_ROW_MAJOR && b_layout != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (sch.tile_n != 0 && sch.tile_n != 128) return BST_ERR_UNSUPPORTED;
+    if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
+    if (lda < 1 || lda < K) return BST_ERR_INVALID_ARG;
+    if (ldb < 1 || ldb < (b_layout == BST_COL_MAJOR ? K : N)) return BST_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BST_OK;
+    if (!C || !scale_a || !scale_b || (K > 0 && (!A || !B))) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (K == 0) {
+        cudaError_t e = launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, M, N, 1, 2, dev.sms, stream);
+        if (e == cudaSuccess && acc_out)
+            e = launch_zero_fill(reinterpret_cast<uint8_t*>(acc_out), ldc, 0, M, N, 1, 4, dev.sms, stream);
+        return cuda_status(e);
+    }
+    const size_t need = bst_gemm_quant_per_token_workspace_size(M, N, K);
+    if (!workspace || workspace_bytes < need) return BST_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return BST_ERR_ALIGNMENT;
+    const int64_t kp = (K + 7) / 8 * 8;
+    const int64_t np = (N + 7) / 8 * 8;
+    uint16_t* wa = static_cast<uint16_t*>(workspace);
+    uint16_t* wb = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + round256(static_cast<size_t>(M) * kp * 2));
+    const bool b_kmajor = b_layout == BST_COL_MAJOR;   // stored [N, K]
+    const int64_t ldwb = b_kmajor ? kp : np;
+    const uint64_t loops_m = (M + kBM - 1) / kBM;
+    const uint64_t tiles = loops_m * ((N + 127) / 128);
+    if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    if (smem_dequant() > dev.max_smem) return BST_ERR_UNSUPPORTED;
+
+    cudaError_t e = launch_widen_s8_bf16(A, lda, wa, kp, M, K, dev.sms, stream);
+    if (e == cudaSuccess)
+        e = b_kmajor ? launch_widen_s8_bf16(B, ldb, wb, ldwb, N, K, dev.sms, stream)
+                     : launch_widen_s8_bf16(B, ldb, wb, ldwb, K, N, dev.sms, stream);
+    if (e != cudaSuccess) return BST_ERR_CUDA;
+
+    OperandSpec a{wa, 2, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kp, 0, 1, false};
+    OperandSpec b{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(K), ldwb, 0, 1, !b_kmajor};
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
+    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
+    p.M = M; p.N = N; p.K = K;
+    p.batch = 1;
+    p.mode = kModePlain;
+    p.ab_fmt = 1;
+    p.esize = 2;
+    p.swz_offset = sch.offset;
+    p.swz_dir = sch.dir;
+    p.num_kb = (K + 63) / 64;
+    p.chunk_kb = kDequantChunkK / 64;
+    p.total_tiles = static_cast<uint32_t>(tiles);
+    p.C = static_cast<uint8_t*>(C);
+    p.ldc = ldc;
+    p.c_type = kOutBF16;
+    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * 2) % 16 == 0) &&
+              (!acc_out || (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0));
+    p.scale_a = scale_a;
+    p.scale_b = scale_b;
+    p.acc_out = acc_out;
+    p.trace = sch.trace;
+    p.trace_cap = static_cast<uint32_t>(tiles);
+    p.err = dev.err;
+    p.timeout_ns = timeout_ns();
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
+    return cuda_status(launch_dequant(p, grid, stream));
+}
+
+bst_status bst_swizzle_map(uint32_t M, uint32_t N, uint32_t tile_m, uint32_t tile_n, uint32_t batch,
+                           const bst_sched* sched_in, uint32_t* out, void* stream) {
+    if (tile_m < 1 || tile_n < 1 || batch < 1) return BST_ERR_INVALID_ARG;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (M == 0 || N == 0) return BST_OK;
+    if (!out) return BST_ERR_INVALID_ARG;
+    const uint64_t lm = (static_cast<uint64_t>(M) + tile_m - 1) / tile_m;
+    const uint64_t ln = (static_cast<uint64_t>(N) + tile_n - 1) / tile_n;
+    const uint64_t total = lm * ln * batch;
+    if (total >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    SwizzleSched s;
+    s.update(M, N, tile_m, tile_n, sch.offset, sch.dir);
+    return cuda_status(launch_swizzle_map(s, static_cast<uint32_t>(total), out, static_cast<cudaStream_t>(stream)));
+}
+
+bst_status bst_swizzle_map_grouped(int32_t G, const int32_t* group_m, uint32_t N, uint32_t tile_m, uint32_t tile_n,
+                                   const bst_sched* sched_in, uint32_t* out, uint32_t max_tasks, void* stream) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups || tile_m < 1 || tile_n < 1) return BST_ERR_INVALID_ARG;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (N == 0) return BST_OK;
+    if (!group_m || (!out && max_tasks > 0)) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    return cuda_status(launch_swizzle_map_grouped(group_m, static_cast<uint32_t>(G), N, tile_m, tile_n, sch.offset,
+                                                  sch.dir, out, max_tasks, dev.err,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+bst_status bst_check_async(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return BST_ERR_CUDA;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    uint32_t w[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(w, dev.err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BST_ERR_CUDA;
+    if (w[0] == 0) return BST_OK;
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(dev.err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return BST_ERR_CUDA;
+    return (w[0] & kErrTimeout) ? BST_ERR_TIMEOUT : BST_ERR_DEVICE;
+}
+
+const char* bst_status_string(bst_status s) {
+    switch (s) {
+        case BST_OK: return "ok";
+        case BST_ERR_INVALID_ARG: return "invalid argument";
+        case BST_ERR_UNSUPPORTED: return "unsupported dtype, layout or device";
+        case BST_ERR_ALIGNMENT: return "address or stride not aligned for this path";
+        case BST_ERR_CUDA: return "CUDA error";
+        case BST_ERR_TIMEOUT: return "device-side wait timed out";
+        case BST_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+void bst_set_wait_timeout_ns(uint64_t ns) { t_timeout_ns = ns; }
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// fp16 / bf16 GEMM instantiations (plain, batched and grouped share them; the
+// mode is a run-time field of GemmParams).
+#include "internal.h"
+
+namespace bst {
+
+template <uint32_t BN, uint32_t STAGES>
+static cudaError_t launch_one(const GemmParams& p, uint32_t grid, cudaStream_t stream) {
+    using Lay = GemmLayout<BN, STAGES, 2, kKindF16>;
+    static std::atomic<uint64_t> attr_done{0};
+    auto kern = gemm_kernel<BN, STAGES, 2, kKindF16, kEpiStore>;
+    const uint32_t smem = Lay::smem_bytes(p.mode == kModeGrouped ? p.G : 0);
+    // the limit is set once for the largest group table any call can need
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(kMaxGroups), attr_done);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kNumThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream) {
+    switch (bn) {
+        case 64: return launch_one<64, kDenseStages64>(p, grid, stream);
+        case 128: return launch_one<128, kDenseStages128>(p, grid, stream);
+        case 256: return launch_one<256, kDenseStages256>(p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+uint32_t smem_dense(uint32_t bn, uint32_t groups) {
+    switch (bn) {
+        case 64: return GemmLayout<64, kDenseStages64, 2, kKindF16>::smem_bytes(groups);
+        case 128: return GemmLayout<128, kDenseStages128, 2, kKindF16>::smem_bytes(groups);
+        case 256: return GemmLayout<256, kDenseStages256, 2, kKindF16>::smem_bytes(groups);
+        default: return 0xFFFFFFFFu;
+    }
+}
+
+}  // namespace bst

@@ -1,0 +1,71 @@
+// int8 GEMM with per-token dequant ("Block Dispatch Policies",
+// 12_quant_matmul).
+//
+// sm_103a has no int8 tcgen05 MMA, so the product is formed exactly on the
+// bf16 tensor cores: every int8 value is exact in bf16, every product of two
+// (|p| <= 127*127 = 16129) is exact in fp32, and a sum of at most 1024 of them
+// stays below 1024*16129 < 2^24, where every integer is exact in fp32.  The
+// MMA therefore accumulates K-chunks of 1024 in TMEM; the epilogue converts
+// each chunk to int32 and carries the running sum in registers, then applies
+// scale_a[row] * scale_b[col] once at the end.
+#include "internal.h"
+
+namespace bst {
+
+cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stream) {
+    using Lay = GemmLayout<128, kDequantStages, 2, kKindF16>;
+    static std::atomic<uint64_t> attr_done{0};
+    auto kern = gemm_kernel<128, kDequantStages, 2, kKindF16, kEpiDequant>;
+    const uint32_t smem = Lay::smem_bytes(0);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, attr_done);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kNumThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+uint32_t smem_dequant() { return GemmLayout<128, kDequantStages, 2, kKindF16>::smem_bytes(0); }
+
+// Widens int8 to bf16, 16 elements per thread per step when the rows allow
+// 16-byte loads, element by element otherwise.  Bandwidth bound.
+__global__ void widen_s8_bf16_kernel(const int8_t* __restrict__ src, int64_t ld_src, uint16_t* __restrict__ dst,
+                                     int64_t ld_dst, int64_t rows, int64_t cols, int vec) {
+    const int64_t chunks_per_row = vec ? cols / 16 : 0;
+    const int64_t total_vec = rows * chunks_per_row;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total_vec; i += stride) {
+        const int64_t r = i / chunks_per_row;
+        const int64_t c = (i - r * chunks_per_row) * 16;
+        const int4 raw = __ldg(reinterpret_cast<const int4*>(src + r * ld_src + c));
+        const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(b[2 * j]), static_cast<float>(b[2 * j + 1]));
+            w[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        uint4* d = reinterpret_cast<uint4*>(dst + r * ld_dst + c);
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    // columns not covered by 16-wide chunks
+    const int64_t tail0 = chunks_per_row * 16;
+    const int64_t tail_cols = cols - tail0;
+    const int64_t total_tail = rows * tail_cols;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total_tail; i += stride) {
+        const int64_t r = i / tail_cols;
+        const int64_t c = tail0 + (i - r * tail_cols);
+        const __nv_bfloat16 h = __float2bfloat16_rn(static_cast<float>(src[r * ld_src + c]));
+        dst[r * ld_dst + c] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+}
+
+cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
+                                 int64_t cols, uint32_t sms, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld_src % 16 == 0) &&
+                    (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (ld_dst % 8 == 0);
+    widen_s8_bf16_kernel<<<sms * 4, 256, 0, stream>>>(src, ld_src, dst, ld_dst, rows, cols, vec);
+    return cudaGetLastError();
+}
+
+}  // namespace bst

@@ -1,0 +1,57 @@
+// Host-side interface between the C-ABI layer (api.cu) and the translation
+// units that instantiate the kernels.  Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "gemm_kernel.cuh"
+
+namespace bst {
+
+// Raises a kernel's dynamic shared-memory limit once per device (bit `dev`
+// of `done`), so that later launches -- including ones recorded into a CUDA
+// graph -- make no attribute call.
+inline cudaError_t set_smem_once(const void* kern, uint32_t bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// Kernel launches.  Each returns the cudaError_t of the launch (attribute
+// setting included); `grid` CTAs of kNumThreads threads on `stream`.
+cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
+cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
+cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stream);
+
+// Shared-memory bytes a launch needs (for validation of the device limit).
+uint32_t smem_dense(uint32_t bn, uint32_t groups);
+uint32_t smem_mxf8(uint32_t bn);
+uint32_t smem_dequant();
+
+// int8 [rows, cols] (ld_src elements) -> bf16 [rows, cols] (ld_dst elements)
+cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
+                                 int64_t cols, uint32_t sms, cudaStream_t stream);
+
+// zero an [rows, cols] row-major output of `esize`-byte elements, `batch`
+// times at `batch_stride` elements apart
+cudaError_t launch_zero_fill(uint8_t* C, int64_t ldc, int64_t batch_stride, int64_t rows, int64_t cols,
+                             int64_t batch, uint32_t esize, uint32_t sms, cudaStream_t stream);
+
+cudaError_t launch_swizzle_map(const SwizzleSched& s, uint32_t total, uint32_t* out, cudaStream_t stream);
+cudaError_t launch_swizzle_map_grouped(const int32_t* group_m, uint32_t G, uint32_t N, uint32_t tile_m,
+                                       uint32_t tile_n, uint32_t offset, uint32_t dir, uint32_t* out,
+                                       uint32_t max_tasks, uint32_t* err, cudaStream_t stream);
+
+// Configurations instantiated for each kernel family.
+constexpr uint32_t kDenseStages64 = 8, kDenseStages128 = 6, kDenseStages256 = 4;
+constexpr uint32_t kMxStages128 = 6, kMxStages256 = 4;
+constexpr uint32_t kDequantStages = 6;
+constexpr uint32_t kDequantChunkK = 1024;  // K elements per exact fp32 chunk
+
+}  // namespace bst

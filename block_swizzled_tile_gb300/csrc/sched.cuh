@@ -1,0 +1,97 @@
+// Device tile scheduler: the task index -> output tile mapping of
+// GemmIdentityBlockSwizzle ("Block Scheduler Code Explained", sections 4.3
+// GetCoreLoops, 4.4 GetBatchIdx, 4.5 GetBlockCoord, 4.6 GetActualBlockShape,
+// 5 Scheduling Policies, 6 DynamicGemmIdentityBlockSwizzle), with the offset
+// and direction chosen at run time as in the dynamic variant.
+//
+// Differences from the page's code, none of which changes the map:
+//  * the offset is clamped to the number of tile-rows (Zn) / tile-columns
+//    (Nz).  With SwizzleOffset >= loopsM there is a single window whose height
+//    is loopsM, so the map is the same; the clamp keeps offset * loops inside
+//    32 bits for any offset the caller passes.
+//  * the Nz branch, elided on the page, is the transpose of Zn: windows of
+//    SwizzleOffset tile-columns, n fastest inside a window, m reversed on odd
+//    windows (the page's prose: "divided by column", "reverses the N-dimension
+//    or M-dimension index").
+#pragma once
+#include <cstdint>
+
+namespace bst {
+
+struct SwizzleSched {
+    uint32_t M, N;            // problem extent (elements)
+    uint32_t tile_m, tile_n;  // tile extent (elements)
+    uint32_t loops_m, loops_n;
+    uint32_t offset;          // SwizzleOffset after the clamp
+    uint32_t direction;       // 0 Zn, 1 Nz
+
+    __host__ __device__ static uint32_t ceil_div(uint32_t a, uint32_t b) { return (a + b - 1) / b; }
+
+    // constructor + Update (sections 4.1, 4.2): loop counts by ceiling division
+    __host__ __device__ void update(uint32_t M_, uint32_t N_, uint32_t tm, uint32_t tn, uint32_t swz_offset,
+                                    uint32_t swz_dir) {
+        M = M_;
+        N = N_;
+        tile_m = tm;
+        tile_n = tn;
+        loops_m = ceil_div(M_, tm);
+        loops_n = ceil_div(N_, tn);
+        direction = swz_dir;
+        const uint32_t lim = swz_dir == 0 ? loops_m : loops_n;
+        offset = swz_offset < lim ? swz_offset : (lim > 0 ? lim : 1);
+    }
+
+    __host__ __device__ uint32_t core_loops() const { return loops_m * loops_n; }       // section 4.3
+    __host__ __device__ uint32_t batch_idx(uint32_t t) const { return t / core_loops(); }  // section 4.4
+
+    // section 4.5
+    __host__ __device__ void block_coord(uint32_t t, uint32_t& m, uint32_t& n) const {
+        const uint32_t inner = t % core_loops();
+        const uint32_t S = offset;
+        if (direction == 0) {
+            const uint32_t per_window = S * loops_n;
+            const uint32_t window = inner / per_window;
+            const uint32_t pos = inner - window * per_window;
+            const uint32_t last = ceil_div(loops_m, S) - 1;
+            const uint32_t h = window == last ? loops_m - S * window : S;
+            m = window * S + pos % h;
+            n = pos / h;
+            if (window & 1u) n = loops_n - 1 - n;
+        } else {
+            const uint32_t per_window = S * loops_m;
+            const uint32_t window = inner / per_window;
+            const uint32_t pos = inner - window * per_window;
+            const uint32_t last = ceil_div(loops_n, S) - 1;
+            const uint32_t w = window == last ? loops_n - S * window : S;
+            n = window * S + pos % w;
+            m = pos / w;
+            if (window & 1u) m = loops_m - 1 - m;
+        }
+    }
+
+    // section 4.6 (kActual is always the whole K)
+    __host__ __device__ void actual_shape(uint32_t m, uint32_t n, uint32_t& m_act, uint32_t& n_act) const {
+        m_act = m == loops_m - 1 ? M - m * tile_m : tile_m;
+        n_act = n == loops_n - 1 ? N - n * tile_n : tile_n;
+    }
+};
+
+// Grouped slice-M: per-group tile offsets (group-major task numbering) and row
+// offsets, as exclusive prefix sums of the group sizes.  Filled once per CTA
+// in shared memory; `find` maps a task to its group by binary search.
+struct GroupTable {
+    uint32_t* tile_off;   // [G+1]
+    uint32_t* row_off;    // [G+1]
+    uint32_t G;
+
+    __device__ uint32_t find(uint32_t t) const {
+        uint32_t lo = 0, hi = G;  // invariant: tile_off[lo] <= t < tile_off[hi]
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (tile_off[mid] <= t) lo = mid; else hi = mid;
+        }
+        return lo;
+    }
+};
+
+}  // namespace bst

@@ -1,0 +1,222 @@
+/*
+ * bst.h -- block-swizzled tile GEMM for GB300 (sm_103a), C ABI.
+ *
+ * What the library computes is the dense contraction C = A.B with fp32
+ * accumulation, in the variants named in "Block Dispatch Policies" (CATLASS
+ * docs: examples 00_basic_matmul, 01_batched_matmul,
+ * 02_grouped_matmul_slice_m, 12_quant_matmul) and the MXFP8 GEMM of "MI450
+ * WMMA and ds_load Scheduling via a DAG Mutation" ("An example run on a real
+ * kernel").  Output tiles are handed to persistent CTAs in the order of
+ * GemmIdentityBlockSwizzle ("Block Scheduler Code Explained", sections 4-7):
+ * windows of SwizzleOffset tile-rows (Zn) or tile-columns (Nz), reversed on
+ * odd windows, tail tiles cut by GetActualBlockShape.
+ *
+ * Conventions for every entry point:
+ *  - Matrices are dense 2-D (or 3-D batched/grouped) arrays in DEVICE memory
+ *    owned by the caller; the library never allocates, frees or keeps them.
+ *    A is logically [M, K], B is logically [K, N], C is [M, N] row-major.
+ *    bst_layout says how an operand is stored: BST_ROW_MAJOR means element
+ *    (r, c) of the logical matrix is at r*ld + c, BST_COL_MAJOR at c*ld + r.
+ *    Leading dimensions and strides are in ELEMENTS.
+ *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) of the CURRENT device.  An argument error
+ *    returns before anything is enqueued.  Device-side failures (a bounded
+ *    wait that gave up, inconsistent group sizes) are recorded in a per-device
+ *    error word and reported by bst_check_async.
+ *  - Operands whose base address and leading dimension are 16-byte aligned
+ *    are fetched with TMA; others are fetched with ordinary loads (slower,
+ *    same results).  There is no CPU fallback: without a usable sm_103a
+ *    device the call returns BST_ERR_CUDA.
+ *  - Empty outputs (M == 0 or N == 0) return BST_OK without a launch; K == 0
+ *    writes zeros.
+ *  - The library holds no mutable host state except cached device properties,
+ *    so calls from several host threads are safe.
+ */
+#ifndef BST_H
+#define BST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BST_OK = 0,
+    BST_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, ...   */
+    BST_ERR_UNSUPPORTED = 2,   /* a dtype/layout combination not implemented   */
+    BST_ERR_ALIGNMENT = 3,     /* an address or stride the path cannot take   */
+    BST_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed            */
+    BST_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up           */
+    BST_ERR_DEVICE = 6         /* a device-side consistency check failed       */
+} bst_status;
+
+typedef enum {
+    BST_F16 = 0,   /* IEEE binary16                                  */
+    BST_BF16 = 1,  /* bfloat16                                       */
+    BST_E4M3 = 2,  /* float8 e4m3 ("fn": no infinities, 0x7F NaN)    */
+    BST_S8 = 3,    /* int8                                           */
+    BST_F32 = 4,   /* IEEE binary32                                  */
+    BST_S32 = 5    /* int32                                          */
+} bst_dtype;
+
+typedef enum { BST_ROW_MAJOR = 0, BST_COL_MAJOR = 1 } bst_layout;
+
+/*
+ * Scheduling parameters ("Block Scheduler Code Explained" section 2.1 and
+ * section 6, DynamicGemmIdentityBlockSwizzle::SetSwizzleParams).  A NULL
+ * bst_sched* means: offset 1, Zn, automatic tile and grid.
+ */
+typedef struct {
+    uint32_t swizzle_offset;    /* SwizzleOffset, >= 1 (0 is rejected)                 */
+    uint32_t swizzle_direction; /* SwizzleDirection: 0 = Zn, 1 = Nz                    */
+    uint32_t tile_n;            /* 0 = automatic, else 64, 128 or 256 (tile_m is 128)  */
+    uint32_t num_ctas;          /* persistent CTAs; 0 = one per SM                      */
+    uint32_t* trace;            /* optional DEVICE buffer of 5 uint32 per task; when
+                                   non-NULL the kernel writes, for task index t, the
+                                   tile it computed: {batch or group, m, n, mActual,
+                                   nActual}.  Debug only.                             */
+} bst_sched;
+
+/*
+ * bst_gemm -- C[M,N] = A[M,K] . B[K,N] ("Block Dispatch Policies",
+ * 00_basic_matmul), accumulated in fp32, rounded once to the type of C.
+ *
+ *   a_type == b_type == BST_F16 or BST_BF16: c_type BST_F16, BST_BF16 or
+ *     BST_F32; any layout for A and B; scale_a/scale_b must be NULL.
+ *   a_type == b_type == BST_E4M3 (MXFP8): A row-major, B column-major (both
+ *     K-contiguous), K a multiple of 128, c_type BST_BF16, BST_F16 or
+ *     BST_F32; scale_a [M, K/32] and scale_b [N, K/32] are dense row-major
+ *     E8M0 codes (value 2^(s-127)), one per 32 consecutive K elements of a
+ *     row of A / a column of B.
+ * ldc >= N.  C must not overlap A or B.
+ * Returns BST_OK once the launch is enqueued.
+ */
+bst_status bst_gemm(int64_t M, int64_t N, int64_t K,
+                    const void* A, bst_dtype a_type, bst_layout a_layout, int64_t lda,
+                    const void* B, bst_dtype b_type, bst_layout b_layout, int64_t ldb,
+                    void* C, bst_dtype c_type, int64_t ldc,
+                    const uint8_t* scale_a, const uint8_t* scale_b,
+                    const bst_sched* sched, void* stream);
+
+/*
+ * bst_gemm_batched -- `batch` independent bst_gemm problems of one shape
+ * ("Block Dispatch Policies", 01_batched_matmul; task t belongs to batch
+ * t / (loopsM*loopsN), "Block Scheduler Code Explained" section 4.4
+ * GetBatchIdx).  Problem i uses A + i*stride_a, B + i*stride_b,
+ * C + i*stride_c (strides in elements; for TMA they must be 16-byte
+ * multiples).  fp16/bf16 operands only.
+ */
+bst_status bst_gemm_batched(int64_t M, int64_t N, int64_t K,
+                            const void* A, bst_dtype a_type, bst_layout a_layout, int64_t lda, int64_t stride_a,
+                            const void* B, bst_dtype b_type, bst_layout b_layout, int64_t ldb, int64_t stride_b,
+                            void* C, bst_dtype c_type, int64_t ldc, int64_t stride_c,
+                            int64_t batch, const bst_sched* sched, void* stream);
+
+/*
+ * bst_gemm_grouped -- grouped GEMM with groups along M ("Block Dispatch
+ * Policies", 02_grouped_matmul_slice_m).  Group g owns the M_g consecutive
+ * rows [off_g, off_g + M_g) of A and of C, off_g = M_0 + ... + M_{g-1}, and
+ * multiplies them by its own B_g:
+ *
+ *   C[off_g + i, :] = A[off_g + i, :] . B_g      for 0 <= i < M_g.
+ *
+ * group_m  DEVICE int32[G] of group sizes (>= 0; zero-size groups own no
+ *          rows).  The host never reads it, so no synchronisation is implied.
+ * total_m  rows of the A and C buffers; the kernel checks sum(M_g) <= total_m
+ *          and otherwise computes nothing and records BST_ERR_DEVICE.
+ * A        [total_m, K] row-major (lda).
+ * B        G matrices; b_layout BST_ROW_MAJOR: B_g is [K, N] at
+ *          B + g*stride_b with leading dimension ldb (N contiguous);
+ *          BST_COL_MAJOR: stored [N, K] (K contiguous).
+ * C        [total_m, N] row-major (ldc); rows past sum(M_g) are not written.
+ * dtype    BST_F16 or BST_BF16 for A and B; c_type BST_F16, BST_BF16, BST_F32.
+ * Tasks are numbered group-major and the swizzle restarts in each group, as
+ * "Block Scheduler Code Explained" section 4.2 (Update) re-targets the
+ * scheduler to (M_g, N, K).  G <= 1024.
+ */
+bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m,
+                            int64_t N, int64_t K,
+                            const void* A, int64_t lda,
+                            const void* B, bst_layout b_layout, int64_t ldb, int64_t stride_b,
+                            void* C, int64_t ldc,
+                            bst_dtype ab_type, bst_dtype c_type,
+                            const bst_sched* sched, void* stream);
+
+/*
+ * bst_gemm_quant_per_token -- int8 GEMM with per-token dequant ("Block
+ * Dispatch Policies", 12_quant_matmul):
+ *
+ *   acc[i,j] = sum_k A[i,k] * B[k,j]          exactly, in int32
+ *   C[i,j]   = bf16( acc[i,j] * scale_a[i] * scale_b[j] )    (fp32 products)
+ *
+ * A int8 [M, K] row-major (lda); B int8 with b_layout (BST_COL_MAJOR: stored
+ * [N, K], the usual weight layout).  scale_a fp32 [M] (one per row/token),
+ * scale_b fp32 [N] (one per output column).  C bf16 [M, N] (ldc).
+ * acc_out: optional int32 [M, N] row-major with leading dimension ldc that
+ * receives the exact accumulators (NULL = not written).
+ * workspace: DEVICE scratch of at least
+ * bst_gemm_quant_per_token_workspace_size(M, N, K) bytes, 256-byte aligned,
+ * owned by the caller and not read after the call's kernels finish; calls
+ * that share one workspace must be ordered on one stream.  The operands are
+ * widened to bf16 there (every int8 is exact in bf16) and multiplied on the
+ * tensor cores in K-chunks of at most 1024, each chunk's fp32 sum being an
+ * exact integer below 2^24, carried into int32.
+ */
+size_t bst_gemm_quant_per_token_workspace_size(int64_t M, int64_t N, int64_t K);
+
+bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K,
+                                    const int8_t* A, int64_t lda,
+                                    const int8_t* B, bst_layout b_layout, int64_t ldb,
+                                    const float* scale_a, const float* scale_b,
+                                    void* C, int64_t ldc, int32_t* acc_out,
+                                    void* workspace, size_t workspace_bytes,
+                                    const bst_sched* sched, void* stream);
+
+/*
+ * bst_swizzle_map -- debug entry: runs the device scheduler the GEMM kernels
+ * use ("Block Scheduler Code Explained" sections 4.3-4.6) for every task of a
+ * (possibly batched) problem and writes, for task t, the 5 uint32
+ * {GetBatchIdx, mIdx, nIdx, mActual, nActual} to out[5*t .. 5*t+4].
+ * out is a DEVICE buffer of 5 * batch * ceil(M/tile_m) * ceil(N/tile_n)
+ * uint32.  Any tile sizes >= 1 are accepted.  The task count must be < 2^32.
+ */
+bst_status bst_swizzle_map(uint32_t M, uint32_t N, uint32_t tile_m, uint32_t tile_n,
+                           uint32_t batch, const bst_sched* sched,
+                           uint32_t* out, void* stream);
+
+/*
+ * bst_swizzle_map_grouped -- the same for a grouped slice-M problem: group
+ * sizes are read from DEVICE int32 group_m[G]; task t (group-major) gets
+ * {group, mIdx, nIdx, mActual, nActual}.  out holds max_tasks rows; tasks
+ * past max_tasks are not written (bst_check_async then reports
+ * BST_ERR_DEVICE).
+ */
+bst_status bst_swizzle_map_grouped(int32_t G, const int32_t* group_m, uint32_t N,
+                                   uint32_t tile_m, uint32_t tile_n, const bst_sched* sched,
+                                   uint32_t* out, uint32_t max_tasks, void* stream);
+
+/*
+ * bst_check_async -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns BST_ERR_TIMEOUT if a kernel's bounded
+ * wait gave up, BST_ERR_DEVICE if a device-side check failed, BST_ERR_CUDA
+ * if the stream reported an error, else BST_OK.
+ */
+bst_status bst_check_async(void* stream);
+
+/* A short static English description of a status code. */
+const char* bst_status_string(bst_status s);
+
+/*
+ * bst_set_wait_timeout_ns -- limit, in nanoseconds, on every device-side
+ * wait of kernels launched afterwards by this thread (0 = the default of
+ * 4 s).  Used by tests to make a wait that cannot complete give up quickly.
+ */
+void bst_set_wait_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BST_H */

@@ -1,0 +1,195 @@
+"""GPU parity of the fp16/bf16 path (bst_gemm, bst_gemm_batched) and of the
+device scheduler (bst_swizzle_map) against the CPU oracle."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import block_swizzled_tile_gb300 as bst
+from block_swizzled_tile_gb300 import workloads as wl
+from oracle import gemm as og, swizzle as osw
+from tests.gpu_util import (DT, OUT_BYTES, assert_close_f16, canary_intact, decode_out, dev, empty_bytes, host)
+from tests.swizzle_checks import check_map
+
+pytestmark = pytest.mark.gpu
+CANARY = 256
+
+
+def _layout(col):
+    return bst.COL_MAJOR if col else bst.ROW_MAJOR
+
+
+def run_dense(w, out="f16", sched=None, ldc=None):
+    M, N, K, dt = w["M"], w["N"], w["K"], w["dtype"]
+    ldc = N if ldc is None else ldc
+    A = dev(w["a"])
+    B = dev(w["b"])
+    cbuf, C = empty_bytes(max(M * ldc, 1) * OUT_BYTES[out], CANARY)
+    bst.gemm(M, N, K, A, DT[dt], _layout(w["a_col_major"]), w["lda"], B, DT[dt], _layout(w["b_col_major"]),
+             w["ldb"], C, DT[out], ldc, sched=sched)
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY), "write outside C"
+    raw = host(C, np.uint8).view(np.float32 if out == "f32" else np.uint16).reshape(M, ldc)[:, :N]
+    return decode_out(raw.copy(), out)
+
+
+def oracle_dense(w, out="f16"):
+    M, N, K, dt = w["M"], w["N"], w["K"], w["dtype"]
+    a = og.as_logical(og.decode(w["a"], dt), M, K, w["lda"], w["a_col_major"])
+    b = og.as_logical(og.decode(w["b"], dt), K, N, w["ldb"], w["b_col_major"])
+    return decode_out(og.gemm(a, b, out), out)
+
+
+# ------------------------------------------------------------ scheduler ---
+
+MAP_SHAPES = [(500, 380, 128, 128, 1), (1024, 1024, 128, 64, 1), (8192, 8192, 128, 256, 1),
+              (129, 2000, 128, 64, 3), (48, 74, 16, 16, 2), (1, 1, 128, 128, 1), (1000, 37, 16, 8, 1)]
+
+
+@pytest.mark.parametrize("shape", MAP_SHAPES)
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 9, 100000])
+@pytest.mark.parametrize("d", [0, 1])
+def test_swizzle_map_bit_exact(shape, S, d):
+    M, N, tm, tn, batch = shape
+    want = np.array(osw.swizzle_map(M, N, tm, tn, S, d, batch=batch), dtype=np.uint32)
+    out = torch.zeros(want.size, dtype=torch.int32, device="cuda")
+    bst.swizzle_map(M, N, tm, tn, batch, bst.sched(S, d), out)
+    bst.check_async()
+    got = out.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(got, want)
+    core = len(want) // batch
+    assert check_map([tuple(r[1:]) for r in got[:core]], M, N, tm, tn, S, d) == []
+
+
+@pytest.mark.parametrize("gm", [[0, 300, 0, 129, 1, 0, 1024], [8192], [0, 0, 5], [1] * 40])
+@pytest.mark.parametrize("S,d", [(1, 0), (2, 0), (3, 1), (8, 1)])
+def test_swizzle_map_grouped_bit_exact(gm, S, d):
+    N, tm, tn = 700, 128, 128
+    want = np.array(osw.grouped_swizzle_map(gm, N, tm, tn, S, d), dtype=np.uint32).reshape(-1, 5)
+    gdev = torch.tensor(gm, dtype=torch.int32, device="cuda")
+    cap = max(len(want), 1)
+    out = torch.full((cap * 5,), -1, dtype=torch.int32, device="cuda")
+    bst.swizzle_map_grouped(len(gm), gdev, N, tm, tn, bst.sched(S, d), out, cap)
+    bst.check_async()
+    got = out.cpu().numpy().view(np.uint32).reshape(-1, 5)[:len(want)]
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------- fp16 tail ------
+
+@pytest.mark.parametrize("d", [0, 1])
+def test_fp16_tail_workload(d):
+    """fp16 500x380x256 row-major A and B, 128x128 tiles, SwizzleOffset 3."""
+    w = wl.fp16_tail()
+    ntiles = 4 * 3
+    trace = torch.zeros(ntiles * 5, dtype=torch.int32, device="cuda")
+    got = run_dense(w, "f16", bst.sched(3, d, tile_n=128, trace=trace))
+    assert_close_f16(got, oracle_dense(w, "f16"))
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(500, 380, 128, 128, 3, d), dtype=np.uint32))
+
+
+# -------------------------------------------------------- fp16 square ------
+
+@pytest.mark.parametrize("S", [1, 2, 4, 8])
+@pytest.mark.parametrize("d", [0, 1])
+def test_fp16_square_workload(S, d):
+    """fp16 1024x1024x2048, A row-major, B column-major, N(0,1)/sqrt(K)."""
+    w = wl.fp16_square()
+    got = run_dense(w, "f16", bst.sched(S, d))
+    assert_close_f16(got, oracle_dense(w, "f16"))
+
+
+def test_fp16_square_trace_per_tile_width():
+    w = wl.fp16_square()
+    ref = oracle_dense(w, "f16")
+    for tn in (64, 128, 256):
+        tiles = 8 * (1024 // tn)
+        trace = torch.zeros(tiles * 5, dtype=torch.int32, device="cuda")
+        got = run_dense(w, "f16", bst.sched(2, 0, tile_n=tn, trace=trace))
+        assert_close_f16(got, ref)
+        tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+        assert np.array_equal(tr, np.array(osw.swizzle_map(1024, 1024, 128, tn, 2, 0), dtype=np.uint32))
+
+
+# ------------------------------------------------- shapes and layouts ------
+
+SMALL = [(1, 1, 16), (127, 129, 72), (128, 128, 64), (129, 127, 200), (500, 64, 256), (64, 500, 24),
+         (257, 300, 1000)]
+
+
+@pytest.mark.parametrize("mnk", SMALL)
+@pytest.mark.parametrize("acol,bcol", [(False, False), (False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_small_shapes_layouts(mnk, acol, bcol, dt):
+    M, N, K = mnk
+    w = wl.dense16(M, N, K, dt, a_col_major=acol, b_col_major=bcol, seed=M * 7 + N + K)
+    for tn in (64, 128, 256):
+        got = run_dense(w, dt, bst.sched(2, 0, tile_n=tn))
+        assert_close_f16(got, oracle_dense(w, dt))
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16", "f32"])
+def test_output_types(out):
+    w = wl.dense16(300, 260, 320, "bf16", seed=3)
+    got = run_dense(w, out, bst.sched(1, 1))
+    assert_close_f16(got, oracle_dense(w, out))
+
+
+@pytest.mark.parametrize("lda_pad,ldb_pad,ldc_pad", [(3, 0, 0), (0, 5, 0), (1, 1, 3), (8, 8, 8)])
+def test_padded_and_unaligned_leading_dims(lda_pad, ldb_pad, ldc_pad):
+    """Odd leading dimensions take the ordinary-load path (TMA needs 16-byte
+    pitches); both paths must give the same result."""
+    M, N, K = 200, 190, 136
+    w = wl.dense16(M, N, K, "f16", b_col_major=False, seed=5, lda=K + lda_pad, ldb=N + ldb_pad)
+    got = run_dense(w, "f16", bst.sched(3, 0), ldc=N + ldc_pad)
+    assert_close_f16(got, oracle_dense(w, "f16"))
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    w = wl.dense16(70, 50, 0, "f16", seed=1, lda=1)
+    got = run_dense(w, "f32")
+    assert not got.any()
+    cbuf, C = empty_bytes(64, CANARY)
+    bst.gemm(0, 10, 10, None, bst.F16, bst.ROW_MAJOR, 10, None, bst.F16, bst.ROW_MAJOR, 10, C, bst.F16, 10)
+    bst.gemm(10, 0, 10, None, bst.F16, bst.ROW_MAJOR, 10, None, bst.F16, bst.ROW_MAJOR, 10, C, bst.F16, 10)
+    bst.check_async()
+    assert (C == 0x5A).all().item()
+
+
+def test_special_values_identity_and_zero():
+    M = 256
+    eye = np.eye(M, dtype=np.float16).view(np.uint16)
+    w = wl.dense16(M, M, M, "f16", seed=2)
+    w_id = dict(w, b=eye, ldb=M, b_col_major=False)
+    got = run_dense(w_id, "f16")
+    assert np.array_equal(got, decode_out(w["a"].copy(), "f16"))   # A.I == A exactly
+    w_zero = dict(w, b=np.zeros_like(eye))
+    assert not run_dense(w_zero, "f32").any()
+
+
+# ------------------------------------------------------------- batched -----
+
+@pytest.mark.parametrize("acol,bcol", [(False, True), (True, False)])
+def test_batched(acol, bcol):
+    M, N, K, batch = 200, 136, 264, 3
+    w = wl.dense16(M, N, K, "bf16", a_col_major=acol, b_col_major=bcol, seed=9, batch=batch)
+    A = dev(w["a"])
+    B = dev(w["b"])
+    sa = w["a"][0].size
+    sb = w["b"][0].size
+    cbuf, C = empty_bytes(batch * M * N * 2, CANARY)
+    trace_tiles = batch * 2 * 2
+    trace = torch.zeros(trace_tiles * 5, dtype=torch.int32, device="cuda")
+    bst.gemm_batched(M, N, K, A, bst.BF16, _layout(acol), w["lda"], sa, B, bst.BF16, _layout(bcol), w["ldb"], sb,
+                     C, bst.BF16, N, M * N, batch, sched=bst.sched(1, 0, tile_n=128, trace=trace))
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY)
+    got = decode_out(host(C, np.uint16).reshape(batch, M, N).copy(), "bf16")
+    for i in range(batch):
+        a = og.as_logical(og.decode(w["a"][i], "bf16"), M, K, w["lda"], acol)
+        b = og.as_logical(og.decode(w["b"][i], "bf16"), K, N, w["ldb"], bcol)
+        assert_close_f16(got[i], decode_out(og.gemm(a, b, "bf16"), "bf16"))
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, 128, 1, 0, batch=batch), dtype=np.uint32))

@@ -1,0 +1,205 @@
+"""GPU parity of the grouped slice-M, MXFP8 and int8 per-token-dequant paths
+against the CPU oracle, at small ragged sizes and at the full workload sizes
+(full sizes compare a seeded sample of whole output rows)."""
+import numpy as np
+import pytest
+import torch
+
+import block_swizzled_tile_gb300 as bst
+from block_swizzled_tile_gb300 import workloads as wl
+from oracle import formats, gemm as og, swizzle as osw
+from tests.gpu_util import (FRO_MX, assert_close_f16, assert_close_fro, canary_intact, decode_out, dev,
+                            empty_bytes, host)
+
+pytestmark = pytest.mark.gpu
+CANARY = 256
+
+
+# ------------------------------------------------------------- grouped -----
+
+def run_grouped(w, sched=None, b_col_major=False, out="bf16"):
+    gm, N, K = w["group_m"], w["N"], w["K"]
+    G = len(gm)
+    total = sum(gm)
+    X = dev(w["x"])
+    W = w["w"]
+    if b_col_major:                                   # store each B_g as [N, K]
+        W = np.ascontiguousarray(np.transpose(W, (0, 2, 1)))
+    Wd = dev(W)
+    gdev = torch.tensor(gm, dtype=torch.int32, device="cuda")
+    ob = 4 if out == "f32" else 2
+    cbuf, C = empty_bytes(max(total, 1) * N * ob, CANARY)
+    bst.gemm_grouped(G, gdev, total, N, K, X, K, Wd, bst.COL_MAJOR if b_col_major else bst.ROW_MAJOR,
+                     K if b_col_major else N, K * N, C, N, bst.BF16, {"bf16": bst.BF16, "f32": bst.F32}[out],
+                     sched=sched)
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY)
+    raw = host(C, np.uint8).view(np.float32 if out == "f32" else np.uint16).reshape(-1, N)[:total]
+    return decode_out(raw.copy(), out)
+
+
+def oracle_grouped_rows(w, rows, out="bf16"):
+    """Oracle output for the given global rows: row i of group g is
+    round(x[i] . w[g])."""
+    gm = w["group_m"]
+    off = np.concatenate([[0], np.cumsum(gm)])
+    x = og.decode(w["x"], "bf16")
+    res = np.zeros((len(rows), w["N"]))
+    rows = np.asarray(rows)
+    for g in range(len(gm)):
+        sel = np.nonzero((rows >= off[g]) & (rows < off[g + 1]))[0]
+        if len(sel):
+            wg = og.decode(w["w"][g], "bf16")
+            res[sel] = decode_out(og.gemm(x[rows[sel]], wg, out), out)
+    return res
+
+
+@pytest.mark.parametrize("gm", [[3, 0, 130, 1, 0, 257], [0, 0, 64], [200], [1] * 17])
+@pytest.mark.parametrize("bcol", [False, True])
+def test_grouped_small(gm, bcol):
+    w = wl.grouped_bf16(group_m=gm, N=200, K=136, seed=len(gm))
+    total = sum(gm)
+    for S, d, tn in [(1, 0, 128), (2, 1, 64), (3, 0, 256)]:
+        G = len(gm)
+        cap = (-(-total // 128) + G) * -(-200 // tn)
+        trace = torch.full((cap * 5,), -1, dtype=torch.int32, device="cuda")
+        got = run_grouped(w, bst.sched(S, d, tile_n=tn, trace=trace), b_col_major=bcol)
+        ref = decode_out(og.gemm_grouped(og.decode(w["x"], "bf16"), og.decode(w["w"], "bf16"), gm, "bf16"), "bf16")
+        assert_close_f16(got, ref)
+        want = np.array(osw.grouped_swizzle_map(gm, 200, 128, tn, S, d), dtype=np.uint32).reshape(-1, 5)
+        tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)[:len(want)]
+        assert np.array_equal(tr, want)
+
+
+def test_grouped_inconsistent_sizes_reported():
+    w = wl.grouped_bf16(group_m=[100, 100], N=64, K=64, seed=1)
+    gdev = torch.tensor([100, 200], dtype=torch.int32, device="cuda")     # sums past total_m = 200
+    X, Wd = dev(w["x"]), dev(w["w"])
+    C = torch.zeros(200 * 64, dtype=torch.int16, device="cuda")
+    bst.gemm_grouped(2, gdev, 200, 64, 64, X, 64, Wd, bst.ROW_MAJOR, 64, 64 * 64, C, 64, bst.BF16, bst.BF16)
+    with pytest.raises(bst.BstError) as e:
+        bst.check_async()
+    assert e.value.status == bst.ERR_DEVICE
+    bst.check_async()      # the error word was cleared
+
+
+@pytest.mark.parametrize("forced", [None, [0, 2048, 0, 1024, 3072, 0, 2048, 0]])
+def test_grouped_full_workload(forced):
+    """G=8 groups summing to 8192 rows, K=N=4096, bf16; sampled rows."""
+    w = wl.grouped_bf16(group_m=forced)
+    got = run_grouped(w)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(sum(w["group_m"]), 384, replace=False))
+    assert_close_f16(got[rows], oracle_grouped_rows(w, rows))
+
+
+# --------------------------------------------------------------- MXFP8 -----
+
+def run_mx(w, sched=None, out="bf16"):
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B, SA, SB = dev(w["a"]), dev(w["b"]), dev(w["sa"]), dev(w["sb"])
+    ob = 4 if out == "f32" else 2
+    cbuf, C = empty_bytes(M * N * ob, CANARY)
+    bst.gemm(M, N, K, A, bst.E4M3, bst.ROW_MAJOR, K, B, bst.E4M3, bst.COL_MAJOR, K, C,
+             {"bf16": bst.BF16, "f32": bst.F32}[out], N, scale_a=SA, scale_b=SB, sched=sched)
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY)
+    raw = host(C, np.uint8).view(np.float32 if out == "f32" else np.uint16).reshape(M, N)
+    return decode_out(raw.copy(), out)
+
+
+@pytest.mark.parametrize("mnk", [(128, 128, 128), (200, 300, 256), (129, 257, 512), (1, 40, 128)])
+@pytest.mark.parametrize("tn", [128, 256])
+def test_mxfp8_small(mnk, tn):
+    M, N, K = mnk
+    w = wl.mxfp8(M, N, K, seed=M + N)
+    got = run_mx(w, bst.sched(2, 0, tile_n=tn))
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"]), "bf16")
+    assert_close_fro(got, ref, FRO_MX)
+
+
+def test_mxfp8_unit_scales_and_single_block():
+    """All scales 1 except one 32-block of one row of A: checks each scale
+    reaches exactly its own rows and K sub-block."""
+    M, N, K = 256, 256, 256
+    w = wl.mxfp8(M, N, K, seed=3)
+    w["sa"][:] = 127
+    w["sb"][:] = 127
+    w["sa"][37, 5] = 130          # x8 on row 37, K 160..191
+    w["sb"][200, 2] = 124         # /8 on column 200, K 64..95
+    got = run_mx(w, bst.sched(1, 0, tile_n=128), out="f32")
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"], "f32"), "f32")
+    assert_close_fro(got, ref, 1e-5)
+
+
+def test_mxfp8_full_workload():
+    """e4m3 1024x2048x4096 with E8M0 scales 2^U{-4..4} per 32 K."""
+    w = wl.mxfp8()
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"]), "bf16")
+    for S, d in [(1, 0), (4, 1)]:
+        got = run_mx(w, bst.sched(S, d))
+        assert_close_fro(got, ref, FRO_MX)
+
+
+# ---------------------------------------------------------------- int8 -----
+
+def run_int8(w, b_col_major=True, sched=None):
+    M, N, K = w["M"], w["N"], w["K"]
+    Bst = w["b"] if b_col_major else np.ascontiguousarray(w["b"].T)
+    A, B = dev(w["a"]), dev(Bst)
+    SA, SB = dev(w["sa"]), dev(w["sb"])
+    cbuf, C = empty_bytes(M * N * 2, CANARY)
+    abuf, ACC = empty_bytes(M * N * 4, CANARY)
+    ws_bytes = bst.gemm_quant_per_token_workspace_size(M, N, K)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    bst.gemm_quant_per_token(M, N, K, A, K, B, bst.COL_MAJOR if b_col_major else bst.ROW_MAJOR,
+                             K if b_col_major else N, SA, SB, C, N, ACC, ws, ws_bytes, sched=sched)
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY) and canary_intact(abuf, CANARY)
+    out = decode_out(host(C, np.uint16).reshape(M, N).copy(), "bf16")
+    acc = host(ACC, np.int32).reshape(M, N).copy()
+    return out, acc
+
+
+def oracle_int8_rows(w, rows):
+    a = w["a"][rows]
+    acc, out = og.gemm_quant_per_token(a, w["b"].T, w["sa"][rows], w["sb"])
+    return acc, decode_out(out, "bf16")
+
+
+@pytest.mark.parametrize("mnk", [(128, 128, 64), (300, 200, 2100), (1, 130, 1024), (257, 129, 40)])
+@pytest.mark.parametrize("bcol", [True, False])
+def test_int8_small(mnk, bcol):
+    M, N, K = mnk
+    w = wl.int8_per_token(M, N, K, seed=M + K)
+    out, acc = run_int8(w, bcol, bst.sched(2, 1))
+    racc, rout = oracle_int8_rows(w, np.arange(M))
+    assert np.array_equal(acc, racc)
+    assert_close_fro(out, rout, FRO_MX)
+
+
+def test_int8_extreme_sums_exact():
+    """All-|127| operands at K=8192 give the largest sums the path must carry
+    exactly (8192*127*127 = 132,128,768)."""
+    M = N = 128
+    K = 8192
+    w = wl.int8_per_token(M, N, K, seed=1)
+    w["a"][:] = 127
+    w["a"][1::2] = -127
+    w["b"][:] = 127
+    w["b"][:, ::3] = -127
+    out, acc = run_int8(w, True, bst.sched(1, 0))
+    racc, rout = oracle_int8_rows(w, np.arange(M))
+    assert np.array_equal(acc, racc)
+    assert_close_fro(out, rout, FRO_MX)
+
+
+def test_int8_full_workload():
+    """int8 8192x8192x8192 with per-row / per-column fp32 scales; exact
+    int32 accumulators and dequantised bf16 on a seeded sample of rows."""
+    w = wl.int8_per_token()
+    out, acc = run_int8(w, True)
+    rows = np.sort(np.random.default_rng(1).choice(w["M"], 256, replace=False))
+    racc, rout = oracle_int8_rows(w, rows)
+    assert np.array_equal(acc[rows], racc)
+    assert_close_fro(out[rows], rout, FRO_MX)

@@ -328,16 +328,24 @@ def total_rows(work):
 
 
 def cpu_rate(work, budget_s):
-    """Oracle throughput on a sample of whole rows sized to ~budget_s."""
+    """Oracle throughput on a sample of whole output rows sized to about
+    budget_s of CPU time (the whole problem, repeated, when that is smaller).
+    Returns (TFLOP/s, sample description, seconds)."""
     rows = 8
     t = time.perf_counter()
-    fl = oracle_rows(work, rows)
+    oracle_rows(work, rows)
     dt = max(time.perf_counter() - t, 1e-6)
-    rows = int(max(8, min(total_rows(work), rows * budget_s / dt)))
+    want = rows * budget_s / dt
+    total = total_rows(work)
+    if want <= total:
+        rows, reps = int(max(8, want)), 1
+    else:
+        rows, reps = total, int(max(1, round(want / total)))
     t = time.perf_counter()
-    fl = oracle_rows(work, rows)
+    fl = sum(oracle_rows(work, rows) for _ in range(reps))
     dt = time.perf_counter() - t
-    return fl / dt / 1e12, rows, dt
+    sample = "%d of %d output rows%s (whole rows, %.1f s)" % (rows, total, " x%d" % reps if reps > 1 else "", dt)
+    return fl / dt / 1e12, sample, dt
 
 
 def reference_arm(args, work_name):
@@ -352,7 +360,11 @@ def reference_arm(args, work_name):
     desc = {"fp16_square": "fp16 GEMM M=1024 N=1024 K=2048, A row-major, B col-major, fp32 accumulate, fp16 out"}
     # size the per-step sample so that warmup + steps take about two minutes
     budget = min(20.0, 120.0 / max(1, args.steps + args.warmup))
-    rate, rows, dt = cpu_rate(work, budget)
+    rows = 8
+    t = time.perf_counter()
+    oracle_rows(work, rows)
+    dt = max(time.perf_counter() - t, 1e-6)
+    rows = int(max(8, min(total_rows(work), rows * budget / dt)))
     for _ in range(args.warmup):
         oracle_rows(work, rows)
     t = time.perf_counter()
@@ -385,6 +397,8 @@ def main():
                     choices=["fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token"])
     ap.add_argument("--lite", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.0)
+    ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (64/128/256); 0 = automatic")
+    ap.add_argument("--swizzle", default="", help="force the schedule, e.g. Zn3 or Nz1; default: sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -413,17 +427,21 @@ def main():
 
     # swizzle sweep (untimed choice of SwizzleOffset/direction for the line)
     sweep = {}
-    if args.workload in ("fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token") and not args.lite:
+    tn = args.tile_n
+    work.sched = work.bst.sched(1, 0, tile_n=tn)
+    if args.swizzle:
+        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, tile_n=tn)
+    elif not args.lite:
         n = max(8, min(200, args.steps))
         for S in (1, 2, 4, 8):
             for d in (0, 1):
-                work.sched = work.bst.sched(S, d)
+                work.sched = work.bst.sched(S, d, tile_n=tn)
                 for i in range(3):
                     work.step(i)
                 ms = timed_steps(work, n, stream)
                 sweep["%s%d" % ("Zn" if d == 0 else "Nz", S)] = round(work.flops * n / (ms * 1e-3) / 1e12, 2)
         best = max(sweep, key=sweep.get)
-        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1)
+        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, tile_n=tn)
 
     for i in range(args.warmup):
         work.step(i)
@@ -479,10 +497,9 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.lite:
-        rate, rows, dt = cpu_rate(work, 12.0)
+        rate, sample, dt = cpu_rate(work, 12.0)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": int(os.environ["OPENBLAS_NUM_THREADS"]), "kind": "oracle",
-               "sample": "%d of %d output rows (whole rows, %.1f s), fp64 BLAS matmul + one rounding"
-                         % (rows, total_rows(work), dt)}
+               "sample": sample + ", fp64 BLAS matmul + one rounding"}
 
     if rank != 0:
         return
@@ -506,6 +523,7 @@ def main():
                                "direction": "Zn" if work.sched.swizzle_direction == 0 else "Nz"},
                    "l2": "inputs rotate over %d copies (%.0f MB > 129 MB L2)"
                          % (work.copies, work.copies * (work.in_bytes + work.out_bytes) / 1e6),
+                   "tile_n": work.sched.tile_n or "auto",
                    "launch": "CUDA graphs, one stream", "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": stored_traffic(work.kernel_key),

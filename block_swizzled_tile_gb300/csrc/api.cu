@@ -95,6 +95,7 @@ uint64_t timeout_ns() { return t_timeout_ns ? t_timeout_ns : kDefaultTimeoutNs; 
 struct Sched {
     uint32_t offset = 1, dir = 0, tile_n = 0, num_ctas = 0;
     uint32_t* trace = nullptr;
+    uint64_t* timeline = nullptr;
 };
 
 bst_status read_sched(const bst_sched* s, Sched& out) {
@@ -106,6 +107,7 @@ bst_status read_sched(const bst_sched* s, Sched& out) {
     out.tile_n = s->tile_n;
     out.num_ctas = s->num_ctas;
     out.trace = s->trace;
+    out.timeline = s->timeline;
     return BST_OK;
 }
 
@@ -266,28 +268,29 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, tmap_type(at), false)) return s;
-    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, bn, tmap_type(bt), false)) return s;
-    p.M = M; p.N = N; p.K = K;
-    p.batch = batch;
-    p.mode = mode;
-    p.ab_fmt = at == BST_BF16 ? 1u : 0u;
-    p.esize = 2;
-    p.swz_offset = sch.offset;
-    p.swz_dir = sch.dir;
-    p.num_kb = (K + 63) / 64;
-    p.chunk_kb = p.num_kb;
-    p.total_tiles = static_cast<uint32_t>(tiles);
-    p.C = static_cast<uint8_t*>(C);
-    p.ldc = ldc;
-    p.c_batch_stride = sc;
-    p.c_type = c_code;
-    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0) &&
+    if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, tmap_type(at), false)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, bn, tmap_type(bt), false)) return s;
+    p.g.M = M; p.g.N = N; p.g.K = K;
+    p.g.batch = batch;
+    p.g.mode = mode;
+    p.g.ab_fmt = at == BST_BF16 ? 1u : 0u;
+    p.g.esize = 2;
+    p.g.swz_offset = sch.offset;
+    p.g.swz_dir = sch.dir;
+    p.g.num_kb = (K + 63) / 64;
+    p.g.chunk_kb = p.g.num_kb;
+    p.g.total_tiles = static_cast<uint32_t>(tiles);
+    p.g.C = static_cast<uint8_t*>(C);
+    p.g.ldc = ldc;
+    p.g.c_batch_stride = sc;
+    p.g.c_type = c_code;
+    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0) &&
               (mode != kModeBatched || (sc * csize) % 16 == 0);
-    p.trace = sch.trace;
-    p.trace_cap = static_cast<uint32_t>(tiles);
-    p.err = dev.err;
-    p.timeout_ns = timeout_ns();
+    p.g.trace = sch.trace;
+    p.g.timeline = sch.timeline;
+    p.g.trace_cap = static_cast<uint32_t>(tiles);
+    p.g.err = dev.err;
+    p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_dense(p, bn, grid, stream));
@@ -327,28 +330,29 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
-    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, bn, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
-    p.M = M; p.N = N; p.K = K;
-    p.batch = 1;
-    p.mode = kModePlain;
-    p.esize = 1;
-    p.swz_offset = sch.offset;
-    p.swz_dir = sch.dir;
-    p.num_kb = K / 128;
-    p.chunk_kb = p.num_kb;
-    p.total_tiles = static_cast<uint32_t>(tiles);
-    p.C = static_cast<uint8_t*>(C);
-    p.ldc = ldc;
-    p.c_type = c_code;
-    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
-    p.sfa = sfa;
-    p.sfb = sfb;
-    p.sf_ld = static_cast<uint32_t>(K / 32);
-    p.trace = sch.trace;
-    p.trace_cap = static_cast<uint32_t>(tiles);
-    p.err = dev.err;
-    p.timeout_ns = timeout_ns();
+    if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, bn, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
+    p.g.M = M; p.g.N = N; p.g.K = K;
+    p.g.batch = 1;
+    p.g.mode = kModePlain;
+    p.g.esize = 1;
+    p.g.swz_offset = sch.offset;
+    p.g.swz_dir = sch.dir;
+    p.g.num_kb = K / 128;
+    p.g.chunk_kb = p.g.num_kb;
+    p.g.total_tiles = static_cast<uint32_t>(tiles);
+    p.g.C = static_cast<uint8_t*>(C);
+    p.g.ldc = ldc;
+    p.g.c_type = c_code;
+    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
+    p.g.sfa = sfa;
+    p.g.sfb = sfb;
+    p.g.sf_ld = static_cast<uint32_t>(K / 32);
+    p.g.trace = sch.trace;
+    p.g.timeline = sch.timeline;
+    p.g.trace_cap = static_cast<uint32_t>(tiles);
+    p.g.err = dev.err;
+    p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_mxf8(p, bn, grid, stream));
@@ -422,28 +426,29 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, tmap_type(ab_type), false)) return s;
-    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, bn, tmap_type(ab_type), false)) return s;
-    p.M = 0; p.N = N; p.K = K;
-    p.batch = 1;
-    p.mode = kModeGrouped;
-    p.ab_fmt = ab_type == BST_BF16 ? 1u : 0u;
-    p.esize = 2;
-    p.swz_offset = sch.offset;
-    p.swz_dir = sch.dir;
-    p.num_kb = (K + 63) / 64;
-    p.chunk_kb = p.num_kb;
-    p.group_m = group_m;
-    p.G = static_cast<uint32_t>(G);
-    p.total_m = static_cast<uint32_t>(total_m);
-    p.C = static_cast<uint8_t*>(C);
-    p.ldc = ldc;
-    p.c_type = c_code;
-    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
-    p.trace = sch.trace;
-    p.trace_cap = static_cast<uint32_t>(tiles_bound);
-    p.err = dev.err;
-    p.timeout_ns = timeout_ns();
+    if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, tmap_type(ab_type), false)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, bn, tmap_type(ab_type), false)) return s;
+    p.g.M = 0; p.g.N = N; p.g.K = K;
+    p.g.batch = 1;
+    p.g.mode = kModeGrouped;
+    p.g.ab_fmt = ab_type == BST_BF16 ? 1u : 0u;
+    p.g.esize = 2;
+    p.g.swz_offset = sch.offset;
+    p.g.swz_dir = sch.dir;
+    p.g.num_kb = (K + 63) / 64;
+    p.g.chunk_kb = p.g.num_kb;
+    p.g.group_m = group_m;
+    p.g.G = static_cast<uint32_t>(G);
+    p.g.total_m = static_cast<uint32_t>(total_m);
+    p.g.C = static_cast<uint8_t*>(C);
+    p.g.ldc = ldc;
+    p.g.c_type = c_code;
+    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
+    p.g.trace = sch.trace;
+    p.g.timeline = sch.timeline;
+    p.g.trace_cap = static_cast<uint32_t>(tiles_bound);
+    p.g.err = dev.err;
+    p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles_bound));
     return cuda_status(launch_dense(p, bn, grid, stream));
@@ -508,30 +513,31 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     OperandSpec b{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(K), ldwb, 0, 1, !b_kmajor};
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    if (bst_status s = fill_operand(p.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
-    if (bst_status s = fill_operand(p.b, &p.tmap_b, b, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
-    p.M = M; p.N = N; p.K = K;
-    p.batch = 1;
-    p.mode = kModePlain;
-    p.ab_fmt = 1;
-    p.esize = 2;
-    p.swz_offset = sch.offset;
-    p.swz_dir = sch.dir;
-    p.num_kb = (K + 63) / 64;
-    p.chunk_kb = kDequantChunkK / 64;
-    p.total_tiles = static_cast<uint32_t>(tiles);
-    p.C = static_cast<uint8_t*>(C);
-    p.ldc = ldc;
-    p.c_type = kOutBF16;
-    p.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * 2) % 16 == 0) &&
+    if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
+    p.g.M = M; p.g.N = N; p.g.K = K;
+    p.g.batch = 1;
+    p.g.mode = kModePlain;
+    p.g.ab_fmt = 1;
+    p.g.esize = 2;
+    p.g.swz_offset = sch.offset;
+    p.g.swz_dir = sch.dir;
+    p.g.num_kb = (K + 63) / 64;
+    p.g.chunk_kb = kDequantChunkK / 64;
+    p.g.total_tiles = static_cast<uint32_t>(tiles);
+    p.g.C = static_cast<uint8_t*>(C);
+    p.g.ldc = ldc;
+    p.g.c_type = kOutBF16;
+    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * 2) % 16 == 0) &&
               (!acc_out || (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0));
-    p.scale_a = scale_a;
-    p.scale_b = scale_b;
-    p.acc_out = acc_out;
-    p.trace = sch.trace;
-    p.trace_cap = static_cast<uint32_t>(tiles);
-    p.err = dev.err;
-    p.timeout_ns = timeout_ns();
+    p.g.scale_a = scale_a;
+    p.g.scale_b = scale_b;
+    p.g.acc_out = acc_out;
+    p.g.trace = sch.trace;
+    p.g.timeline = sch.timeline;
+    p.g.trace_cap = static_cast<uint32_t>(tiles);
+    p.g.err = dev.err;
+    p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_dequant(p, grid, stream));

@@ -9,7 +9,7 @@ static cudaError_t launch_one(const GemmParams& p, uint32_t grid, cudaStream_t s
     using Lay = GemmLayout<BN, STAGES, 2, kKindF16>;
     static std::atomic<uint64_t> attr_done{0};
     auto kern = gemm_kernel<BN, STAGES, 2, kKindF16, kEpiStore>;
-    const uint32_t smem = Lay::smem_bytes(p.mode == kModeGrouped ? p.G : 0);
+    const uint32_t smem = Lay::smem_bytes(p.g.mode == kModeGrouped ? p.g.G : 0);
     // the limit is set once for the largest group table any call can need
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(kMaxGroups), attr_done);
     if (e != cudaSuccess) return e;

@@ -5,12 +5,11 @@
 // scheduler (sched.cuh, "Block Scheduler Code Explained" sections 4-7).
 // Roles inside the CTA (192 threads):
 //   warp 0     producer: per k-block waits for a free shared-memory stage and
-//              fills it (TMA, or ordinary loads for operands TMA cannot take;
-//              MXFP8 scale factors by cp.async) -- the counterpart of the
-//              GM->L1 copies of "Block Dispatch Policies"
-//              (MmadAtlasA2Preload/PreloadAsync: the producer runs ahead
-//              across tile and group boundaries, i.e. inter-block and
-//              inter-group preloading).
+//              fills it (TMA, or cp.async for operands TMA cannot take; MXFP8
+//              scale factors by cp.async) -- the counterpart of the GM->L1
+//              copies of "Block Dispatch Policies" (MmadAtlasA2Preload /
+//              PreloadAsync: the producer runs ahead across tile and group
+//              boundaries, i.e. inter-block and inter-group preloading).
 //   warp 1     MMA issuer: one thread issues tcgen05.mma into a TMEM
 //              accumulator, releasing each stage with tcgen05.commit.
 //   warps 2-5  epilogue: TMEM -> registers -> global, with the tail tile cut
@@ -20,9 +19,13 @@
 //
 // Shared-memory stage layout (STAGES copies): A tile 128 rows x 128 bytes,
 // then B tile BN rows x 128 bytes, both in the 128-byte-swizzled layout TMA
-// writes.  A "row" is a 128-byte line: for K-contiguous operands one row of
-// the matrix and one k-block (64 x 16-bit or 128 x 8-bit elements); for
+// writes.  A "line" is 128 bytes: for K-contiguous operands one row of the
+// matrix over one k-block (64 x 16-bit or 128 x 8-bit elements); for
 // MN-contiguous operands one k of a 64/128-element MN atom.
+//
+// All kernel arguments are read into registers once at entry; the loops then
+// touch no parameter memory (the inline PTX that orders shared memory would
+// otherwise force every field to be re-read after each such statement).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -48,13 +51,12 @@ struct OperandDesc {
     int64_t batch_stride;  // elements
     uint32_t mn_major;     // 1: the M (or N) index is contiguous
     uint32_t use_tma;
-    uint32_t vec_bytes;    // ordinary-load vector width when !use_tma
+    uint32_t vec_bytes;    // cp.async / plain-load vector width when !use_tma
     uint32_t tma_rank;     // 2, or 3 when the tensor map has a batch/group dimension
 };
 
-struct GemmParams {
-    CUtensorMap tmap_a;
-    CUtensorMap tmap_b;
+// Every scalar argument of the kernel.
+struct GemmArgs {
     OperandDesc a, b;
     uint32_t M, N, K;
     uint32_t batch;
@@ -81,8 +83,15 @@ struct GemmParams {
     uint32_t sf_ld;         // bytes per row of sfa / sfb (K / 32)
     uint32_t* trace;
     uint32_t trace_cap;     // tasks the trace buffer holds
+    uint64_t* timeline;     // optional: 64 %globaltimer stamps per CTA
     uint32_t* err;
     uint64_t timeout_ns;
+};
+
+struct GemmParams {
+    CUtensorMap tmap_a;
+    CUtensorMap tmap_b;
+    GemmArgs g;
 };
 
 template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND>
@@ -106,67 +115,75 @@ struct GemmLayout {
         kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM budget");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static constexpr uint32_t smem_bytes(uint32_t groups) {
-        return 1024 + kTableOff + 8 * (groups + 1);
-    }
+    static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
 };
 
-// Every lane of the warp waits; the warp proceeds only if all lanes saw the
-// phase complete, so a timeout never leaves the lanes of a warp in different
-// places of the loop.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, uint32_t where) {
-    const bool ok = mbar_wait(bar, parity, ctl, where);
-    return __all_sync(0xFFFFFFFFu, ok);
+// One lane of the warp waits on the barrier (the others would only add
+// shared-memory traffic); the warp then re-converges, with the memory
+// ordering of __syncwarp, and every lane gets the same verdict, so a timeout
+// never splits the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
+    uint32_t ok = 1;
+    if ((threadIdx.x & 31u) == 0) ok = mbar_wait(bar, parity, ctl, where) ? 1u : 0u;
+    __syncwarp();
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
+
+// What the scheduler needs, in registers.
+struct SchedArgs {
+    uint32_t M, N, swz_offset, swz_dir, mode, total_m;
+};
 
 struct TileInfo {
     uint32_t tag;      // batch index or group index
     uint32_t m, n;     // tile indices
     uint32_t m_act, n_act;
     uint32_t row0;     // first row of the tile in A / C (includes the group offset)
-    uint32_t m_lim;    // rows of A that may be read (TMA bound is the tensor map)
+    uint32_t m_lim;    // rows of A that exist (loads past it read zeros)
 };
 
-__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, uint32_t t, uint32_t BN, const GroupTable& gt) {
+__device__ __forceinline__ TileInfo tile_info(const SchedArgs& sa, uint32_t t, uint32_t BN, const GroupTable& gt) {
     TileInfo ti;
     SwizzleSched s;
-    if (p.mode == kModeGrouped) {
+    if (sa.mode == kModeGrouped) {
         const uint32_t g = gt.find(t);
         const uint32_t mg = gt.row_off[g + 1] - gt.row_off[g];
-        s.update(mg, p.N, kBM, BN, p.swz_offset, p.swz_dir);
-        const uint32_t inner = t - gt.tile_off[g];
-        s.block_coord(inner, ti.m, ti.n);
+        s.update(mg, sa.N, kBM, BN, sa.swz_offset, sa.swz_dir);
+        s.block_coord(t - gt.tile_off[g], ti.m, ti.n);
         s.actual_shape(ti.m, ti.n, ti.m_act, ti.n_act);
         ti.tag = g;
         ti.row0 = gt.row_off[g] + ti.m * kBM;
-        ti.m_lim = p.total_m;
+        ti.m_lim = sa.total_m;
     } else {
-        s.update(p.M, p.N, kBM, BN, p.swz_offset, p.swz_dir);
+        s.update(sa.M, sa.N, kBM, BN, sa.swz_offset, sa.swz_dir);
         ti.tag = s.batch_idx(t);
         s.block_coord(t, ti.m, ti.n);
         s.actual_shape(ti.m, ti.n, ti.m_act, ti.n_act);
         ti.row0 = ti.m * kBM;
-        ti.m_lim = p.M;
+        ti.m_lim = sa.M;
     }
     return ti;
 }
 
-// Ordinary-load fallback that writes the exact shared-memory image a TMA load
-// with 128-byte swizzle would: line L (128 bytes) at L*128, its 16-byte chunk
-// c at ((c ^ (L % 8)) * 16).  Out-of-range elements are zero, like TMA's
-// out-of-bounds fill.
-static __device__ __noinline__ void load_tile_plain(uint8_t* dst, const OperandDesc& op, uint32_t esize, uint32_t lines,
-                                             uint32_t mn0, uint32_t mn_lim, uint32_t k0, uint32_t k_lim,
-                                             int64_t base_elems, uint32_t lane) {
+// Fallback for operands TMA cannot fetch (pitch or base not 16-byte
+// aligned).  Writes the exact shared-memory image a TMA load with 128-byte
+// swizzle would: line L (128 bytes) at L*128, its 16-byte chunk c at
+// ((c ^ (L % 8)) * 16); out-of-range elements are zero, like TMA's
+// out-of-bounds fill.  Vectors of 4-16 bytes go through cp.async (zero-fill
+// past the edge) and complete on the stage barrier through the caller's
+// cp.async.mbarrier.arrive; 2-byte vectors (odd pitches) use plain loads and
+// stores and the caller fences them for the async proxy.
+__device__ __noinline__ static void load_tile_plain(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t mn_major,
+                                                    uint32_t V, uint32_t esize, uint32_t lines, uint32_t mn0,
+                                                    uint32_t mn_lim, uint32_t k0, uint32_t k_lim, uint32_t lane) {
     const uint32_t line_elems = kLine / esize;
-    const uint32_t V = op.vec_bytes;
     const uint32_t vpl = kLine / V;
     const uint32_t total = lines * vpl;
     for (uint32_t idx = lane; idx < total; idx += 32) {
         const uint32_t L = idx / vpl;
         const uint32_t byte_in_line = (idx % vpl) * V;
         uint32_t outer, outer_lim, inner0, inner_lim;
-        if (!op.mn_major) {           // line = one MN row, a k-block of K
+        if (!mn_major) {              // line = one MN row, a k-block of K
             outer = mn0 + L;
             outer_lim = mn_lim;
             inner0 = k0;
@@ -178,30 +195,45 @@ static __device__ __noinline__ void load_tile_plain(uint8_t* dst, const OperandD
             inner_lim = mn_lim;
         }
         const uint32_t e = inner0 + byte_in_line / esize;
-        const uint32_t ve = V / esize;
         uint8_t* d = dst + L * kLine + ((((byte_in_line >> 4) ^ (L & 7u)) << 4) | (byte_in_line & 15u));
-        const uint8_t* src = op.ptr + (base_elems + static_cast<int64_t>(outer) * op.ld + e) * esize;
-        if (outer < outer_lim && e + ve <= inner_lim) {
-            if (V == 16) *reinterpret_cast<uint4*>(d) = __ldg(reinterpret_cast<const uint4*>(src));
-            else if (V == 8) *reinterpret_cast<uint2*>(d) = __ldg(reinterpret_cast<const uint2*>(src));
-            else if (V == 4) *reinterpret_cast<uint32_t*>(d) = __ldg(reinterpret_cast<const uint32_t*>(src));
-            else if (V == 2) *reinterpret_cast<uint16_t*>(d) = __ldg(reinterpret_cast<const uint16_t*>(src));
-            else *d = __ldg(src);
+        const bool row_in = outer < outer_lim;
+        const uint32_t in_elems = (row_in && e < inner_lim) ? inner_lim - e : 0u;
+        const uint32_t in_bytes = min(V, in_elems * esize);
+        const uint8_t* src = in_bytes ? base + (static_cast<int64_t>(outer) * ld + e) * esize : base;
+        if (V >= 4) {
+            cp_async_n(d, src, V, in_bytes);
         } else {
-            for (uint32_t j = 0; j < V; ++j) {
-                const uint32_t ej = e + j / esize;
-                d[j] = (outer < outer_lim && ej < inner_lim) ? src[j] : 0;
-            }
+            uint16_t v = 0;
+            if (in_bytes) v = __ldg(reinterpret_cast<const uint16_t*>(src));
+            *reinterpret_cast<uint16_t*>(d) = v;
+        }
+    }
+}
+
+// Issues the TMA loads of one operand tile: one box for K-contiguous
+// operands, one box per 128-byte MN atom otherwise.
+__device__ __forceinline__ void tma_tile(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, uint32_t mn_major,
+                                         uint32_t rank3, uint32_t mn0, uint32_t rows, uint32_t k0, int32_t z,
+                                         uint32_t bk_elems) {
+    if (!mn_major) {
+        if (rank3) tma_load_3d(dst, map, bar, k0, mn0, z);
+        else tma_load_2d(dst, map, bar, k0, mn0);
+    } else {
+        for (uint32_t j = 0; j < rows / bk_elems; ++j) {
+            uint8_t* d = dst + j * bk_elems * kLine;
+            const int32_t x = mn0 + j * bk_elems;
+            if (rank3) tma_load_3d(d, map, bar, x, k0, z);
+            else tma_load_2d(d, map, bar, x, k0);
         }
     }
 }
 
 // Stores 32 consecutive fp32 accumulator columns of one output row.
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, uint8_t* row_ptr, uint32_t col0, uint32_t n_valid,
-                                                const uint32_t (&v)[32]) {
-    if (p.c_type == kOutF32) {
+__device__ __forceinline__ void store_row_chunk(uint32_t c_type, uint32_t c_vec, uint8_t* row_ptr, uint32_t col0,
+                                                uint32_t n_valid, const uint32_t (&v)[32]) {
+    if (c_type == kOutF32) {
         float* out = reinterpret_cast<float*>(row_ptr) + col0;
-        if (p.c_vec && n_valid >= 32) {
+        if (c_vec && n_valid >= 32) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<uint4*>(out + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -213,7 +245,7 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, uint8_t* ro
         return;
     }
     uint32_t packed[16];
-    if (p.c_type == kOutF16) {
+    if (c_type == kOutF16) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             __half2 h = __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
@@ -227,7 +259,7 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, uint8_t* ro
         }
     }
     uint16_t* out = reinterpret_cast<uint16_t*>(row_ptr) + col0;
-    if (p.c_vec && n_valid >= 32) {
+    if (c_vec && n_valid >= 32) {
 #pragma unroll
         for (int j = 0; j < 16; j += 4)
             *reinterpret_cast<uint4*>(out + 2 * j) = make_uint4(packed[j], packed[j + 1], packed[j + 2], packed[j + 3]);
@@ -239,12 +271,23 @@ __device__ __forceinline__ void store_row_chunk(const GemmParams& p, uint8_t* ro
 }
 
 template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND, uint32_t EPI>
-__global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_constant__ GemmParams prm) {
     using Lay = GemmLayout<BN, STAGES, ACC, KIND>;
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
     static_assert(EPI == kEpiStore || BN == 128, "dequant epilogue keeps 128 int32 per thread");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    // ---- arguments into registers, once
+    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m};
+    const uint32_t N = prm.g.N, K = prm.g.K, mode = prm.g.mode, esize = prm.g.esize;
+    const uint32_t num_kb = prm.g.num_kb, chunk_kb = prm.g.chunk_kb, G = prm.g.G;
+    const uint32_t a_tma = prm.g.a.use_tma, b_tma = prm.g.b.use_tma;
+    const uint32_t a_mn = prm.g.a.mn_major, b_mn = prm.g.b.mn_major;
+    const uint32_t a_rank3 = prm.g.a.tma_rank == 3, b_rank3 = prm.g.b.tma_rank == 3;
+    uint32_t* const err = prm.g.err;
+    uint64_t* const tl = prm.g.timeline ? prm.g.timeline + static_cast<uint64_t>(blockIdx.x) * 64 : nullptr;
+    const uint32_t bk_elems = kLine / esize;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
     uint64_t* full = bars;
@@ -259,15 +302,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
+    const bool lanes_copy = KIND == kKindMXF8 || !(a_tma && b_tma);
 
     GroupTable gt;
-    gt.G = p.G;
+    gt.G = G;
     gt.tile_off = reinterpret_cast<uint32_t*>(smem + Lay::kTableOff);
-    gt.row_off = gt.tile_off + (p.mode == kModeGrouped ? p.G + 1 : 0);
+    gt.row_off = gt.tile_off + (mode == kModeGrouped ? G + 1 : 0);
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], KIND == kKindMXF8 ? 33u : 1u);
+            // 1 arrival from the issuing lane (+ TMA bytes), plus one per lane
+            // when lanes also copy (MXFP8 scale factors, non-TMA operands)
+            mbar_init(&full[s], lanes_copy ? 33u : 1u);
             mbar_init(&empty[s], 1);
         }
         for (uint32_t a = 0; a < ACC; ++a) {
@@ -276,25 +322,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
-        *tiles_smem = p.total_tiles;
+        *tiles_smem = prm.g.total_tiles;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        if (p.a.use_tma) prefetch_tmap(&p.tmap_a);
-        if (p.b.use_tma) prefetch_tmap(&p.tmap_b);
+        if (a_tma) prefetch_tmap(&prm.tmap_a);
+        if (b_tma) prefetch_tmap(&prm.tmap_b);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, Lay::kTmemCols);
         tmem_relinquish();
     }
-    if (p.mode == kModeGrouped && warp == 2) {
+    if (mode == kModeGrouped && warp == 2) {
         // exclusive prefix sums of rows and tiles over the groups (warp scan)
-        const uint32_t loops_n = (p.N + BN - 1) / BN;
+        const uint32_t loops_n = (N + BN - 1) / BN;
+        const int32_t* group_m = prm.g.group_m;
         uint32_t row_carry = 0, tile_carry = 0, bad = 0;
         if (lane == 0) { gt.row_off[0] = 0; gt.tile_off[0] = 0; }
-        for (uint32_t base = 0; base < p.G; base += 32) {
+        for (uint32_t base = 0; base < G; base += 32) {
             const uint32_t g = base + lane;
-            int32_t mg = g < p.G ? p.group_m[g] : 0;
+            int32_t mg = g < G ? group_m[g] : 0;
             if (mg < 0) { bad = 1; mg = 0; }
             uint32_t rows = static_cast<uint32_t>(mg);
             uint32_t tiles = ((rows + kBM - 1) / kBM) * loops_n;
@@ -304,7 +351,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                 const uint32_t tt = __shfl_up_sync(0xFFFFFFFFu, tiles, d);
                 if (lane >= d) { rows += r; tiles += tt; }
             }
-            if (g < p.G) {
+            if (g < G) {
                 gt.row_off[g + 1] = row_carry + rows;
                 gt.tile_off[g + 1] = tile_carry + tiles;
             }
@@ -313,9 +360,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         }
         bad = __any_sync(0xFFFFFFFFu, bad);
         if (lane == 0) {
-            if (bad || row_carry > p.total_m) {
+            if (bad || row_carry > sa.total_m) {
                 *tiles_smem = 0;
-                if (blockIdx.x == 0) atomicOr(&p.err[0], kErrGroups);
+                if (blockIdx.x == 0) atomicOr(&err[0], kErrGroups);
             } else {
                 *tiles_smem = tile_carry;
             }
@@ -326,23 +373,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t total_tiles = *tiles_smem;
-    const WaitCtl ctl{abort_flag, p.timeout_ns, p.err};
-    const uint32_t bk_elems = kLine / p.esize;
+    const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
+    if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
+        const uint8_t* a_ptr = prm.g.a.ptr;
+        const uint8_t* b_ptr = prm.g.b.ptr;
+        const int64_t a_ld = prm.g.a.ld, b_ld = prm.g.b.ld;
+        const int64_t a_bs = prm.g.a.batch_stride, b_bs = prm.g.b.batch_stride;
+        const uint32_t a_vec = prm.g.a.vec_bytes, b_vec = prm.g.b.vec_bytes;
+        const uint8_t* sfa = prm.g.sfa;
+        const uint8_t* sfb = prm.g.sfb;
+        const uint32_t sf_ld = prm.g.sf_ld;
+        const bool plain_stores = (!a_tma && a_vec < 4) || (!b_tma && b_vec < 4);
+        const uint32_t tx = (a_tma ? Lay::kABytes : 0u) + (b_tma ? Lay::kBBytes : 0u);
         uint32_t stage = 0, phase = 0, issued = 0;
         bool ok = true;
-        const bool mixed = !(p.a.use_tma && p.b.use_tma);
-        const uint32_t tx = (p.a.use_tma ? Lay::kABytes : 0u) + (p.b.use_tma ? Lay::kBBytes : 0u);
         for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = tile_info(p, t, BN, gt);
+            const TileInfo ti = tile_info(sa, t, BN, gt);
             const uint32_t n0 = ti.n * BN;
             const int32_t zc = static_cast<int32_t>(ti.tag);
-            for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+            for (uint32_t kb = 0; kb < num_kb; ++kb) {
                 if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
-                uint8_t* sa = smem + stage * Lay::kStageBytes;
-                uint8_t* sb = sa + Lay::kABytes;
+                uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+                uint8_t* sb_s = sa_s + Lay::kABytes;
                 const uint32_t k0 = kb * bk_elems;
                 if (KIND == kKindMXF8) {
                     // scale factors for this k-block, written straight into the
@@ -355,7 +410,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                     for (uint32_t i = 0; i < 4; ++i) {
                         const uint32_t r = lane + 32 * i;
                         const bool v = ti.row0 + r < ti.m_lim;
-                        const uint8_t* src = v ? p.sfa + static_cast<int64_t>(ti.row0 + r) * p.sf_ld + kb * 4 : p.sfa;
+                        const uint8_t* src = v ? sfa + static_cast<int64_t>(ti.row0 + r) * sf_ld + kb * 4 : sfa;
                         cp_async_4(sfa_s + (lane * 4 + i) * 4, src, v ? 4u : 0u);
                     }
 #pragma unroll
@@ -363,57 +418,32 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
 #pragma unroll
                         for (uint32_t i = 0; i < 4; ++i) {
                             const uint32_t r = 128 * h + lane + 32 * i;
-                            const bool v = n0 + r < p.N;
-                            const uint8_t* src = v ? p.sfb + static_cast<int64_t>(n0 + r) * p.sf_ld + kb * 4 : p.sfb;
+                            const bool v = n0 + r < N;
+                            const uint8_t* src = v ? sfb + static_cast<int64_t>(n0 + r) * sf_ld + kb * 4 : sfb;
                             cp_async_4(sfb_s + h * 512 + (lane * 4 + i) * 4, src, v ? 4u : 0u);
                         }
                     }
                     cp_async_arrive_noinc(&full[stage]);
+                } else if (lanes_copy) {
+                    if (!a_tma)
+                        load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec, esize,
+                                        kBM, ti.row0, ti.m_lim, k0, K, lane);
+                    if (!b_tma)
+                        load_tile_plain(sb_s, b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
+                                        b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane);
+                    if (plain_stores) {
+                        cp_async_wait_all();         // the other operand may have used cp.async
+                        fence_proxy_async_smem();
+                        mbar_arrive(&full[stage]);
+                    } else {
+                        cp_async_arrive_noinc(&full[stage]);
+                    }
                 }
                 if (lane == 0) {
-                    if (mixed) { if (tx) mbar_expect_tx(&full[stage], tx); }
-                    else mbar_arrive_expect_tx(&full[stage], tx);
-                    if (p.a.use_tma) {
-                        const bool a3 = p.a.tma_rank == 3;
-                        if (!p.a.mn_major) {
-                            if (a3) tma_load_3d(sa, &p.tmap_a, &full[stage], k0, ti.row0, zc);
-                            else tma_load_2d(sa, &p.tmap_a, &full[stage], k0, ti.row0);
-                        } else {
-                            for (uint32_t j = 0; j < kBM / bk_elems; ++j) {
-                                uint8_t* d = sa + j * bk_elems * kLine;
-                                const int32_t x = ti.row0 + j * bk_elems;
-                                if (a3) tma_load_3d(d, &p.tmap_a, &full[stage], x, k0, zc);
-                                else tma_load_2d(d, &p.tmap_a, &full[stage], x, k0);
-                            }
-                        }
-                    }
-                    if (p.b.use_tma) {
-                        const bool b3 = p.b.tma_rank == 3;
-                        if (!p.b.mn_major) {
-                            if (b3) tma_load_3d(sb, &p.tmap_b, &full[stage], k0, n0, zc);
-                            else tma_load_2d(sb, &p.tmap_b, &full[stage], k0, n0);
-                        } else {
-                            for (uint32_t j = 0; j < BN / bk_elems; ++j) {
-                                uint8_t* d = sb + j * bk_elems * kLine;
-                                const int32_t x = n0 + j * bk_elems;
-                                if (b3) tma_load_3d(d, &p.tmap_b, &full[stage], x, k0, zc);
-                                else tma_load_2d(d, &p.tmap_b, &full[stage], x, k0);
-                            }
-                        }
-                    }
-                }
-                if (mixed) {
-                    if (!p.a.use_tma) {
-                        const int64_t base = p.mode == kModeBatched ? static_cast<int64_t>(ti.tag) * p.a.batch_stride : 0;
-                        load_tile_plain(sa, p.a, p.esize, kBM, ti.row0, ti.m_lim, k0, p.K, base, lane);
-                    }
-                    if (!p.b.use_tma) {
-                        const int64_t base = p.mode != kModePlain ? static_cast<int64_t>(ti.tag) * p.b.batch_stride : 0;
-                        load_tile_plain(sb, p.b, p.esize, BN, n0, p.N, k0, p.K, base, lane);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[stage]);
+                    mbar_arrive_expect_tx(&full[stage], tx);
+                    if (a_tma) tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
+                    if (b_tma) tma_tile(&prm.tmap_b, sb_s, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
+                    if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
                 }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -425,39 +455,43 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
             const uint32_t pending = issued < STAGES ? issued : STAGES;
             for (uint32_t i = 0; i < pending; ++i) {
                 if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
-                mbar_wait_drain(&full[s], ph, p.timeout_ns);
+                mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
             }
         }
     } else if (warp == 1) {
         // --------------------------------------------------- MMA issuer --
-        const uint32_t a_mn = p.a.mn_major, b_mn = p.b.mn_major;
-        const uint32_t umma_k_bytes_mn = (32u / p.esize) * kLine;   // MN-major: UMMA_K rows of 128 B
+        const uint32_t umma_k_bytes_mn = (32u / esize) * kLine;   // MN-major: UMMA_K rows of 128 B
         const uint32_t a_lbo = a_mn ? bk_elems * kLine : 16u;
         const uint32_t b_lbo = b_mn ? bk_elems * kLine : 16u;
         const uint32_t a_step = a_mn ? umma_k_bytes_mn : 32u;
         const uint32_t b_step = b_mn ? umma_k_bytes_mn : 32u;
-        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        const uint32_t idesc = idesc_f16(prm.g.ab_fmt, a_mn, b_mn, kBM, BN);
+        const uint32_t smem_base = smem_u32(smem);
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
         bool ok = true, any_mma = false;
-        const uint32_t nchunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
+        const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
         for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
             for (uint32_t c = 0; ok && c < nchunks; ++c) {
-                const uint32_t kb_begin = c * p.chunk_kb;
-                const uint32_t kb_end = min(p.num_kb, kb_begin + p.chunk_kb);
+                const uint32_t kb_begin = c * chunk_kb;
+                const uint32_t kb_end = min(num_kb, kb_begin + chunk_kb);
                 if (!warp_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
                     if (!warp_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
-                    if (KIND == kKindMXF8) fence_proxy_async_smem();
+                    // stages written by cp.async / plain stores need a proxy
+                    // fence before tcgen05 reads them
+                    if (lanes_copy) fence_proxy_async_smem();
                     if (lane == 0) {
-                        const uint32_t sa_addr = smem_u32(smem + stage * Lay::kStageBytes);
+                        if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
+                        const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
                         const uint32_t sb_addr = sa_addr + Lay::kABytes;
                         const uint64_t adesc = smem_desc(sa_addr, a_lbo, 1024, kSwizzle128B);
                         const uint64_t bdesc = smem_desc(sb_addr, b_lbo, 1024, kSwizzle128B);
                         if (KIND == kKindMXF8) {
                             const uint32_t sf_col = ACC * BN + stage * Lay::kSfCols;
-                            const uint32_t sfa_addr = smem_u32(smem + Lay::kSfOff + stage * Lay::kSfStageBytes);
+                            const uint32_t sfa_addr = smem_base + Lay::kSfOff + stage * Lay::kSfStageBytes;
                             tmem_cp_32x128b_warpx4(tmem_base + sf_col, smem_desc(sfa_addr, 0, 128, kSwizzleNone));
 #pragma unroll
                             for (uint32_t h = 0; h < (BN >= 128 ? BN / 128 : 0u); ++h)
@@ -469,7 +503,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                                           idesc_mxf8(kBM, BN, kk), tmem_base + sf_col, tmem_base + sf_col + 4,
                                           (kb > kb_begin || kk > 0) ? 1u : 0u);
                         } else {
-                            const uint32_t idesc = idesc_f16(p.ab_fmt, a_mn, b_mn, kBM, BN);
 #pragma unroll
                             for (uint32_t kk = 0; kk < 4; ++kk)
                                 umma_f16(d_tmem, adesc + ((kk * a_step) >> 4), bdesc + ((kk * b_step) >> 4), idesc,
@@ -477,6 +510,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                         }
                         umma_commit(&empty[stage]);
                     }
+                    ++mma_kb;
                     any_mma = true;
                     __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -491,30 +525,38 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
             // every tcgen05 op issued so far must finish before TMEM is freed
             if (lane == 0) umma_commit(drain);
             __syncwarp();
-            mbar_wait_drain(drain, 0, p.timeout_ns);
+            mbar_wait_drain(drain, 0, ctl.timeout_ns);
         }
     } else {
         // ----------------------------------------------------- epilogue --
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread
-        uint32_t acc = 0, acc_phase = 0;
-        const uint32_t nchunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
-        const uint32_t csize = p.c_type == kOutF32 ? 4u : 2u;
+        const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
+        uint8_t* const C = prm.g.C;
+        const int64_t ldc = prm.g.ldc, c_bs = prm.g.c_batch_stride;
+        const float* scale_a = prm.g.scale_a;
+        const float* scale_b = prm.g.scale_b;
+        int32_t* const acc_out = prm.g.acc_out;
+        uint32_t* const trace = prm.g.trace;
+        const uint32_t trace_cap = prm.g.trace_cap;
+        const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
+        const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
+        uint32_t acc = 0, acc_phase = 0, ep_tile = 0;
         bool ok = true;
         for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = tile_info(p, t, BN, gt);
-            if (p.trace && warp == 2 && lane == 0) {
-                if (t < p.trace_cap) {
-                    uint32_t* tr = p.trace + static_cast<uint64_t>(t) * 5;
+            const TileInfo ti = tile_info(sa, t, BN, gt);
+            if (trace && warp == 2 && lane == 0) {
+                if (t < trace_cap) {
+                    uint32_t* tr = trace + static_cast<uint64_t>(t) * 5;
                     tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
                 } else {
-                    atomicOr(&p.err[0], kErrTraceOverflow);
+                    atomicOr(&err[0], kErrTraceOverflow);
                 }
             }
             const bool row_ok = r < ti.m_act;
             const uint32_t grow = ti.row0 + r;
-            const int64_t cbase = p.mode == kModeBatched ? static_cast<int64_t>(ti.tag) * p.c_batch_stride : 0;
-            uint8_t* crow = p.C + (cbase + static_cast<int64_t>(grow) * p.ldc) * csize;
+            const int64_t cbase = mode == kModeBatched ? static_cast<int64_t>(ti.tag) * c_bs : 0;
+            uint8_t* crow = C + (cbase + static_cast<int64_t>(grow) * ldc) * csize;
             const uint32_t n0 = ti.n * BN;
             int32_t run[EPI == kEpiDequant ? BN : 1];
             if (EPI == kEpiDequant) {
@@ -524,23 +566,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
             for (uint32_t c = 0; c < nchunks; ++c) {
                 if (!warp_wait(&tfull[acc], acc_phase, ctl, 4)) { ok = false; break; }
                 tc_fence_after();
+                if (tl && warp == 2 && lane == 0 && c == 0 && ep_tile < 8) tl[32 + ep_tile] = globaltimer_ns();
                 const uint32_t taddr = tmem_base + ((q * 32) << 16) + acc * BN;
                 if (EPI == kEpiStore) {
 #pragma unroll 1
                     for (uint32_t cc = 0; cc < BN / 32; ++cc) {
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(taddr + cc * 32, v);
-                        tmem_ld_wait();
-                        const uint32_t col0 = n0 + cc * 32;
                         if (row_ok && cc * 32 < ti.n_act)
-                            store_row_chunk(p, crow, col0, ti.n_act - cc * 32, v);
+                            store_row_chunk(c_type, c_vec, crow, n0 + cc * 32, ti.n_act - cc * 32, v);
                     }
                 } else {
 #pragma unroll
                     for (uint32_t cc = 0; cc < BN / 32; ++cc) {
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(taddr + cc * 32, v);
-                        tmem_ld_wait();
 #pragma unroll
                         for (uint32_t j = 0; j < 32; ++j)
                             run[(EPI == kEpiDequant ? cc * 32 + j : 0)] += __float2int_rn(__uint_as_float(v[j]));
@@ -551,8 +591,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
             }
             if (!ok) break;
+            if (tl && warp == 2 && lane == 0 && ep_tile < 8) tl[40 + ep_tile] = globaltimer_ns();
+            ++ep_tile;
             if (EPI == kEpiDequant && row_ok) {
-                const float sa = p.scale_a[grow];
+                const float sa_row = scale_a[grow];
 #pragma unroll
                 for (uint32_t cc = 0; cc < BN / 32; ++cc) {
                     if (cc * 32 >= ti.n_act) break;
@@ -561,13 +603,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                     uint32_t v[32];
 #pragma unroll
                     for (uint32_t j = 0; j < 32; ++j) {
-                        const float sb = j < nv ? __ldg(p.scale_b + col0 + j) : 0.f;
-                        v[j] = __float_as_uint(static_cast<float>(run[(EPI == kEpiDequant ? cc * 32 + j : 0)]) * sa * sb);
+                        const float sb = j < nv ? __ldg(scale_b + col0 + j) : 0.f;
+                        v[j] = __float_as_uint(static_cast<float>(run[(EPI == kEpiDequant ? cc * 32 + j : 0)]) * sa_row * sb);
                     }
-                    store_row_chunk(p, crow, col0, nv, v);
-                    if (p.acc_out) {
-                        int32_t* arow = p.acc_out + static_cast<int64_t>(grow) * p.ldc + col0;
-                        if (p.c_vec && nv == 32) {
+                    store_row_chunk(c_type, c_vec, crow, col0, nv, v);
+                    if (acc_out) {
+                        int32_t* arow = acc_out + static_cast<int64_t>(grow) * ldc + col0;
+                        if (c_vec && nv == 32) {
 #pragma unroll
                             for (uint32_t j = 0; j < 32; j += 4)
                                 *reinterpret_cast<int4*>(arow + j) =
@@ -586,6 +628,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         }
     }
 
+    if (tl && lane == 0 && warp <= 2) tl[48 + warp] = globaltimer_ns();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

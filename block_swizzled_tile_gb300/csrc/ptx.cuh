@@ -70,6 +70,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// parked (for at most hint_ns) instead of re-polling, and wakes when the phase
+// completes
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Error word layout (one per device, in the library's own __device__ memory).
 enum : uint32_t {
     kErrTimeout = 1u,       // a bounded wait gave up
@@ -87,15 +102,13 @@ struct WaitCtl {
 // after ctl.timeout_ns (measured on %globaltimer) or a hard iteration cap,
 // raising the CTA's abort flag and recording the failure; returns false then,
 // and also as soon as another role of the CTA has aborted.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, uint32_t where) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1; it < (1u << 28); ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*ctl.abort_flag) return false;
-            if (globaltimer_ns() - t0 > ctl.timeout_ns) break;
-        }
+    for (uint32_t it = 1; it < (1u << 24); ++it) {
+        if (mbar_try_wait_sleep(a, parity, 20000u)) return true;
+        if (*ctl.abort_flag) return false;
+        if (globaltimer_ns() - t0 > ctl.timeout_ns) break;
     }
     *ctl.abort_flag = 1;
     if (atomicOr(&ctl.err_word[0], kErrTimeout) == 0) {
@@ -105,7 +118,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     return false;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& ctl, uint32_t where) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
     if (mbar_try_wait(smem_u32(bar), parity)) return true;
     return mbar_wait_slow(bar, parity, ctl, where);
 }
@@ -115,9 +128,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0; it < (1u << 28); ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 31u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        if (mbar_try_wait_sleep(a, parity, 20000u)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
     return false;
 }
@@ -133,7 +146,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
+        );
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y,
@@ -142,7 +155,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
+        );
 }
 
 // orders this thread's generic-proxy shared-memory writes before later
@@ -156,8 +169,25 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // 4-byte global->shared copy; src_bytes 0 writes zeros instead of reading
 __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
+                 );
 }
+
+// 4-, 8- or 16-byte global->shared copy of which the first src_bytes are read
+// and the rest zero-filled
+__device__ __forceinline__ void cp_async_n(void* dst, const void* src, uint32_t n, uint32_t src_bytes) {
+    if (n == 16)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                    );
+    else if (n == 8)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                    );
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                    );
+}
+
+// waits until every cp.async issued by this thread has landed
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // the barrier receives one arrival (counted in its expected count) when all
 // earlier cp.async of this thread have landed
@@ -225,7 +255,7 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        );
 }
 
 __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -236,33 +266,37 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint6
         "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
+        );
 }
 
 // arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+                 );
 }
 
 // 32 lanes x 128 bits from shared memory into TMEM, replicated to all four
 // 32-lane quarters of the accumulator
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
 }
 
-// each thread of the warp reads 32 consecutive 32-bit columns of its own lane
+// each thread of the warp reads 32 consecutive 32-bit columns of its own lane;
+// the wait for completion sits in the same asm statement so that no use of the
+// destination registers can be scheduled before the data has arrived
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+        : "r"(taddr)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }

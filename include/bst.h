@@ -76,7 +76,16 @@ typedef struct {
     uint32_t* trace;            /* optional DEVICE buffer of 5 uint32 per task; when
                                    non-NULL the kernel writes, for task index t, the
                                    tile it computed: {batch or group, m, n, mActual,
-                                   nActual}.  Debug only.                             */
+                                   nActual}.  For grouped calls it must hold
+                                   (ceil(total_m/128) + G) * ceil(N/tile_n) tasks.
+                                   Debug only.                                        */
+    uint64_t* timeline;         /* optional DEVICE buffer of 64 uint64 per CTA; when
+                                   non-NULL the GEMM kernels write %globaltimer stamps
+                                   (ns) of their pipeline events: [0] start, [1..15]
+                                   producer k-block issues, [16..31] MMA k-block starts,
+                                   [32..39] epilogue tile starts, [40..47] epilogue tile
+                                   ends, [48..50] producer/MMA/epilogue exit.  Profiling
+                                   only.                                               */
 } bst_sched;
 
 /*

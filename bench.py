@@ -398,6 +398,7 @@ def main():
     ap.add_argument("--lite", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.0)
     ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (64/128/256); 0 = automatic")
+    ap.add_argument("--tile-m", type=int, default=0, help="force 128 (one CTA) or 256 (CTA pair); 0 = automatic")
     ap.add_argument("--swizzle", default="", help="force the schedule, e.g. Zn3 or Nz1; default: sweep")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -427,21 +428,22 @@ def main():
 
     # swizzle sweep (untimed choice of SwizzleOffset/direction for the line)
     sweep = {}
-    tn = args.tile_n
-    work.sched = work.bst.sched(1, 0, tile_n=tn)
+    tn, tm = args.tile_n, args.tile_m
+    work.sched = work.bst.sched(1, 0, tile_n=tn, tile_m=tm)
     if args.swizzle:
-        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, tile_n=tn)
+        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, tile_n=tn,
+                                    tile_m=tm)
     elif not args.lite:
         n = max(8, min(200, args.steps))
         for S in (1, 2, 4, 8):
             for d in (0, 1):
-                work.sched = work.bst.sched(S, d, tile_n=tn)
+                work.sched = work.bst.sched(S, d, tile_n=tn, tile_m=tm)
                 for i in range(3):
                     work.step(i)
                 ms = timed_steps(work, n, stream)
                 sweep["%s%d" % ("Zn" if d == 0 else "Nz", S)] = round(work.flops * n / (ms * 1e-3) / 1e12, 2)
         best = max(sweep, key=sweep.get)
-        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, tile_n=tn)
+        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, tile_n=tn, tile_m=tm)
 
     for i in range(args.warmup):
         work.step(i)
@@ -523,7 +525,7 @@ def main():
                                "direction": "Zn" if work.sched.swizzle_direction == 0 else "Nz"},
                    "l2": "inputs rotate over %d copies (%.0f MB > 129 MB L2)"
                          % (work.copies, work.copies * (work.in_bytes + work.out_bytes) / 1e6),
-                   "tile_n": work.sched.tile_n or "auto",
+                   "tile_n": work.sched.tile_n or "auto", "tile_m": work.sched.tile_m or "auto",
                    "launch": "CUDA graphs, one stream", "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": stored_traffic(work.kernel_key),

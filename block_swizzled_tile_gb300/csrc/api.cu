@@ -93,7 +93,7 @@ bool out_code(bst_dtype t, uint32_t& code) {
 uint64_t timeout_ns() { return t_timeout_ns ? t_timeout_ns : kDefaultTimeoutNs; }
 
 struct Sched {
-    uint32_t offset = 1, dir = 0, tile_n = 0, num_ctas = 0;
+    uint32_t offset = 1, dir = 0, tile_n = 0, tile_m = 0, num_ctas = 0;
     uint32_t* trace = nullptr;
     uint64_t* timeline = nullptr;
 };
@@ -102,9 +102,11 @@ bst_status read_sched(const bst_sched* s, Sched& out) {
     if (!s) return BST_OK;
     if (s->swizzle_offset < 1 || s->swizzle_direction > 1) return BST_ERR_INVALID_ARG;
     if (s->tile_n != 0 && s->tile_n != 64 && s->tile_n != 128 && s->tile_n != 256) return BST_ERR_INVALID_ARG;
+    if (s->tile_m != 0 && s->tile_m != 128 && s->tile_m != 256) return BST_ERR_INVALID_ARG;
     out.offset = s->swizzle_offset;
     out.dir = s->swizzle_direction;
     out.tile_n = s->tile_n;
+    out.tile_m = s->tile_m;
     out.num_ctas = s->num_ctas;
     out.trace = s->trace;
     out.timeline = s->timeline;
@@ -207,6 +209,40 @@ uint32_t choose_bn(uint64_t loops_m_total, uint64_t N, uint32_t sms, bool allow6
     return best;
 }
 
+// fp16/bf16 tile choice among one-CTA 128 x {64,128,256} tiles and CTA-pair
+// 256 x {128,256} tiles.  Cost = waves of tiles over the SMs (pairs count as
+// one unit per two SMs) x per-tile time, the per-tile time being BN divided
+// by how close that shape gets to the tensor peak when every SM pulls
+// operands through L2 (narrow tiles need more operand bytes per flop).
+struct TileChoice {
+    uint32_t tm = kBM, bn = 128;
+};
+
+bst_status choose_tile(const Sched& sch, bool pair_ok, bool grouped, uint64_t M, uint64_t mult, uint64_t N,
+                       uint32_t sms, TileChoice& out) {
+    struct Cand {
+        uint32_t tm, bn;
+        double eff;
+    };
+    static const Cand cands[] = {{256, 256, 0.9}, {256, 128, 0.62}, {128, 256, 0.6}, {128, 128, 0.5}, {128, 64, 0.33}};
+    if (sch.tile_m == 256 && !pair_ok) return BST_ERR_UNSUPPORTED;
+    double best = 1e300;
+    for (const Cand& c : cands) {
+        if ((sch.tile_m && c.tm != sch.tile_m) || (sch.tile_n && c.bn != sch.tile_n)) continue;
+        if (c.tm == 256 && !pair_ok) continue;
+        const uint64_t lm = grouped ? (M + c.tm - 1) / c.tm + mult : ((M + c.tm - 1) / c.tm) * mult;
+        const uint64_t tiles = lm * ((N + c.bn - 1) / c.bn);
+        const uint64_t units = c.tm == 256 ? std::max(1u, sms / 2) : sms;
+        const double cost = static_cast<double>((tiles + units - 1) / units) * c.bn / c.eff;
+        if (cost < best * 0.999) {
+            best = cost;
+            out.tm = c.tm;
+            out.bn = c.bn;
+        }
+    }
+    return best < 1e300 ? BST_OK : BST_ERR_UNSUPPORTED;
+}
+
 CUtensorMapDataType tmap_type(bst_dtype t) {
     if (t == BST_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (t == BST_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -260,16 +296,18 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     if (K == 0)
         return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, sc, M, N, batch, csize, dev.sms, stream));
 
-    const uint64_t loops_m = (M + kBM - 1) / kBM;
-    const uint32_t bn = sch.tile_n ? sch.tile_n : choose_bn(loops_m * batch, N, dev.sms, true);
-    const uint64_t tiles = loops_m * ((N + bn - 1) / bn) * batch;
+    TileChoice tc;
+    if (bst_status s = choose_tile(sch, tma_ok(a) && tma_ok(b), false, M, batch, N, dev.sms, tc)) return s;
+    const uint32_t bn = tc.bn;
+    const bool pair = tc.tm == 256;
+    const uint64_t tiles = ((M + tc.tm - 1) / tc.tm) * ((N + bn - 1) / bn) * batch;
     if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
-    if (smem_dense(bn, 0) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+    if ((pair ? smem_pair(bn, 0) : smem_dense(bn, 0)) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, tmap_type(at), false)) return s;
-    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, bn, tmap_type(bt), false)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, pair ? bn / 2 : bn, tmap_type(bt), false)) return s;
     p.g.M = M; p.g.N = N; p.g.K = K;
     p.g.batch = batch;
     p.g.mode = mode;
@@ -292,6 +330,9 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    if (pair)
+        return cuda_status(launch_pair(p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
+                                       stream));
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_dense(p, bn, grid, stream));
 }
@@ -309,7 +350,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     if (bst_status s = read_sched(sched_in, sch)) return s;
     if (la != BST_ROW_MAJOR || lb != BST_COL_MAJOR) return BST_ERR_UNSUPPORTED;
     if (K % 128) return BST_ERR_UNSUPPORTED;
-    if (sch.tile_n == 64) return BST_ERR_UNSUPPORTED;
+    if (sch.tile_n == 64 || sch.tile_m == 256) return BST_ERR_UNSUPPORTED;
     if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return BST_OK;
     if (!C || (K > 0 && (!A || !B || !sfa || !sfb))) return BST_ERR_INVALID_ARG;
@@ -417,17 +458,20 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
     if (K == 0)
         return cuda_status(
             launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, total_m, N, 1, csize, dev.sms, stream));
-    // an upper bound of the tile count: sum ceil(M_g/128) <= total_m/128 + G
-    const uint64_t loops_m_bound = (total_m + kBM - 1) / kBM + G;
-    const uint32_t bn = sch.tile_n ? sch.tile_n : choose_bn(loops_m_bound, N, dev.sms, true);
+    TileChoice tc;
+    if (bst_status s = choose_tile(sch, tma_ok(a) && tma_ok(b), true, total_m, G, N, dev.sms, tc)) return s;
+    const uint32_t bn = tc.bn;
+    const bool pair = tc.tm == 256;
+    // an upper bound of the tile count: sum ceil(M_g/tm) <= total_m/tm + G
+    const uint64_t loops_m_bound = (total_m + tc.tm - 1) / tc.tm + G;
     const uint64_t tiles_bound = loops_m_bound * ((N + bn - 1) / bn);
     if (tiles_bound >= (1ull << 32)) return BST_ERR_INVALID_ARG;
-    if (smem_dense(bn, G) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+    if ((pair ? smem_pair(bn, G) : smem_dense(bn, G)) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, tmap_type(ab_type), false)) return s;
-    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, bn, tmap_type(ab_type), false)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, pair ? bn / 2 : bn, tmap_type(ab_type), false)) return s;
     p.g.M = 0; p.g.N = N; p.g.K = K;
     p.g.batch = 1;
     p.g.mode = kModeGrouped;
@@ -450,6 +494,9 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    if (pair)
+        return cuda_status(launch_pair(
+            p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles_bound)), stream));
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles_bound));
     return cuda_status(launch_dense(p, bn, grid, stream));
 }
@@ -474,7 +521,7 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     if (b_layout != BST_ROW_MAJOR && b_layout != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
     Sched sch;
     if (bst_status s = read_sched(sched_in, sch)) return s;
-    if (sch.tile_n != 0 && sch.tile_n != 128) return BST_ERR_UNSUPPORTED;
+    if ((sch.tile_n != 0 && sch.tile_n != 128) || sch.tile_m == 256) return BST_ERR_UNSUPPORTED;
     if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
     if (lda < 1 || lda < K) return BST_ERR_INVALID_ARG;
     if (ldb < 1 || ldb < (b_layout == BST_COL_MAJOR ? K : N)) return BST_ERR_INVALID_ARG;

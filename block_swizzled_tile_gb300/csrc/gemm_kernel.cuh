@@ -42,7 +42,10 @@ enum : uint32_t { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
 
 constexpr uint32_t kBM = 128;          // tile rows = TMEM lanes
 constexpr uint32_t kLine = 128;        // bytes per k-block line
-constexpr uint32_t kNumThreads = 192;
+constexpr uint32_t kNumThreads = 192;   // warps: 0 TMA, 1 MMA, 2-5 epilogue
+constexpr uint32_t kScaleWarp = 6;      // MXFP8 only: a 7th warp copies scale factors
+template <uint32_t KIND>
+constexpr uint32_t threads_for() { return KIND == 1 ? kNumThreads + 32 : kNumThreads; }
 constexpr uint32_t kMaxGroups = 1024;
 
 struct OperandDesc {
@@ -142,27 +145,69 @@ struct TileInfo {
     uint32_t m_lim;    // rows of A that exist (loads past it read zeros)
 };
 
-__device__ __forceinline__ TileInfo tile_info(const SchedArgs& sa, uint32_t t, uint32_t BN, const GroupTable& gt) {
+// Task t -> tile of TM x BN (TM = 128 for one CTA, 256 for a CTA pair).
+__device__ __forceinline__ TileInfo tile_info(const SchedArgs& sa, uint32_t t, uint32_t TM, uint32_t BN,
+                                              const GroupTable& gt) {
     TileInfo ti;
     SwizzleSched s;
     if (sa.mode == kModeGrouped) {
         const uint32_t g = gt.find(t);
         const uint32_t mg = gt.row_off[g + 1] - gt.row_off[g];
-        s.update(mg, sa.N, kBM, BN, sa.swz_offset, sa.swz_dir);
+        s.update(mg, sa.N, TM, BN, sa.swz_offset, sa.swz_dir);
         s.block_coord(t - gt.tile_off[g], ti.m, ti.n);
         s.actual_shape(ti.m, ti.n, ti.m_act, ti.n_act);
         ti.tag = g;
-        ti.row0 = gt.row_off[g] + ti.m * kBM;
+        ti.row0 = gt.row_off[g] + ti.m * TM;
         ti.m_lim = sa.total_m;
     } else {
-        s.update(sa.M, sa.N, kBM, BN, sa.swz_offset, sa.swz_dir);
+        s.update(sa.M, sa.N, TM, BN, sa.swz_offset, sa.swz_dir);
         ti.tag = s.batch_idx(t);
         s.block_coord(t, ti.m, ti.n);
         s.actual_shape(ti.m, ti.n, ti.m_act, ti.n_act);
-        ti.row0 = ti.m * kBM;
+        ti.row0 = ti.m * TM;
         ti.m_lim = sa.M;
     }
     return ti;
+}
+
+// Grouped slice-M: one warp computes the exclusive prefix sums of rows and of
+// tiles (tile_m x tile_n) over the groups into shared memory and stores the
+// task count in *tiles_out; inconsistent sizes (a negative size, or more rows
+// than total_m) give no tasks and raise the error word.
+__device__ __forceinline__ void build_group_table(const GroupTable& gt, const int32_t* group_m, uint32_t G, uint32_t N,
+                                                  uint32_t TM, uint32_t BN, uint32_t total_m, uint32_t* err,
+                                                  uint32_t* tiles_out, uint32_t lane) {
+    const uint32_t loops_n = (N + BN - 1) / BN;
+    uint32_t row_carry = 0, tile_carry = 0, bad = 0;
+    if (lane == 0) { gt.row_off[0] = 0; gt.tile_off[0] = 0; }
+    for (uint32_t base = 0; base < G; base += 32) {
+        const uint32_t g = base + lane;
+        int32_t mg = g < G ? group_m[g] : 0;
+        if (mg < 0) { bad = 1; mg = 0; }
+        uint32_t rows = static_cast<uint32_t>(mg);
+        uint32_t tiles = ((rows + TM - 1) / TM) * loops_n;
+#pragma unroll
+        for (uint32_t d = 1; d < 32; d <<= 1) {
+            const uint32_t r = __shfl_up_sync(0xFFFFFFFFu, rows, d);
+            const uint32_t tt = __shfl_up_sync(0xFFFFFFFFu, tiles, d);
+            if (lane >= d) { rows += r; tiles += tt; }
+        }
+        if (g < G) {
+            gt.row_off[g + 1] = row_carry + rows;
+            gt.tile_off[g + 1] = tile_carry + tiles;
+        }
+        row_carry += __shfl_sync(0xFFFFFFFFu, rows, 31);
+        tile_carry += __shfl_sync(0xFFFFFFFFu, tiles, 31);
+    }
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+        if (bad || row_carry > total_m) {
+            *tiles_out = 0;
+            if (blockIdx.x == 0) atomicOr(&err[0], kErrGroups);
+        } else {
+            *tiles_out = tile_carry;
+        }
+    }
 }
 
 // Fallback for operands TMA cannot fetch (pitch or base not 16-byte
@@ -271,7 +316,7 @@ __device__ __forceinline__ void store_row_chunk(uint32_t c_type, uint32_t c_vec,
 }
 
 template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND, uint32_t EPI>
-__global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_constant__ GemmParams prm) {
+__global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __grid_constant__ GemmParams prm) {
     using Lay = GemmLayout<BN, STAGES, ACC, KIND>;
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
     static_assert(EPI == kEpiStore || BN == 128, "dequant epilogue keeps 128 int32 per thread");
@@ -333,41 +378,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         tmem_alloc(tmem_holder, Lay::kTmemCols);
         tmem_relinquish();
     }
-    if (mode == kModeGrouped && warp == 2) {
-        // exclusive prefix sums of rows and tiles over the groups (warp scan)
-        const uint32_t loops_n = (N + BN - 1) / BN;
-        const int32_t* group_m = prm.g.group_m;
-        uint32_t row_carry = 0, tile_carry = 0, bad = 0;
-        if (lane == 0) { gt.row_off[0] = 0; gt.tile_off[0] = 0; }
-        for (uint32_t base = 0; base < G; base += 32) {
-            const uint32_t g = base + lane;
-            int32_t mg = g < G ? group_m[g] : 0;
-            if (mg < 0) { bad = 1; mg = 0; }
-            uint32_t rows = static_cast<uint32_t>(mg);
-            uint32_t tiles = ((rows + kBM - 1) / kBM) * loops_n;
-#pragma unroll
-            for (uint32_t d = 1; d < 32; d <<= 1) {
-                const uint32_t r = __shfl_up_sync(0xFFFFFFFFu, rows, d);
-                const uint32_t tt = __shfl_up_sync(0xFFFFFFFFu, tiles, d);
-                if (lane >= d) { rows += r; tiles += tt; }
-            }
-            if (g < G) {
-                gt.row_off[g + 1] = row_carry + rows;
-                gt.tile_off[g + 1] = tile_carry + tiles;
-            }
-            row_carry += __shfl_sync(0xFFFFFFFFu, rows, 31);
-            tile_carry += __shfl_sync(0xFFFFFFFFu, tiles, 31);
-        }
-        bad = __any_sync(0xFFFFFFFFu, bad);
-        if (lane == 0) {
-            if (bad || row_carry > sa.total_m) {
-                *tiles_smem = 0;
-                if (blockIdx.x == 0) atomicOr(&err[0], kErrGroups);
-            } else {
-                *tiles_smem = tile_carry;
-            }
-        }
-    }
+    if (mode == kModeGrouped && warp == 2)
+        build_group_table(gt, prm.g.group_m, G, N, kBM, BN, sa.total_m, err, tiles_smem, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -376,7 +388,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
 
-    if (warp == 0) {
+    if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp)) {
         // ------------------------------------------------------ producer --
         const uint8_t* a_ptr = prm.g.a.ptr;
         const uint8_t* b_ptr = prm.g.b.ptr;
@@ -388,74 +400,86 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         const uint32_t sf_ld = prm.g.sf_ld;
         const bool plain_stores = (!a_tma && a_vec < 4) || (!b_tma && b_vec < 4);
         const uint32_t tx = (a_tma ? Lay::kABytes : 0u) + (b_tma ? Lay::kBBytes : 0u);
-        uint32_t stage = 0, phase = 0, issued = 0;
-        bool ok = true;
-        for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = tile_info(sa, t, BN, gt);
-            const uint32_t n0 = ti.n * BN;
-            const int32_t zc = static_cast<int32_t>(ti.tag);
-            for (uint32_t kb = 0; kb < num_kb; ++kb) {
-                if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
-                uint8_t* sa_s = smem + stage * Lay::kStageBytes;
-                uint8_t* sb_s = sa_s + Lay::kABytes;
-                const uint32_t k0 = kb * bk_elems;
-                if (KIND == kKindMXF8) {
-                    // scale factors for this k-block, written straight into the
-                    // order tcgen05.cp 32x128b.warpx4 expects: 16-byte line r%32
-                    // holds rows r%32, +32, +64, +96 (4 bytes each = the 4
-                    // E8M0 codes of the k-block's four 32-element sub-blocks)
-                    uint8_t* sfa_s = smem + Lay::kSfOff + stage * Lay::kSfStageBytes;
-                    uint8_t* sfb_s = sfa_s + Lay::kSfaBytes;
-#pragma unroll
-                    for (uint32_t i = 0; i < 4; ++i) {
-                        const uint32_t r = lane + 32 * i;
-                        const bool v = ti.row0 + r < ti.m_lim;
-                        const uint8_t* src = v ? sfa + static_cast<int64_t>(ti.row0 + r) * sf_ld + kb * 4 : sfa;
-                        cp_async_4(sfa_s + (lane * 4 + i) * 4, src, v ? 4u : 0u);
-                    }
-#pragma unroll
-                    for (uint32_t h = 0; h < (BN >= 128 ? BN / 128 : 0u); ++h) {
+        // Fast path: one thread issues every TMA load (a loop run by a single
+        // lane costs far fewer cycles per k-block than the same loop run by a
+        // whole warp with one active lane).  Lanes copy only for the MXFP8
+        // scale factors (their own warp) and for operands TMA cannot fetch.
+        const bool tma_thread = (warp == 0 && lane == 0);
+        const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp) : (warp == 0 && lanes_copy);
+        if (tma_thread || warp_copies) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
+                const uint32_t n0 = ti.n * BN;
+                const int32_t zc = static_cast<int32_t>(ti.tag);
+                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                    const bool got = warp_copies ? warp_wait(&empty[stage], phase ^ 1u, ctl, 1)
+                                                 : mbar_wait(&empty[stage], phase ^ 1u, ctl, 1);
+                    if (!got) { ok = false; break; }
+                    uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+                    uint8_t* sb_s = sa_s + Lay::kABytes;
+                    const uint32_t k0 = kb * bk_elems;
+                    if (KIND == kKindMXF8 && warp_copies) {
+                        // scale factors for this k-block, written straight into the
+                        // order tcgen05.cp 32x128b.warpx4 expects: 16-byte line r%32
+                        // holds rows r%32, +32, +64, +96 (4 bytes each = the 4
+                        // E8M0 codes of the k-block's four 32-element sub-blocks)
+                        uint8_t* sfa_s = smem + Lay::kSfOff + stage * Lay::kSfStageBytes;
+                        uint8_t* sfb_s = sfa_s + Lay::kSfaBytes;
 #pragma unroll
                         for (uint32_t i = 0; i < 4; ++i) {
-                            const uint32_t r = 128 * h + lane + 32 * i;
-                            const bool v = n0 + r < N;
-                            const uint8_t* src = v ? sfb + static_cast<int64_t>(n0 + r) * sf_ld + kb * 4 : sfb;
-                            cp_async_4(sfb_s + h * 512 + (lane * 4 + i) * 4, src, v ? 4u : 0u);
+                            const uint32_t r = lane + 32 * i;
+                            const bool v = ti.row0 + r < ti.m_lim;
+                            const uint8_t* src = v ? sfa + static_cast<int64_t>(ti.row0 + r) * sf_ld + kb * 4 : sfa;
+                            cp_async_4(sfa_s + (lane * 4 + i) * 4, src, v ? 4u : 0u);
+                        }
+#pragma unroll
+                        for (uint32_t h = 0; h < (BN >= 128 ? BN / 128 : 0u); ++h) {
+#pragma unroll
+                            for (uint32_t i = 0; i < 4; ++i) {
+                                const uint32_t r = 128 * h + lane + 32 * i;
+                                const bool v = n0 + r < N;
+                                const uint8_t* src = v ? sfb + static_cast<int64_t>(n0 + r) * sf_ld + kb * 4 : sfb;
+                                cp_async_4(sfb_s + h * 512 + (lane * 4 + i) * 4, src, v ? 4u : 0u);
+                            }
+                        }
+                        cp_async_arrive_noinc(&full[stage]);
+                    } else if (KIND != kKindMXF8 && warp_copies) {
+                        if (!a_tma)
+                            load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec,
+                                            esize, kBM, ti.row0, ti.m_lim, k0, K, lane);
+                        if (!b_tma)
+                            load_tile_plain(sb_s,
+                                            b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
+                                            b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane);
+                        if (plain_stores) {
+                            cp_async_wait_all();         // the other operand may have used cp.async
+                            fence_proxy_async_smem();
+                            mbar_arrive(&full[stage]);
+                        } else {
+                            cp_async_arrive_noinc(&full[stage]);
                         }
                     }
-                    cp_async_arrive_noinc(&full[stage]);
-                } else if (lanes_copy) {
-                    if (!a_tma)
-                        load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec, esize,
-                                        kBM, ti.row0, ti.m_lim, k0, K, lane);
-                    if (!b_tma)
-                        load_tile_plain(sb_s, b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
-                                        b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane);
-                    if (plain_stores) {
-                        cp_async_wait_all();         // the other operand may have used cp.async
-                        fence_proxy_async_smem();
-                        mbar_arrive(&full[stage]);
-                    } else {
-                        cp_async_arrive_noinc(&full[stage]);
+                    if (tma_thread) {
+                        mbar_arrive_expect_tx(&full[stage], tx);
+                        if (a_tma)
+                            tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
+                        if (b_tma) tma_tile(&prm.tmap_b, sb_s, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
+                        if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
                     }
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[stage], tx);
-                    if (a_tma) tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
-                    if (b_tma) tma_tile(&prm.tmap_b, sb_s, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
-                    if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
-                }
-                ++issued;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
-        }
-        if (!ok) {
-            // let every copy already issued land before the CTA exits
-            uint32_t s = stage, ph = phase;
-            const uint32_t pending = issued < STAGES ? issued : STAGES;
-            for (uint32_t i = 0; i < pending; ++i) {
-                if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
-                mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
+            if (!ok && tma_thread) {
+                // let every copy already issued land before the CTA exits
+                uint32_t s = stage, ph = phase;
+                const uint32_t pending = issued < STAGES ? issued : STAGES;
+                for (uint32_t i = 0; i < pending; ++i) {
+                    if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
+                    mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
+                }
             }
         }
     } else if (warp == 1) {
@@ -470,20 +494,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
         bool ok = true, any_mma = false;
         const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
-        for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        // one thread issues every MMA (a single-lane loop, see the producer)
+        for (uint32_t t = blockIdx.x; lane == 0 && ok && t < total_tiles; t += gridDim.x) {
             for (uint32_t c = 0; ok && c < nchunks; ++c) {
                 const uint32_t kb_begin = c * chunk_kb;
                 const uint32_t kb_end = min(num_kb, kb_begin + chunk_kb);
-                if (!warp_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!warp_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
+                    if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
                     // stages written by cp.async / plain stores need a proxy
                     // fence before tcgen05 reads them
                     if (lanes_copy) fence_proxy_async_smem();
-                    if (lane == 0) {
+                    {
                         if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
                         const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
                         const uint32_t sb_addr = sa_addr + Lay::kABytes;
@@ -512,22 +537,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
                     }
                     ++mma_kb;
                     any_mma = true;
-                    __syncwarp();
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if (lane == 0) umma_commit(&tfull[acc]);
-                __syncwarp();
+                umma_commit(&tfull[acc]);
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
             }
         }
-        if (!ok && any_mma) {
+        if (lane == 0 && !ok && any_mma) {
             // every tcgen05 op issued so far must finish before TMEM is freed
-            if (lane == 0) umma_commit(drain);
-            __syncwarp();
+            umma_commit(drain);
             mbar_wait_drain(drain, 0, ctl.timeout_ns);
         }
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ----------------------------------------------------- epilogue --
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread
@@ -544,7 +566,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_kernel(const __grid_const
         uint32_t acc = 0, acc_phase = 0, ep_tile = 0;
         bool ok = true;
         for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = tile_info(sa, t, BN, gt);
+            const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
             if (trace && warp == 2 && lane == 0) {
                 if (t < trace_cap) {
                     uint32_t* tr = trace + static_cast<uint64_t>(t) * 5;

@@ -15,7 +15,7 @@ static cudaError_t launch_one(const GemmParams& p, uint32_t grid, cudaStream_t s
     const uint32_t smem = Lay::smem_bytes(0);
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, attr_done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kNumThreads, smem, stream>>>(p);
+    kern<<<grid, threads_for<kKindMXF8>(), smem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "gemm_kernel.cuh"
@@ -28,11 +29,15 @@ inline cudaError_t set_smem_once(const void* kern, uint32_t bytes, std::atomic<u
 cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
 cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
 cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stream);
+// CTA-pair kernel: launches clusters of 2, at most max_pairs of them (and no
+// more than fit on the device at once)
+cudaError_t launch_pair(const GemmParams& p, uint32_t bn, uint32_t max_pairs, cudaStream_t stream);
 
 // Shared-memory bytes a launch needs (for validation of the device limit).
 uint32_t smem_dense(uint32_t bn, uint32_t groups);
 uint32_t smem_mxf8(uint32_t bn);
 uint32_t smem_dequant();
+uint32_t smem_pair(uint32_t bn, uint32_t groups);
 
 // int8 [rows, cols] (ld_src elements) -> bf16 [rows, cols] (ld_dst elements)
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
@@ -52,6 +57,7 @@ cudaError_t launch_swizzle_map_grouped(const int32_t* group_m, uint32_t G, uint3
 constexpr uint32_t kDenseStages64 = 8, kDenseStages128 = 6, kDenseStages256 = 4;
 constexpr uint32_t kMxStages128 = 6, kMxStages256 = 4;
 constexpr uint32_t kDequantStages = 6;
+constexpr uint32_t kPairStages128 = 8, kPairStages256 = 6;
 constexpr uint32_t kDequantChunkK = 1024;  // K elements per exact fp32 chunk
 
 }  // namespace bst

@@ -71,7 +71,11 @@ typedef enum { BST_ROW_MAJOR = 0, BST_COL_MAJOR = 1 } bst_layout;
 typedef struct {
     uint32_t swizzle_offset;    /* SwizzleOffset, >= 1 (0 is rejected)                 */
     uint32_t swizzle_direction; /* SwizzleDirection: 0 = Zn, 1 = Nz                    */
-    uint32_t tile_n;            /* 0 = automatic, else 64, 128 or 256 (tile_m is 128)  */
+    uint32_t tile_n;            /* 0 = automatic, else 64, 128 or 256                   */
+    uint32_t tile_m;            /* 0 = automatic, 128 (one CTA per tile) or 256 (a pair
+                                   of CTAs on one TPC per tile, tcgen05 cta_group::2;
+                                   fp16/bf16 with 16-byte-aligned operands, tile_n 128
+                                   or 256)                                             */
     uint32_t num_ctas;          /* persistent CTAs; 0 = one per SM                      */
     uint32_t* trace;            /* optional DEVICE buffer of 5 uint32 per task; when
                                    non-NULL the kernel writes, for task index t, the

@@ -84,7 +84,7 @@ def test_fp16_tail_workload(d):
     w = wl.fp16_tail()
     ntiles = 4 * 3
     trace = torch.zeros(ntiles * 5, dtype=torch.int32, device="cuda")
-    got = run_dense(w, "f16", bst.sched(3, d, tile_n=128, trace=trace))
+    got = run_dense(w, "f16", bst.sched(3, d, tile_n=128, tile_m=128, trace=trace))
     assert_close_f16(got, oracle_dense(w, "f16"))
     tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
     assert np.array_equal(tr, np.array(osw.swizzle_map(500, 380, 128, 128, 3, d), dtype=np.uint32))
@@ -107,7 +107,7 @@ def test_fp16_square_trace_per_tile_width():
     for tn in (64, 128, 256):
         tiles = 8 * (1024 // tn)
         trace = torch.zeros(tiles * 5, dtype=torch.int32, device="cuda")
-        got = run_dense(w, "f16", bst.sched(2, 0, tile_n=tn, trace=trace))
+        got = run_dense(w, "f16", bst.sched(2, 0, tile_n=tn, tile_m=128, trace=trace))
         assert_close_f16(got, ref)
         tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
         assert np.array_equal(tr, np.array(osw.swizzle_map(1024, 1024, 128, tn, 2, 0), dtype=np.uint32))
@@ -183,7 +183,7 @@ def test_batched(acol, bcol):
     trace_tiles = batch * 2 * 2
     trace = torch.zeros(trace_tiles * 5, dtype=torch.int32, device="cuda")
     bst.gemm_batched(M, N, K, A, bst.BF16, _layout(acol), w["lda"], sa, B, bst.BF16, _layout(bcol), w["ldb"], sb,
-                     C, bst.BF16, N, M * N, batch, sched=bst.sched(1, 0, tile_n=128, trace=trace))
+                     C, bst.BF16, N, M * N, batch, sched=bst.sched(1, 0, tile_n=128, tile_m=128, trace=trace))
     bst.check_async()
     assert canary_intact(cbuf, CANARY)
     got = decode_out(host(C, np.uint16).reshape(batch, M, N).copy(), "bf16")
@@ -193,3 +193,60 @@ def test_batched(acol, bcol):
         assert_close_f16(got[i], decode_out(og.gemm(a, b, "bf16"), "bf16"))
     tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
     assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, 128, 1, 0, batch=batch), dtype=np.uint32))
+
+
+# ------------------------------------------------- CTA-pair (256-row) ------
+
+PAIR_SHAPES = [(256, 256, 64), (300, 200, 136), (513, 384, 1000), (1, 136, 72)]
+
+
+@pytest.mark.parametrize("mnk", PAIR_SHAPES)
+@pytest.mark.parametrize("acol,bcol", [(False, False), (False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("tn", [128, 256])
+def test_pair_shapes_layouts(mnk, acol, bcol, tn):
+    M, N, K = mnk
+    up8 = lambda x: -(-x // 8) * 8           # 16-byte pitches, so both operands can use TMA
+    w = wl.dense16(M, N, K, "bf16", a_col_major=acol, b_col_major=bcol, seed=M + 3 * N + K,
+                   lda=up8(M if acol else K), ldb=up8(K if bcol else N))
+    lm, ln = -(-M // 256), -(-N // tn)
+    trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
+    got = run_dense(w, "bf16", bst.sched(2, 1, tile_n=tn, tile_m=256, trace=trace))
+    assert_close_f16(got, oracle_dense(w, "bf16"))
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 256, tn, 2, 1), dtype=np.uint32))
+
+
+@pytest.mark.parametrize("S,d", [(1, 0), (2, 0), (4, 1), (8, 1)])
+def test_pair_fp16_square_workload(S, d):
+    w = wl.fp16_square()
+    trace = torch.zeros(16 * 5, dtype=torch.int32, device="cuda")
+    got = run_dense(w, "f16", bst.sched(S, d, tile_n=256, tile_m=256, trace=trace))
+    assert_close_f16(got, oracle_dense(w, "f16"))
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(1024, 1024, 256, 256, S, d), dtype=np.uint32))
+
+
+def test_pair_needs_tma_operands():
+    """A CTA pair fetches both operands with TMA; forcing it on a 260-byte
+    pitch is refused instead of silently changing the schedule."""
+    w = wl.dense16(64, 130, 72, "f16", b_col_major=False, seed=1)
+    with pytest.raises(bst.BstError) as e:
+        run_dense(w, "f16", bst.sched(1, 0, tile_m=256))
+    assert e.value.status == bst.ERR_UNSUPPORTED
+    assert_close_f16(run_dense(w, "f16", bst.sched(1, 0)), oracle_dense(w, "f16"))
+
+
+def test_pair_batched():
+    M, N, K, batch = 300, 256, 200, 3
+    w = wl.dense16(M, N, K, "f16", b_col_major=True, seed=4, batch=batch)
+    A, B = dev(w["a"]), dev(w["b"])
+    cbuf, C = empty_bytes(batch * M * N * 2, CANARY)
+    bst.gemm_batched(M, N, K, A, bst.F16, bst.ROW_MAJOR, w["lda"], w["a"][0].size, B, bst.F16, bst.COL_MAJOR,
+                     w["ldb"], w["b"][0].size, C, bst.F16, N, M * N, batch, sched=bst.sched(1, 0, tile_m=256))
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY)
+    got = decode_out(host(C, np.uint16).reshape(batch, M, N).copy(), "f16")
+    for i in range(batch):
+        a = og.as_logical(og.decode(w["a"][i], "f16"), M, K, w["lda"], False)
+        b = og.as_logical(og.decode(w["b"][i], "f16"), K, N, w["ldb"], True)
+        assert_close_f16(got[i], decode_out(og.gemm(a, b, "f16"), "f16"))

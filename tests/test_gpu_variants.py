@@ -54,19 +54,19 @@ def oracle_grouped_rows(w, rows, out="bf16"):
     return res
 
 
-@pytest.mark.parametrize("gm", [[3, 0, 130, 1, 0, 257], [0, 0, 64], [200], [1] * 17])
+@pytest.mark.parametrize("gm", [[3, 0, 130, 1, 0, 257], [0, 0, 64], [200], [1] * 17, [300, 0, 513]])
 @pytest.mark.parametrize("bcol", [False, True])
 def test_grouped_small(gm, bcol):
     w = wl.grouped_bf16(group_m=gm, N=200, K=136, seed=len(gm))
     total = sum(gm)
-    for S, d, tn in [(1, 0, 128), (2, 1, 64), (3, 0, 256)]:
+    for S, d, tm, tn in [(1, 0, 128, 128), (2, 1, 128, 64), (3, 0, 128, 256), (1, 1, 256, 256), (2, 0, 256, 128)]:
         G = len(gm)
-        cap = (-(-total // 128) + G) * -(-200 // tn)
+        cap = (-(-total // tm) + G) * -(-200 // tn)
         trace = torch.full((cap * 5,), -1, dtype=torch.int32, device="cuda")
-        got = run_grouped(w, bst.sched(S, d, tile_n=tn, trace=trace), b_col_major=bcol)
+        got = run_grouped(w, bst.sched(S, d, tile_n=tn, tile_m=tm, trace=trace), b_col_major=bcol)
         ref = decode_out(og.gemm_grouped(og.decode(w["x"], "bf16"), og.decode(w["w"], "bf16"), gm, "bf16"), "bf16")
         assert_close_f16(got, ref)
-        want = np.array(osw.grouped_swizzle_map(gm, 200, 128, tn, S, d), dtype=np.uint32).reshape(-1, 5)
+        want = np.array(osw.grouped_swizzle_map(gm, 200, tm, tn, S, d), dtype=np.uint32).reshape(-1, 5)
         tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)[:len(want)]
         assert np.array_equal(tr, want)
 
@@ -84,10 +84,11 @@ def test_grouped_inconsistent_sizes_reported():
 
 
 @pytest.mark.parametrize("forced", [None, [0, 2048, 0, 1024, 3072, 0, 2048, 0]])
-def test_grouped_full_workload(forced):
+@pytest.mark.parametrize("tm", [0, 128, 256])
+def test_grouped_full_workload(forced, tm):
     """G=8 groups summing to 8192 rows, K=N=4096, bf16; sampled rows."""
     w = wl.grouped_bf16(group_m=forced)
-    got = run_grouped(w)
+    got = run_grouped(w, bst.sched(1, 0, tile_m=tm))
     rng = np.random.default_rng(0)
     rows = np.sort(rng.choice(sum(w["group_m"]), 384, replace=False))
     assert_close_f16(got[rows], oracle_grouped_rows(w, rows))

@@ -330,17 +330,16 @@ def total_rows(work):
 def cpu_rate(work, budget_s):
     """Oracle throughput on a sample of whole output rows sized to about
     budget_s of CPU time (the whole problem, repeated, when that is smaller).
-    Returns (TFLOP/s, sample description, seconds)."""
-    rows = 8
-    t = time.perf_counter()
-    oracle_rows(work, rows)
-    dt = max(time.perf_counter() - t, 1e-6)
-    want = rows * budget_s / dt
+    Each oracle call decodes its operands, so the calibration run uses all
+    rows.  Returns (TFLOP/s, sample description, seconds)."""
     total = total_rows(work)
-    if want <= total:
-        rows, reps = int(max(8, want)), 1
+    t = time.perf_counter()
+    oracle_rows(work, total)
+    dt_full = max(time.perf_counter() - t, 1e-6)
+    if dt_full >= budget_s:
+        rows, reps = max(8, int(total * budget_s / dt_full)), 1
     else:
-        rows, reps = total, int(max(1, round(want / total)))
+        rows, reps = total, max(1, int(round(budget_s / dt_full)))
     t = time.perf_counter()
     fl = sum(oracle_rows(work, rows) for _ in range(reps))
     dt = time.perf_counter() - t

@@ -6,10 +6,11 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
-#include "../../include/bst.h"
+#include "bst.h"
 #include "internal.h"
 
 namespace bst {
@@ -243,6 +244,30 @@ bst_status choose_tile(const Sched& sch, bool pair_ok, bool grouped, uint64_t M,
     return best < 1e300 ? BST_OK : BST_ERR_UNSUPPORTED;
 }
 
+// Small problems are bound by the DRAM latency of their first touches: when
+// the operands' storage fits well inside L2 the kernel prefetches all of it
+// at start.  BST_PREFETCH_MB sets the limit (0 disables).
+void set_prefetch(GemmArgs& g, const OperandSpec& a, const OperandSpec& b, const uint8_t* s1, uint64_t s1_bytes,
+                  const uint8_t* s2, uint64_t s2_bytes) {
+    static const uint64_t limit = [] {
+        const char* e = std::getenv("BST_PREFETCH_MB");
+        return (e ? std::strtoull(e, nullptr, 10) : 32ull) << 20;
+    }();
+    auto span = [](const OperandSpec& o) {
+        const uint64_t rows = o.mn_major ? o.k : o.mn;          // rows of storage
+        const uint64_t per = static_cast<uint64_t>(o.ld) * (rows ? rows - 1 : 0) + (o.mn_major ? o.mn : o.k);
+        const uint64_t slab = per * o.esize;
+        return o.batch > 1 ? static_cast<uint64_t>(o.batch_stride) * o.esize * (o.batch - 1) + slab : slab;
+    };
+    const uint64_t ab = span(a), bb = span(b);
+    for (int i = 0; i < 4; ++i) { g.pf_ptr[i] = nullptr; g.pf_bytes[i] = 0; }
+    if (ab + bb + s1_bytes + s2_bytes > limit) return;
+    g.pf_ptr[0] = static_cast<const uint8_t*>(a.ptr); g.pf_bytes[0] = ab;
+    g.pf_ptr[1] = static_cast<const uint8_t*>(b.ptr); g.pf_bytes[1] = bb;
+    g.pf_ptr[2] = s1; g.pf_bytes[2] = s1 ? s1_bytes : 0;
+    g.pf_ptr[3] = s2; g.pf_bytes[3] = s2 ? s2_bytes : 0;
+}
+
 CUtensorMapDataType tmap_type(bst_dtype t) {
     if (t == BST_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (t == BST_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -329,6 +354,7 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.trace_cap = static_cast<uint32_t>(tiles);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (pair)
         return cuda_status(launch_pair(p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
@@ -394,6 +420,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.trace_cap = static_cast<uint32_t>(tiles);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    set_prefetch(p.g, a, b, sfa, static_cast<uint64_t>(M) * (K / 32), sfb, static_cast<uint64_t>(N) * (K / 32));
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_mxf8(p, bn, grid, stream));
@@ -493,6 +520,7 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
     p.g.trace_cap = static_cast<uint32_t>(tiles_bound);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (pair)
         return cuda_status(launch_pair(

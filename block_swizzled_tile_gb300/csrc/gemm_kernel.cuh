@@ -89,7 +89,25 @@ struct GemmArgs {
     uint64_t* timeline;     // optional: 64 %globaltimer stamps per CTA
     uint32_t* err;
     uint64_t timeout_ns;
+    // operand byte ranges pulled into L2 at kernel start (small problems,
+    // whose loads would otherwise each wait for DRAM); bytes 0 = none
+    const uint8_t* pf_ptr[4];
+    uint64_t pf_bytes[4];
 };
+
+// Each CTA's epilogue threads (idle until the first accumulator is ready)
+// issue L2 prefetches for an interleaved 1/grid share of the ranges, so every
+// line is requested once and the DRAM fetch of the whole footprint starts
+// immediately instead of trickling in behind the TMA loads.
+__device__ __forceinline__ void prefetch_operands(const GemmArgs& g, uint32_t tid, uint32_t nthreads) {
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * nthreads;
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r) {
+        const uint64_t lines = (g.pf_bytes[r] + 127) / 128;
+        for (uint64_t L = static_cast<uint64_t>(blockIdx.x) * nthreads + tid; L < lines; L += stride)
+            prefetch_l2(g.pf_ptr[r] + L * 128);
+    }
+}
 
 struct GemmParams {
     CUtensorMap tmap_a;
@@ -324,6 +342,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     // ---- arguments into registers, once
+    const uint64_t t_entry = globaltimer_ns();
     const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m};
     const uint32_t N = prm.g.N, K = prm.g.K, mode = prm.g.mode, esize = prm.g.esize;
     const uint32_t num_kb = prm.g.num_kb, chunk_kb = prm.g.chunk_kb, G = prm.g.G;
@@ -386,7 +405,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t total_tiles = *tiles_smem;
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
-    if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
+    if (tl && threadIdx.x == 0) { tl[0] = globaltimer_ns(); tl[55] = t_entry; }
 
     if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp)) {
         // ------------------------------------------------------ producer --
@@ -400,13 +419,62 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const uint32_t sf_ld = prm.g.sf_ld;
         const bool plain_stores = (!a_tma && a_vec < 4) || (!b_tma && b_vec < 4);
         const uint32_t tx = (a_tma ? Lay::kABytes : 0u) + (b_tma ? Lay::kBBytes : 0u);
-        // Fast path: one thread issues every TMA load (a loop run by a single
-        // lane costs far fewer cycles per k-block than the same loop run by a
-        // whole warp with one active lane).  Lanes copy only for the MXFP8
-        // scale factors (their own warp) and for operands TMA cannot fetch.
+        // The TMA thread runs a loop of its own that contains no warp-synchronous
+        // operation: mixing it with the warp-wide copy loop (whose waits end in
+        // __syncwarp / shfl.sync) made every iteration pay for reconvergence
+        // bookkeeping, and a tight single-thread loop issues a k-block in about
+        // half the time.  Lanes copy only for the MXFP8 scale factors (their own
+        // warp) and for operands TMA cannot fetch (warp 0, which then also
+        // carries the TMA issue).
         const bool tma_thread = (warp == 0 && lane == 0);
         const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp) : (warp == 0 && lanes_copy);
-        if (tma_thread || warp_copies) {
+        if (tma_thread && !warp_copies) {
+            const bool simple = !a_mn && !b_mn && !a_rank3 && !b_rank3;
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                if (tl && issued == 0) tl[56] = globaltimer_ns();
+                const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
+                const uint32_t n0 = ti.n * BN;
+                const int32_t zc = static_cast<int32_t>(ti.tag);
+                if (tl && issued == 0) tl[57] = globaltimer_ns();
+                if (simple) {
+                    // both operands K-contiguous, 2-D maps: one box each per k-block
+                    for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+                        uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+                        const int32_t k0 = static_cast<int32_t>(kb * bk_elems);
+                        mbar_arrive_expect_tx(&full[stage], tx);
+                        tma_load_2d(sa_s, &prm.tmap_a, &full[stage], k0, ti.row0);
+                        tma_load_2d(sa_s + Lay::kABytes, &prm.tmap_b, &full[stage], k0, n0);
+                        if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
+                        ++issued;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    continue;
+                }
+                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+                    uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+                    const uint32_t k0 = kb * bk_elems;
+                    mbar_arrive_expect_tx(&full[stage], tx);
+                    tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
+                    tma_tile(&prm.tmap_b, sa_s + Lay::kABytes, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
+                    if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA exits
+                uint32_t s = stage, ph = phase;
+                const uint32_t pending = issued < STAGES ? issued : STAGES;
+                for (uint32_t i = 0; i < pending; ++i) {
+                    if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
+                    mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
+                }
+            }
+        } else if (warp_copies) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
@@ -414,13 +482,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 const uint32_t n0 = ti.n * BN;
                 const int32_t zc = static_cast<int32_t>(ti.tag);
                 for (uint32_t kb = 0; kb < num_kb; ++kb) {
-                    const bool got = warp_copies ? warp_wait(&empty[stage], phase ^ 1u, ctl, 1)
-                                                 : mbar_wait(&empty[stage], phase ^ 1u, ctl, 1);
-                    if (!got) { ok = false; break; }
+                    if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     uint8_t* sb_s = sa_s + Lay::kABytes;
                     const uint32_t k0 = kb * bk_elems;
-                    if (KIND == kKindMXF8 && warp_copies) {
+                    if (KIND == kKindMXF8) {
                         // scale factors for this k-block, written straight into the
                         // order tcgen05.cp 32x128b.warpx4 expects: 16-byte line r%32
                         // holds rows r%32, +32, +64, +96 (4 bytes each = the 4
@@ -445,7 +511,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                             }
                         }
                         cp_async_arrive_noinc(&full[stage]);
-                    } else if (KIND != kKindMXF8 && warp_copies) {
+                    } else {
                         if (!a_tma)
                             load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec,
                                             esize, kBM, ti.row0, ti.m_lim, k0, K, lane);
@@ -460,20 +526,19 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         } else {
                             cp_async_arrive_noinc(&full[stage]);
                         }
-                    }
-                    if (tma_thread) {
-                        mbar_arrive_expect_tx(&full[stage], tx);
-                        if (a_tma)
-                            tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
-                        if (b_tma) tma_tile(&prm.tmap_b, sb_s, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
-                        if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
+                        if (tma_thread) {                // the TMA half of a mixed stage
+                            mbar_arrive_expect_tx(&full[stage], tx);
+                            if (a_tma)
+                                tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
+                            if (b_tma)
+                                tma_tile(&prm.tmap_b, sb_s, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
+                        }
                     }
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok && tma_thread) {
-                // let every copy already issued land before the CTA exits
                 uint32_t s = stage, ph = phase;
                 const uint32_t pending = issued < STAGES ? issued : STAGES;
                 for (uint32_t i = 0; i < pending; ++i) {
@@ -551,6 +616,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         }
     } else if (warp >= 2 && warp < 6) {
         // ----------------------------------------------------- epilogue --
+        prefetch_operands(prm.g, threadIdx.x - 64, 128);
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread
         const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;

@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
         }
     } else {
         // ---------------------------------------------- epilogue (both) --
+        prefetch_operands(prm.g, threadIdx.x - 64, 128);
         const uint32_t q = warp & 3u;                    // TMEM lane quarter of this warp
         const uint32_t r = rank * kBM + q * 32 + lane;   // row of this thread in the 256-row tile
         const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;

@@ -119,7 +119,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 }
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
-    if (mbar_try_wait(smem_u32(bar), parity)) return true;
+    const uint32_t a = smem_u32(bar);
+#pragma unroll 1
+    for (uint32_t i = 0; i < 16; ++i)
+        if (mbar_try_wait(a, parity)) return true;
     return mbar_wait_slow(bar, parity, ctl, where);
 }
 
@@ -162,6 +165,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
 // async-proxy (TMA / tcgen05) accesses
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// brings the 128-byte line holding `p` into L2 (no register result, no TMA)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // ------------------------------------------------------------- cp.async ----

@@ -94,7 +94,7 @@ bool out_code(bst_dtype t, uint32_t& code) {
 uint64_t timeout_ns() { return t_timeout_ns ? t_timeout_ns : kDefaultTimeoutNs; }
 
 struct Sched {
-    uint32_t offset = 1, dir = 0, tile_n = 0, tile_m = 0, num_ctas = 0;
+    uint32_t offset = 1, dir = 0, tile_n = 0, tile_m = 0, num_ctas = 0, split_k = 0;
     uint32_t* trace = nullptr;
     uint64_t* timeline = nullptr;
 };
@@ -104,10 +104,12 @@ bst_status read_sched(const bst_sched* s, Sched& out) {
     if (s->swizzle_offset < 1 || s->swizzle_direction > 1) return BST_ERR_INVALID_ARG;
     if (s->tile_n != 0 && s->tile_n != 64 && s->tile_n != 128 && s->tile_n != 256) return BST_ERR_INVALID_ARG;
     if (s->tile_m != 0 && s->tile_m != 128 && s->tile_m != 256) return BST_ERR_INVALID_ARG;
+    if (s->split_k > 4 || s->split_k == 3) return BST_ERR_INVALID_ARG;
     out.offset = s->swizzle_offset;
     out.dir = s->swizzle_direction;
     out.tile_n = s->tile_n;
     out.tile_m = s->tile_m;
+    out.split_k = s->split_k;
     out.num_ctas = s->num_ctas;
     out.trace = s->trace;
     out.timeline = s->timeline;
@@ -268,6 +270,26 @@ void set_prefetch(GemmArgs& g, const OperandSpec& a, const OperandSpec& b, const
     g.pf_ptr[3] = s2; g.pf_bytes[3] = s2 ? s2_bytes : 0;
 }
 
+// Split-K on 256 x 256 CTA-pair tiles for problems whose tiles cannot fill the
+// GPU: the largest S in {4, 2} whose clusters of 2*S CTAs (one per tile) are
+// all resident at once, with at least 4 k-blocks per split.  Returns 1 for no
+// split, 0 if the caller forced a split this problem cannot take.
+uint32_t choose_splits(const Sched& sch, bool eligible, uint64_t M, uint64_t N, uint32_t num_kb, uint32_t sms) {
+    if (sch.split_k == 1) return 1;
+    const bool forced = sch.split_k >= 2;
+    if (!eligible || (sch.tile_m && sch.tile_m != 256) || (sch.tile_n && sch.tile_n != 256)) return forced ? 0 : 1;
+    const uint64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    if (forced) return sch.split_k;
+    if (tiles * 2 * 2 > sms) return 1;                  // pairs alone already fill half the GPU or more
+    for (uint32_t s : {4u, 2u}) {
+        uint32_t resident = 0;
+        if (tiles * 2 * s > sms || num_kb < 4 * s) continue;
+        if (splitk_resident_clusters(s, &resident) != cudaSuccess) { cudaGetLastError(); continue; }
+        if (tiles <= resident) return s;
+    }
+    return 1;
+}
+
 CUtensorMapDataType tmap_type(bst_dtype t) {
     if (t == BST_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (t == BST_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -321,8 +343,13 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     if (K == 0)
         return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, sc, M, N, batch, csize, dev.sms, stream));
 
+    const bool pair_ok = tma_ok(a) && tma_ok(b);
+    const uint32_t num_kb = static_cast<uint32_t>((K + 63) / 64);
+    const uint32_t splits = choose_splits(sch, pair_ok && mode == kModePlain, M, N, num_kb, dev.sms);
+    if (splits == 0) return BST_ERR_UNSUPPORTED;
     TileChoice tc;
-    if (bst_status s = choose_tile(sch, tma_ok(a) && tma_ok(b), false, M, batch, N, dev.sms, tc)) return s;
+    if (splits > 1) { tc.tm = 256; tc.bn = 256; }
+    else if (bst_status s = choose_tile(sch, pair_ok, false, M, batch, N, dev.sms, tc)) return s;
     const uint32_t bn = tc.bn;
     const bool pair = tc.tm == 256;
     const uint64_t tiles = ((M + tc.tm - 1) / tc.tm) * ((N + bn - 1) / bn) * batch;
@@ -356,6 +383,7 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.timeout_ns = timeout_ns();
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    if (splits > 1) return cuda_status(launch_pair_splitk(p, splits, static_cast<uint32_t>(tiles), stream));
     if (pair)
         return cuda_status(launch_pair(p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
                                        stream));

@@ -278,3 +278,243 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
 }
 
 }  // namespace bst
+
+namespace bst {
+
+// Split-K variant for problems with fewer 256 x BN tiles than the GPU has
+// CTA pairs ("09_split_matmul" of "Block Dispatch Policies" names split
+// GEMMs; the split here is along K).  A cluster of 2*S CTAs owns one tile:
+// CTA pair p (cluster ranks 2p, 2p+1) accumulates k-blocks
+// [p*ceil(kb/S), (p+1)*ceil(kb/S)) of it exactly as gemm_pair_kernel does.
+// The S partial tiles are then summed through distributed shared memory:
+// each split finishes R = 128/S of the 128 accumulator rows its CTA holds.
+// After a cluster barrier (every pipeline of the cluster drained, so the
+// stage buffers can be reused), epilogue warp q of each CTA sends its 32
+// accumulator rows to the CTA of split 32q/R on the same half of the tile
+// (reduce-scatter); after a second barrier each CTA adds the S slots it
+// received for its R rows, rounds once and stores them.  Nothing goes
+// through global memory and no second kernel runs.
+template <uint32_t BN, uint32_t STAGES, uint32_t S>
+struct SplitLayout {
+    using Pair = PairLayout<BN, STAGES>;
+    static constexpr uint32_t kRows = kBM / S;                     // rows each split finishes
+    static constexpr uint32_t kRowFloats = BN + 4;                 // padded: conflict-free 16-byte stores
+    static constexpr uint32_t kSlotBytes = kRows * kRowFloats * 4; // the rows one split sends
+    static_assert(S * kSlotBytes <= STAGES * Pair::kStageBytes, "receive slots reuse the stage buffers");
+};
+
+template <uint32_t BN, uint32_t STAGES, uint32_t S>
+__global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_splitk_kernel(const __grid_constant__ GemmParams prm) {
+    using Lay = PairLayout<BN, STAGES>;
+    using SL = SplitLayout<BN, STAGES, S>;
+    constexpr uint32_t TM = 2 * kBM;
+    constexpr uint32_t BH = BN / 2;
+    static_assert(S == 2 || S == 4, "splits");
+    static_assert(BN == 256, "split-K runs 256 x 256 tiles");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m};
+    const uint32_t num_kb = prm.g.num_kb;
+    const uint32_t a_mn = prm.g.a.mn_major, b_mn = prm.g.b.mn_major;
+    uint32_t* const err = prm.g.err;
+    constexpr uint32_t bk_elems = 64;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* drain = bars + 2 * STAGES + 2 * Lay::kACC;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    uint32_t* tmem_holder = misc;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    uint64_t* const tl = prm.g.timeline ? prm.g.timeline + static_cast<uint64_t>(blockIdx.x) * 64 : nullptr;
+    if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
+    const uint32_t crank = cluster_rank();
+    const uint32_t split = crank >> 1, half = crank & 1u, leader = crank & ~1u;
+    const uint16_t pair_mask = static_cast<uint16_t>(3u << leader);
+    const uint32_t t = cluster_id_x();               // one tile per cluster
+    const bool has_tile = t < prm.g.total_tiles;
+    // balanced ranges: sizes differ by at most one; a range is empty only
+    // when there are fewer k-blocks than splits
+    const uint32_t kb_begin = (split * num_kb) / S, kb_end = ((split + 1) * num_kb) / S;
+    const bool has_k = kb_end > kb_begin;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&tfull[0], 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&prm.tmap_a);
+        prefetch_tmap(&prm.tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, Lay::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    if (tl && threadIdx.x == 0) tl[1] = globaltimer_ns();
+    const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
+    GroupTable gt{nullptr, nullptr, 0};
+    TileInfo ti{};
+    if (has_tile) ti = tile_info(sa, t, TM, BN, gt);
+
+    if (warp == 0 && lane == 0 && has_tile) {
+        // ------------------------------------------------------ producer --
+        const uint32_t full_leader = map_to_cta(smem_u32(full), leader);
+        constexpr uint32_t tx = Lay::kABytes + Lay::kBBytes;
+        const uint32_t a_row = ti.row0 + half * kBM;
+        const uint32_t b_col = ti.n * BN + half * BH;
+        uint32_t stage = 0, phase = 0, issued = 0;
+        bool ok = true;
+        for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+            uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+            uint8_t* sb_s = sa_s + Lay::kABytes;
+            const uint32_t bar = full_leader + stage * 8;
+            const int32_t k0 = kb * bk_elems;
+            if (half == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
+            if (!a_mn) tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);
+            else
+                for (uint32_t j = 0; j < kBM / bk_elems; ++j)
+                    tma_load_2d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0);
+            if (!b_mn) tma_load_2d_pair(sb_s, &prm.tmap_b, bar, k0, b_col);
+            else
+                for (uint32_t j = 0; j < BH / bk_elems; ++j)
+                    tma_load_2d_pair(sb_s + j * bk_elems * kLine, &prm.tmap_b, bar, b_col + j * bk_elems, k0);
+            if (tl && issued < 14) tl[2 + issued] = globaltimer_ns();
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok && half == 0) {
+            uint32_t s = stage, ph = phase;
+            const uint32_t pending = issued < STAGES ? issued : STAGES;
+            for (uint32_t i = 0; i < pending; ++i) {
+                if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
+                mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
+            }
+        }
+    } else if (warp == 1 && lane == 0 && has_tile && has_k && half == 0) {
+        // ------------------------------------- MMA issuer (pair leaders) --
+        const uint32_t a_lbo = a_mn ? bk_elems * kLine : 16u;
+        const uint32_t b_lbo = b_mn ? bk_elems * kLine : 16u;
+        const uint32_t a_step = a_mn ? 16u * kLine : 32u;
+        const uint32_t b_step = b_mn ? 16u * kLine : 32u;
+        const uint32_t idesc = idesc_f16(prm.g.ab_fmt, a_mn, b_mn, TM, BN);
+        const uint32_t smem_base = smem_u32(smem);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true, any_mma = false;
+        for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
+            if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
+            const uint64_t adesc = smem_desc(sa_addr, a_lbo, 1024, kSwizzle128B);
+            const uint64_t bdesc = smem_desc(sa_addr + Lay::kABytes, b_lbo, 1024, kSwizzle128B);
+#pragma unroll
+            for (uint32_t kk = 0; kk < 4; ++kk)
+                umma_f16_pair(tmem_base, adesc + ((kk * a_step) >> 4), bdesc + ((kk * b_step) >> 4), idesc,
+                              (kb > kb_begin || kk > 0) ? 1u : 0u);
+            umma_commit_pair_mc(&empty[stage], pair_mask);
+            if (tl && kb - kb_begin < 16) tl[16 + kb - kb_begin] = globaltimer_ns();
+            any_mma = true;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) umma_commit_pair_mc(&tfull[0], pair_mask);
+        else if (any_mma) {
+            umma_commit_pair_mc(drain, static_cast<uint16_t>(1u << crank));
+            mbar_wait_drain(drain, 0, ctl.timeout_ns);
+        }
+    }
+
+    // every role of every CTA of the cluster is done with the pipeline: the
+    // epilogue waits for its accumulator first
+    bool acc_ok = true;
+    if (warp >= 2 && has_tile && has_k) acc_ok = warp_wait(&tfull[0], 0, ctl, 4);
+    if (tl && warp == 2 && lane == 0) tl[32] = globaltimer_ns();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (tl && threadIdx.x == 64) tl[33] = globaltimer_ns();
+
+    // reduce-scatter: warp q's 32 rows go to split 32q/R (same half), into
+    // the slot of the sending split
+    if (warp >= 2 && has_tile) {
+        const uint32_t q = warp & 3u;
+        const uint32_t dest = 2 * ((q * 32) / SL::kRows) + half;      // a rank of this cluster: < 2*S
+        const uint32_t row_in_slot = (q * 32) % SL::kRows + lane;
+        const uint32_t slot =
+            map_to_cta(smem_u32(smem), dest) + split * SL::kSlotBytes + row_in_slot * SL::kRowFloats * 4;
+        const bool have = acc_ok && has_k;            // an empty range sends zeros
+        const uint32_t taddr = tmem_base + ((q * 32) << 16);
+#pragma unroll 1
+        for (uint32_t cc = 0; cc < BN / 32; ++cc) {
+            uint32_t v[32];
+            if (have) tmem_ld_32x32b_x32(taddr + cc * 32, v);
+#pragma unroll
+            for (uint32_t j = 0; j < 32; j += 4) {
+                if (have) st_cluster_v4(slot + (cc * 32 + j) * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
+                else st_cluster_v4(slot + (cc * 32 + j) * 4, 0u, 0u, 0u, 0u);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tl && threadIdx.x == 64) tl[34] = globaltimer_ns();
+    cluster_sync();
+    if (tl && threadIdx.x == 64) tl[35] = globaltimer_ns();
+
+    // sum the S slots for rows [split*R, split*R + R) of this half and store
+    if (warp >= 2 && has_tile) {
+        const uint32_t e = threadIdx.x - 64;             // 0..127: S threads per row
+        const uint32_t row = e / S;                      // 0..R-1
+        const uint32_t c0 = (e % S) * (BN / S);          // BN/S columns per thread
+        const uint32_t r = half * kBM + split * SL::kRows + row;   // row within the 256-row tile
+        const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
+        const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
+        uint8_t* crow = prm.g.C + (static_cast<int64_t>(ti.row0 + r) * prm.g.ldc) * csize;
+        const float* base = reinterpret_cast<const float*>(smem) + row * SL::kRowFloats + c0;
+#pragma unroll 1
+        for (uint32_t cc = 0; cc < BN / S; cc += 32) {
+            uint32_t v[32];
+#pragma unroll
+            for (uint32_t j = 0; j < 32; ++j) {
+                float acc = 0.f;
+#pragma unroll
+                for (uint32_t sidx = 0; sidx < S; ++sidx) acc += base[sidx * (SL::kSlotBytes / 4) + cc + j];
+                v[j] = __float_as_uint(acc);
+            }
+            const uint32_t col = c0 + cc;
+            if (r < ti.m_act && col < ti.n_act)
+                store_row_chunk(c_type, c_vec, crow, ti.n * BN + col, ti.n_act - col, v);
+        }
+        if (prm.g.trace && split == 0 && half == 0 && e == 0 && t < prm.g.trace_cap) {
+            uint32_t* tr = prm.g.trace + static_cast<uint64_t>(t) * 5;
+            tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
+        }
+    }
+    if (tl && threadIdx.x == 64) tl[36] = globaltimer_ns();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Lay::kTmemCols);
+    }
+    if (tl && threadIdx.x == 0) tl[37] = globaltimer_ns();
+}
+
+}  // namespace bst

@@ -32,6 +32,10 @@ cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stre
 // CTA-pair kernel: launches clusters of 2, at most max_pairs of them (and no
 // more than fit on the device at once)
 cudaError_t launch_pair(const GemmParams& p, uint32_t bn, uint32_t max_pairs, cudaStream_t stream);
+// split-K CTA pairs on 256 x 256 tiles: one cluster of 2*splits CTAs per tile
+cudaError_t launch_pair_splitk(const GemmParams& p, uint32_t splits, uint32_t tiles, cudaStream_t stream);
+// clusters of 2*splits CTAs the split-K kernel can keep resident at once
+cudaError_t splitk_resident_clusters(uint32_t splits, uint32_t* out);
 
 // Shared-memory bytes a launch needs (for validation of the device limit).
 uint32_t smem_dense(uint32_t bn, uint32_t groups);

@@ -406,4 +406,10 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t cta_
         "h"(cta_mask));
 }
 
+// 16-byte store into the shared memory of any CTA of the cluster
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 }  // namespace bst

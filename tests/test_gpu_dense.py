@@ -250,3 +250,28 @@ def test_pair_batched():
         a = og.as_logical(og.decode(w["a"][i], "f16"), M, K, w["lda"], False)
         b = og.as_logical(og.decode(w["b"][i], "f16"), K, N, w["ldb"], True)
         assert_close_f16(got[i], decode_out(og.gemm(a, b, "f16"), "f16"))
+
+
+# ------------------------------------------------- split-K CTA pairs -------
+
+@pytest.mark.parametrize("mnk", [(256, 256, 512), (300, 500, 1000), (1024, 1024, 2048), (17, 260, 4096)])
+@pytest.mark.parametrize("acol,bcol", [(False, True), (True, False), (False, False), (True, True)])
+@pytest.mark.parametrize("splits", [2, 4])
+def test_splitk_shapes_layouts(mnk, acol, bcol, splits):
+    M, N, K = mnk
+    up8 = lambda x: -(-x // 8) * 8
+    w = wl.dense16(M, N, K, "f16", a_col_major=acol, b_col_major=bcol, seed=M + N + K + splits,
+                   lda=up8(M if acol else K), ldb=up8(K if bcol else N), dist="normal")
+    lm, ln = -(-M // 256), -(-N // 256)
+    trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
+    got = run_dense(w, "f16", bst.sched(3, 1, split_k=splits, trace=trace))
+    assert_close_f16(got, oracle_dense(w, "f16"))
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 256, 256, 3, 1), dtype=np.uint32))
+
+
+def test_splitk_more_splits_than_kblocks_and_f32_out():
+    # K = 64: one k-block, four splits -> three splits contribute zeros
+    w = wl.dense16(256, 256, 64, "bf16", b_col_major=True, seed=8)
+    got = run_dense(w, "f32", bst.sched(1, 0, split_k=4))
+    assert_close_f16(got, oracle_dense(w, "f32"))

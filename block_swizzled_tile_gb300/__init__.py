@@ -20,8 +20,10 @@ ROW_MAJOR, COL_MAJOR = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(7)
 
 EXPORTED = ["bst_gemm", "bst_gemm_batched", "bst_gemm_grouped", "bst_gemm_quant_per_token",
-            "bst_gemm_quant_per_token_workspace_size", "bst_swizzle_map", "bst_swizzle_map_grouped",
-            "bst_check_async", "bst_status_string", "bst_set_wait_timeout_ns"]
+            "bst_gemm_quant_per_token_noalloc", "bst_gemm_quant_per_token_workspace_size", "bst_swizzle_map",
+            "bst_swizzle_map_grouped", "bst_check_async", "bst_status_string", "bst_set_wait_timeout_ns"]
+# BST_NOALLOC_SCRATCH_BYTES: the scratch limit of gemm_quant_per_token_noalloc
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class BstError(RuntimeError):
@@ -56,6 +58,8 @@ _SIGS = {
     "bst_gemm_quant_per_token_workspace_size": [_i64, _i64, _i64],
     "bst_gemm_quant_per_token": [_i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _sz,
                                  ctypes.POINTER(Sched), _vp],
+    "bst_gemm_quant_per_token_noalloc": [_i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64, _vp,
+                                         ctypes.POINTER(Sched), _vp],
     "bst_swizzle_map": [_u32, _u32, _u32, _u32, _u32, ctypes.POINTER(Sched), _vp, _vp],
     "bst_swizzle_map_grouped": [_i32, _vp, _u32, _u32, _u32, ctypes.POINTER(Sched), _vp, _u32, _vp],
     "bst_check_async": [_vp],
@@ -142,6 +146,21 @@ def gemm_quant_per_token(M, N, K, A, lda, B, b_layout, ldb, scale_a, scale_b, C,
                                           _ptr(scale_b), _ptr(C), ldc, _ptr(acc_out), _ptr(workspace),
                                           workspace_bytes, _sched(sched), _stream(stream)),
            "bst_gemm_quant_per_token")
+
+
+def gemm_quant_per_token_noalloc(M, N, K, A, lda, B, b_layout, ldb, scale_a, scale_b, C, ldc, acc_out,
+                                 sched=None, stream=None):
+    """gemm_quant_per_token without a workspace argument: the library's own
+    fixed scratch of NOALLOC_SCRATCH_BYTES is used and nothing is allocated.
+    Problems needing more scratch raise BstError(ERR_UNSUPPORTED)."""
+    status = lib().bst_gemm_quant_per_token_noalloc(M, N, K, _ptr(A), lda, _ptr(B), b_layout, ldb, _ptr(scale_a),
+                                                    _ptr(scale_b), _ptr(C), ldc, _ptr(acc_out), _sched(sched),
+                                                    _stream(stream))
+    where = "bst_gemm_quant_per_token_noalloc"
+    need = gemm_quant_per_token_workspace_size(M, N, K)
+    if status == ERR_UNSUPPORTED and need > NOALLOC_SCRATCH_BYTES:
+        where += " (needs %d bytes of scratch, limit %d)" % (need, NOALLOC_SCRATCH_BYTES)
+    _check(status, where)
 
 
 def swizzle_map(M, N, tile_m, tile_n, batch, sched, out, stream=None):

@@ -196,6 +196,36 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K,
                                     const bst_sched* sched, void* stream);
 
 /*
+ * bst_gemm_quant_per_token_noalloc -- the same int8 GEMM with per-token
+ * dequant as bst_gemm_quant_per_token (same arguments, results and errors),
+ * for callers that cannot allocate device memory at the point of the call:
+ * a plain C host program that has no device allocator of its own, or a
+ * process whose device memory is already reserved by another framework's
+ * pool, where an extra allocation would fail or fragment that pool.  The
+ * pages have no counterpart of this entry point; it exists for such callers.
+ *
+ * Instead of a caller-owned workspace it uses one scratch array of
+ * BST_NOALLOC_SCRATCH_BYTES compiled into the library, and it allocates
+ * nothing (no cudaMalloc, no library allocator).  A problem whose
+ * bst_gemm_quant_per_token_workspace_size(M, N, K) exceeds that limit is
+ * rejected with BST_ERR_UNSUPPORTED before any CUDA call.  The first call on
+ * each device looks up the array's device address with that device current
+ * (a one-time set-up, not repeated); make that first call before any stream
+ * capture.  Every call on a device shares the one array: calls on the same
+ * stream run one after another and are safe, while calls that can overlap
+ * (different streams, or host threads without ordering between their
+ * streams) race on the scratch and give wrong results.
+ */
+#define BST_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+bst_status bst_gemm_quant_per_token_noalloc(int64_t M, int64_t N, int64_t K,
+                                            const int8_t* A, int64_t lda,
+                                            const int8_t* B, bst_layout b_layout, int64_t ldb,
+                                            const float* scale_a, const float* scale_b,
+                                            void* C, int64_t ldc, int32_t* acc_out,
+                                            const bst_sched* sched, void* stream);
+
+/*
  * bst_swizzle_map -- debug entry: runs the device scheduler the GEMM kernels
  * use ("Block Scheduler Code Explained" sections 4.3-4.6) for every task of a
  * (possibly batched) problem and writes, for task t, the 5 uint32

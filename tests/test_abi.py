@@ -84,3 +84,19 @@ def test_argument_errors_need_no_device(lib):
                                 None, None) == bst.ERR_INVALID_ARG
     assert lib.bst_swizzle_map(10, 10, 0, 4, 1, None, 1, None) == bst.ERR_INVALID_ARG
     assert lib.bst_swizzle_map(1 << 31, 1 << 31, 1, 1, 1, None, 1, None) == bst.ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_oversize_without_a_device(lib):
+    # 4096^3 needs 64 MiB of scratch, past the 32 MiB array: rejected before any CUDA call
+    assert bst.gemm_quant_per_token_workspace_size(4096, 4096, 4096) > bst.NOALLOC_SCRATCH_BYTES
+    s = lib.bst_gemm_quant_per_token_noalloc(4096, 4096, 4096, 1 << 20, 4096, 1 << 20, bst.COL_MAJOR, 4096,
+                                             1 << 20, 1 << 20, 1 << 20, 4096, None, None, None)
+    assert s == bst.ERR_UNSUPPORTED
+    assert lib.bst_gemm_quant_per_token_noalloc(-1, 4, 4, None, 4, None, bst.COL_MAJOR, 4, None, None, None, 4,
+                                                None, None, None) == bst.ERR_INVALID_ARG
+
+
+def test_noalloc_limit_matches_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define BST_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == bst.NOALLOC_SCRATCH_BYTES

@@ -270,24 +270,65 @@ void set_prefetch(GemmArgs& g, const OperandSpec& a, const OperandSpec& b, const
     g.pf_ptr[3] = s2; g.pf_bytes[3] = s2 ? s2_bytes : 0;
 }
 
-// Split-K on 256 x 256 CTA-pair tiles for problems whose tiles cannot fill the
-// GPU: the largest S in {4, 2} whose clusters of 2*S CTAs (one per tile) are
-// all resident at once, with at least 4 k-blocks per split.  Returns 1 for no
-// split, 0 if the caller forced a split this problem cannot take.
-uint32_t choose_splits(const Sched& sch, bool eligible, uint64_t M, uint64_t N, uint32_t num_kb, uint32_t sms) {
-    if (sch.split_k == 1) return 1;
+// Widest store (16, 8, 4 or 2 bytes, at least the element size) that every
+// row start of an output allows: the base address, the row pitch and the
+// batch stride in bytes must all be multiples of it.
+uint32_t store_vec(const void* ptr, int64_t ld_bytes, int64_t batch_stride_bytes, uint32_t esize) {
+    uint32_t v = 16;
+    const uint64_t p = reinterpret_cast<uintptr_t>(ptr);
+    while (v > esize && (p % v || static_cast<uint64_t>(ld_bytes) % v || static_cast<uint64_t>(batch_stride_bytes) % v))
+        v >>= 1;
+    return v;
+}
+
+// Split-K on CTA-pair tiles (256 x 256 or 256 x 128) for problems whose
+// tiles cannot fill the GPU.  Among the shapes whose clusters of 2*S CTAs
+// (one per tile) all fit on the SMs and are resident at once, with at least
+// 4 k-blocks per split, it takes the one with the fewest k-block time units
+// per cluster: a 256 x 128 k-block costs about 0.6 of a 256 x 256 one (it is
+// shared-memory-port bound, the wide one tensor bound).  splits = 1: no
+// split; splits = 0: the caller forced a split this problem cannot take.
+struct SplitChoice {
+    uint32_t splits = 1;
+    uint32_t bn = 256;
+};
+
+SplitChoice choose_splits(const Sched& sch, bool eligible, uint64_t M, uint64_t N, uint32_t num_kb, uint32_t sms) {
+    SplitChoice none;
+    if (sch.split_k == 1) return none;
     const bool forced = sch.split_k >= 2;
-    if (!eligible || (sch.tile_m && sch.tile_m != 256) || (sch.tile_n && sch.tile_n != 256)) return forced ? 0 : 1;
-    const uint64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (forced) return sch.split_k;
-    if (tiles * 2 * 2 > sms) return 1;                  // pairs alone already fill half the GPU or more
-    for (uint32_t s : {4u, 2u}) {
-        uint32_t resident = 0;
-        if (tiles * 2 * s > sms || num_kb < 4 * s) continue;
-        if (splitk_resident_clusters(s, &resident) != cudaSuccess) { cudaGetLastError(); continue; }
-        if (tiles <= resident) return s;
+    const bool bn_ok = sch.tile_n == 0 || sch.tile_n == 128 || sch.tile_n == 256;
+    if (!eligible || (sch.tile_m && sch.tile_m != 256) || !bn_ok) {
+        if (forced) none.splits = 0;
+        return none;
     }
-    return 1;
+    auto tiles_of = [&](uint64_t bn) { return ((M + 255) / 256) * ((N + bn - 1) / bn); };
+    if (forced) {
+        SplitChoice c;
+        c.splits = sch.split_k;
+        c.bn = sch.tile_n ? sch.tile_n : 256;
+        return c;
+    }
+    if (tiles_of(256) * 2 * 2 > sms) return none;     // pairs alone already fill half the GPU or more
+    SplitChoice best;
+    double best_cost = 0;
+    for (uint32_t bn : {256u, 128u}) {
+        if (sch.tile_n && sch.tile_n != bn) continue;
+        const uint64_t tiles = tiles_of(bn);
+        for (uint32_t s : {4u, 2u}) {
+            uint32_t resident = 0;
+            if (tiles * 2 * s > sms || num_kb < 4 * s) continue;
+            if (splitk_resident_clusters(bn, s, &resident) != cudaSuccess) { cudaGetLastError(); continue; }
+            if (tiles > resident) continue;
+            const double cost = static_cast<double>((num_kb + s - 1) / s) * (bn == 256 ? 1.0 : 0.6);
+            if (best.splits == 1 || cost < best_cost) {
+                best.splits = s;
+                best.bn = bn;
+                best_cost = cost;
+            }
+        }
+    }
+    return best;
 }
 
 CUtensorMapDataType tmap_type(bst_dtype t) {
@@ -345,16 +386,18 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
 
     const bool pair_ok = tma_ok(a) && tma_ok(b);
     const uint32_t num_kb = static_cast<uint32_t>((K + 63) / 64);
-    const uint32_t splits = choose_splits(sch, pair_ok && mode == kModePlain, M, N, num_kb, dev.sms);
+    const SplitChoice sc_k = choose_splits(sch, pair_ok && mode == kModePlain, M, N, num_kb, dev.sms);
+    const uint32_t splits = sc_k.splits;
     if (splits == 0) return BST_ERR_UNSUPPORTED;
     TileChoice tc;
-    if (splits > 1) { tc.tm = 256; tc.bn = 256; }
+    if (splits > 1) { tc.tm = 256; tc.bn = sc_k.bn; }
     else if (bst_status s = choose_tile(sch, pair_ok, false, M, batch, N, dev.sms, tc)) return s;
     const uint32_t bn = tc.bn;
     const bool pair = tc.tm == 256;
     const uint64_t tiles = ((M + tc.tm - 1) / tc.tm) * ((N + bn - 1) / bn) * batch;
     if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
-    if ((pair ? smem_pair(bn, 0) : smem_dense(bn, 0)) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+    const uint32_t smem_need = splits > 1 ? smem_splitk(bn, splits) : pair ? smem_pair(bn, 0) : smem_dense(bn, 0);
+    if (smem_need == 0 || smem_need > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -374,8 +417,7 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.ldc = ldc;
     p.g.c_batch_stride = sc;
     p.g.c_type = c_code;
-    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0) &&
-              (mode != kModeBatched || (sc * csize) % 16 == 0);
+    p.g.c_vec = store_vec(C, ldc * csize, mode == kModeBatched ? sc * csize : 0, csize);
     p.g.trace = sch.trace;
     p.g.timeline = sch.timeline;
     p.g.trace_cap = static_cast<uint32_t>(tiles);
@@ -383,7 +425,7 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.timeout_ns = timeout_ns();
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
-    if (splits > 1) return cuda_status(launch_pair_splitk(p, splits, static_cast<uint32_t>(tiles), stream));
+    if (splits > 1) return cuda_status(launch_pair_splitk(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     if (pair)
         return cuda_status(launch_pair(p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
                                        stream));
@@ -439,10 +481,31 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.C = static_cast<uint8_t*>(C);
     p.g.ldc = ldc;
     p.g.c_type = c_code;
-    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
+    p.g.c_vec = store_vec(C, ldc * csize, 0, csize);
     p.g.sfa = sfa;
     p.g.sfb = sfb;
     p.g.sf_ld = static_cast<uint32_t>(K / 32);
+    // scale factors by TMA when each row's codes are a whole number of 16-byte
+    // groups (K a multiple of 512) and both arrays start 16-byte aligned;
+    // otherwise the scale warp copies them row by row
+    if (K % 512 == 0 && reinterpret_cast<uintptr_t>(sfa) % 16 == 0 && reinterpret_cast<uintptr_t>(sfb) % 16 == 0) {
+        if (!encoder()) return BST_ERR_CUDA;
+        const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 32);
+        cuuint32_t estr[2] = {1, 1};
+        cuuint64_t dims_a[2] = {row_bytes, static_cast<cuuint64_t>(M)};
+        cuuint64_t dims_b[2] = {row_bytes, static_cast<cuuint64_t>(N)};
+        cuuint64_t strides[1] = {row_bytes};
+        cuuint32_t box_a[2] = {16, kBM};
+        cuuint32_t box_b[2] = {16, bn};
+        if (g_encode(&p.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(sfa), dims_a, strides, box_a,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            g_encode(&p.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(sfb), dims_b, strides, box_b,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return BST_ERR_CUDA;
+        p.g.sf_tma = 1;
+    }
     p.g.trace = sch.trace;
     p.g.timeline = sch.timeline;
     p.g.trace_cap = static_cast<uint32_t>(tiles);
@@ -542,7 +605,7 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
     p.g.C = static_cast<uint8_t*>(C);
     p.g.ldc = ldc;
     p.g.c_type = c_code;
-    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * csize) % 16 == 0);
+    p.g.c_vec = store_vec(C, ldc * csize, 0, csize);
     p.g.trace = sch.trace;
     p.g.timeline = sch.timeline;
     p.g.trace_cap = static_cast<uint32_t>(tiles_bound);
@@ -631,8 +694,8 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     p.g.C = static_cast<uint8_t*>(C);
     p.g.ldc = ldc;
     p.g.c_type = kOutBF16;
-    p.g.c_vec = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ldc * 2) % 16 == 0) &&
-              (!acc_out || (reinterpret_cast<uintptr_t>(acc_out) % 16 == 0));
+    p.g.c_vec = store_vec(C, ldc * 2, 0, 2);
+    p.g.acc_vec = acc_out ? store_vec(acc_out, ldc * 4, 0, 4) : 4u;
     p.g.scale_a = scale_a;
     p.g.scale_b = scale_b;
     p.g.acc_out = acc_out;

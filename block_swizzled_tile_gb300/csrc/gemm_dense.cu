@@ -13,8 +13,7 @@ static cudaError_t launch_one(const GemmParams& p, uint32_t grid, cudaStream_t s
     // the limit is set once for the largest group table any call can need
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(kMaxGroups), attr_done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kNumThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_gemm(kern, p, grid, threads_for<kKindF16>(), smem, stream);
 }
 
 cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream) {

@@ -38,14 +38,22 @@ namespace bst {
 enum : uint32_t { kKindF16 = 0, kKindMXF8 = 1 };
 enum : uint32_t { kEpiStore = 0, kEpiDequant = 1 };
 enum : uint32_t { kModePlain = 0, kModeBatched = 1, kModeGrouped = 2 };
-enum : uint32_t { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2 };
+enum : uint32_t { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2, kOutS32 = 3 };   // kOutS32: raw int32 (device side only)
 
 constexpr uint32_t kBM = 128;          // tile rows = TMEM lanes
 constexpr uint32_t kLine = 128;        // bytes per k-block line
-constexpr uint32_t kNumThreads = 192;   // warps: 0 TMA, 1 MMA, 2-5 epilogue
+constexpr uint32_t kNumThreads = 192;   // CTA-pair kernels: warps 0 TMA, 1 MMA, 2-5 epilogue
 constexpr uint32_t kScaleWarp = 6;      // MXFP8 only: a 7th warp copies scale factors
+// One-CTA kernels add a warp whose lane 0 issues the B loads: one thread
+// issues about one TMA (or one mbarrier arrive) per 0.1-0.15 us, so a single
+// issuing thread cannot feed a 128 x 128 tile's MMAs (one k-block per
+// 0.14 us); two threads on two warps issue in parallel.
 template <uint32_t KIND>
-constexpr uint32_t threads_for() { return KIND == 1 ? kNumThreads + 32 : kNumThreads; }
+constexpr uint32_t b_warp_for() { return KIND == 1 ? 7u : 6u; }
+template <uint32_t KIND>
+constexpr uint32_t threads_for() { return (b_warp_for<KIND>() + 1) * 32; }
+// Shared-memory staging of one epilogue warp: a 32 x 32 chunk of 4-byte values.
+constexpr uint32_t kEpiWarpBytes = 32 * 32 * 4;
 constexpr uint32_t kMaxGroups = 1024;
 
 struct OperandDesc {
@@ -77,13 +85,15 @@ struct GemmArgs {
     int64_t ldc;
     int64_t c_batch_stride;
     uint32_t c_type;
-    uint32_t c_vec;         // 16-byte vector stores allowed for whole 32-column chunks
+    uint32_t c_vec;         // widest store (16, 8, 4 or 2 bytes) C's base, pitch and batch stride allow
+    uint32_t acc_vec;       // the same for acc_out (int32 accumulators)
     const float* scale_a;
     const float* scale_b;
     int32_t* acc_out;
     const uint8_t* sfa;
     const uint8_t* sfb;
     uint32_t sf_ld;         // bytes per row of sfa / sfb (K / 32)
+    uint32_t sf_tma;        // 1: scale factors arrive by TMA (tmap_sfa / tmap_sfb), 16 bytes per row per 4 k-blocks
     uint32_t* trace;
     uint32_t trace_cap;     // tasks the trace buffer holds
     uint64_t* timeline;     // optional: 64 %globaltimer stamps per CTA
@@ -112,6 +122,8 @@ __device__ __forceinline__ void prefetch_operands(const GemmArgs& g, uint32_t ti
 struct GemmParams {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;
+    CUtensorMap tmap_sfa;   // MXFP8 scale factors as uint8 [rows, K/32], boxes of 16 bytes x 128 / BN rows
+    CUtensorMap tmap_sfb;
     GemmArgs g;
 };
 
@@ -124,8 +136,14 @@ struct GemmLayout {
     static constexpr uint32_t kSfbBytes = KIND == kKindMXF8 ? BN * 4u : 0u;
     static constexpr uint32_t kSfStageBytes = kSfaBytes + kSfbBytes;
     static constexpr uint32_t kSfOff = STAGES * kStageBytes;
-    static constexpr uint32_t kBarOff = kSfOff + STAGES * kSfStageBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1;
+    // MXFP8: two raw scale slots, each 16 bytes (4 k-blocks of E8M0 codes) of
+    // the tile's 128 A rows and BN B rows, as TMA delivers them
+    static constexpr uint32_t kRawRowsA = 128;
+    static constexpr uint32_t kRawSlotBytes = KIND == kKindMXF8 ? (kRawRowsA + BN) * 16u : 0u;
+    static constexpr uint32_t kRawOff = (kSfOff + STAGES * kSfStageBytes + 1023) & ~1023u;
+    static constexpr uint32_t kEpiOff = kRawOff + 2 * kRawSlotBytes;       // 4 epilogue warps x 4 KB staging
+    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2;     // ..., drain, raw_full[2]
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
     // TMEM: ACC accumulators of BN fp32 columns, then (MXFP8) per stage 4
@@ -232,43 +250,117 @@ __device__ __forceinline__ void build_group_table(const GroupTable& gt, const in
 // aligned).  Writes the exact shared-memory image a TMA load with 128-byte
 // swizzle would: line L (128 bytes) at L*128, its 16-byte chunk c at
 // ((c ^ (L % 8)) * 16); out-of-range elements are zero, like TMA's
-// out-of-bounds fill.  Vectors of 4-16 bytes go through cp.async (zero-fill
-// past the edge) and complete on the stage barrier through the caller's
-// cp.async.mbarrier.arrive; 2-byte vectors (odd pitches) use plain loads and
-// stores and the caller fences them for the async proxy.
-__device__ __noinline__ static void load_tile_plain(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t mn_major,
-                                                    uint32_t V, uint32_t esize, uint32_t lines, uint32_t mn0,
-                                                    uint32_t mn_lim, uint32_t k0, uint32_t k_lim, uint32_t lane) {
-    const uint32_t line_elems = kLine / esize;
-    const uint32_t vpl = kLine / V;
+// out-of-bounds fill.  The warp moves the tile in V-byte vectors (V = 16, 8,
+// 4 or 2, the widest the operand's base and pitch allow): each lane first
+// loads 8 vectors through L2 into registers (so 256 loads of the warp are in
+// flight together), then stores them.  The stores are generic-proxy writes:
+// the caller fences them for the async proxy before arriving on the stage
+// barrier.  (A cp.async version of this loader issued each warp-wide copy in
+// roughly 0.3 us when L1 is almost entirely carved out for the stage ring.)
+template <uint32_t V>
+struct VecT;
+template <> struct VecT<16> { using T = uint4; };
+template <> struct VecT<8> { using T = uint2; };
+template <> struct VecT<4> { using T = uint32_t; };
+template <> struct VecT<2> { using T = uint16_t; };
+
+__device__ __forceinline__ uint4 ld_cg(const uint4* p) { return __ldcg(p); }
+__device__ __forceinline__ uint2 ld_cg(const uint2* p) { return __ldcg(p); }
+__device__ __forceinline__ uint32_t ld_cg(const uint32_t* p) { return __ldcg(p); }
+__device__ __forceinline__ uint16_t ld_cg(const uint16_t* p) { return __ldcg(p); }
+
+// The first n bytes at p (n < V, a multiple of the element size esize), zero
+// above: the ragged end of a row, read element by element into two 64-bit
+// halves (no dynamically indexed register array, which would live in local
+// memory).
+template <uint32_t V>
+__device__ __forceinline__ typename VecT<V>::T ld_partial(const uint8_t* p, uint32_t n, uint32_t esize) {
+    uint64_t lo = 0, hi = 0;
+    for (uint32_t b = 0; b < n; b += esize) {
+        const uint64_t x = esize == 1 ? static_cast<uint64_t>(__ldcg(reinterpret_cast<const unsigned char*>(p + b)))
+                                      : static_cast<uint64_t>(__ldcg(reinterpret_cast<const uint16_t*>(p + b)));
+        if (b < 8) lo |= x << (b * 8);
+        else hi |= x << ((b - 8) * 8);
+    }
+    typename VecT<V>::T out;
+    if constexpr (V == 16)
+        out = make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32), static_cast<uint32_t>(hi),
+                         static_cast<uint32_t>(hi >> 32));
+    else if constexpr (V == 8) out = make_uint2(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32));
+    else if constexpr (V == 4) out = static_cast<uint32_t>(lo);
+    else out = static_cast<uint16_t>(lo);
+    return out;
+}
+
+// Operands reaching this loader are 2-byte (fp16/bf16); the element size,
+// the vector width and the layout are compile-time, so the per-vector index
+// arithmetic is a few shifts and adds.
+template <uint32_t V, bool MN>
+__device__ __noinline__ static void load_tile_regs(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t lines,
+                                                   uint32_t mn0, uint32_t mn_lim, uint32_t k0, uint32_t k_lim,
+                                                   uint32_t lane) {
+    using T = typename VecT<V>::T;
+    constexpr uint32_t kEsize = 2;
+    constexpr uint32_t kLineElems = kLine / kEsize;   // 64
+    constexpr uint32_t vpl = kLine / V;               // vectors per 128-byte line
+    constexpr uint32_t kBatch = 8;
     const uint32_t total = lines * vpl;
-    for (uint32_t idx = lane; idx < total; idx += 32) {
-        const uint32_t L = idx / vpl;
-        const uint32_t byte_in_line = (idx % vpl) * V;
-        uint32_t outer, outer_lim, inner0, inner_lim;
-        if (!mn_major) {              // line = one MN row, a k-block of K
-            outer = mn0 + L;
-            outer_lim = mn_lim;
-            inner0 = k0;
-            inner_lim = k_lim;
-        } else {                      // line = one k of a 64/128-element MN atom
-            outer = k0 + L % line_elems;
-            outer_lim = k_lim;
-            inner0 = mn0 + (L / line_elems) * line_elems;
-            inner_lim = mn_lim;
+    const uint32_t byte_in_line = (lane % vpl) * V;   // the same for every vector of this lane (vpl divides 32)
+    const uint32_t e_in_line = byte_in_line / kEsize;
+    static_assert(32 % vpl == 0 || vpl % 32 == 0, "lane pattern");
+#pragma unroll 1
+    for (uint32_t i0 = 0; i0 < total; i0 += 32 * kBatch) {
+        T tmp[kBatch];
+        uint32_t off[kBatch];
+#pragma unroll
+        for (uint32_t u = 0; u < kBatch; ++u) {
+            const uint32_t idx = i0 + u * 32 + lane;
+            const uint32_t L = idx / vpl;
+            const uint32_t bil = vpl <= 32 ? byte_in_line : (idx % vpl) * V;
+            const uint32_t eil = vpl <= 32 ? e_in_line : bil / kEsize;
+            uint32_t outer, outer_lim, e, inner_lim;
+            if (!MN) {                    // line = one MN row, a k-block of K
+                outer = mn0 + L;
+                outer_lim = mn_lim;
+                e = k0 + eil;
+                inner_lim = k_lim;
+            } else {                      // line = one k of a 64-element MN atom
+                outer = k0 + (L % kLineElems);
+                outer_lim = k_lim;
+                e = mn0 + (L / kLineElems) * kLineElems + eil;
+                inner_lim = mn_lim;
+            }
+            off[u] = idx < total ? L * kLine + ((((bil >> 4) ^ (L & 7u)) << 4) | (bil & 15u)) : 0xFFFFFFFFu;
+            const uint32_t in_elems = (idx < total && outer < outer_lim && e < inner_lim) ? inner_lim - e : 0u;
+            const uint32_t in_bytes = min(V, in_elems * kEsize);
+            const uint8_t* src = base + (static_cast<int64_t>(outer) * ld + e) * kEsize;
+            if (in_bytes == V) tmp[u] = ld_cg(reinterpret_cast<const T*>(src));
+            else if (in_bytes) tmp[u] = ld_partial<V>(src, in_bytes, kEsize);
+            else tmp[u] = T{};
         }
-        const uint32_t e = inner0 + byte_in_line / esize;
-        uint8_t* d = dst + L * kLine + ((((byte_in_line >> 4) ^ (L & 7u)) << 4) | (byte_in_line & 15u));
-        const bool row_in = outer < outer_lim;
-        const uint32_t in_elems = (row_in && e < inner_lim) ? inner_lim - e : 0u;
-        const uint32_t in_bytes = min(V, in_elems * esize);
-        const uint8_t* src = in_bytes ? base + (static_cast<int64_t>(outer) * ld + e) * esize : base;
-        if (V >= 4) {
-            cp_async_n(d, src, V, in_bytes);
-        } else {
-            uint16_t v = 0;
-            if (in_bytes) v = __ldg(reinterpret_cast<const uint16_t*>(src));
-            *reinterpret_cast<uint16_t*>(d) = v;
+#pragma unroll
+        for (uint32_t u = 0; u < kBatch; ++u)
+            if (off[u] != 0xFFFFFFFFu) *reinterpret_cast<T*>(dst + off[u]) = tmp[u];
+    }
+}
+
+__device__ __forceinline__ void load_tile_plain(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t mn_major,
+                                                uint32_t V, uint32_t esize, uint32_t lines, uint32_t mn0,
+                                                uint32_t mn_lim, uint32_t k0, uint32_t k_lim, uint32_t lane) {
+    (void)esize;   // always 2 here
+    if (mn_major) {
+        switch (V) {
+            case 16: load_tile_regs<16, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            case 8: load_tile_regs<8, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            case 4: load_tile_regs<4, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            default: load_tile_regs<2, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+        }
+    } else {
+        switch (V) {
+            case 16: load_tile_regs<16, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            case 8: load_tile_regs<8, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            case 4: load_tile_regs<4, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            default: load_tile_regs<2, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
         }
     }
 }
@@ -291,45 +383,105 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap* map, uint8_t* dst, u
     }
 }
 
-// Stores 32 consecutive fp32 accumulator columns of one output row.
-__device__ __forceinline__ void store_row_chunk(uint32_t c_type, uint32_t c_vec, uint8_t* row_ptr, uint32_t col0,
-                                                uint32_t n_valid, const uint32_t (&v)[32]) {
-    if (c_type == kOutF32) {
-        float* out = reinterpret_cast<float*>(row_ptr) + col0;
-        if (c_vec && n_valid >= 32) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<uint4*>(out + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        } else {
-#pragma unroll
-            for (uint32_t j = 0; j < 32; ++j)
-                if (j < n_valid) out[j] = __uint_as_float(v[j]);
-        }
-        return;
-    }
-    uint32_t packed[16];
-    if (c_type == kOutF16) {
+// Stores one 32 x 32 output chunk that a warp holds one row per lane (v[j] =
+// column j as 32-bit data: fp32 bits converted to out_type, or with kOutS32 a
+// raw int32).  The chunk goes through the warp's 4 KB staging buffer -- rows
+// of 64 (16-bit) or 128 (32-bit) bytes whose 16-byte granules are XOR-swizzled
+// by row, so the row-wise writes and the segment-wise reads are both free of
+// bank conflicts -- and leaves as whole row segments: consecutive lanes store
+// consecutive VEC-byte pieces of one row, so every store instruction writes
+// full sectors.  Rows >= rows_valid and columns >= cols_valid are not written
+// (both warp-uniform).  c0 addresses row 0, column 0 of the chunk; ld_bytes is
+// the row pitch; VEC (at least the element size ESZ) divides c0's address and
+// ld_bytes.  Everything but the data is compile-time, and every shared-memory
+// read of the chunk is issued before the first global store: one warp runs
+// this alone, so a loop of dependent address arithmetic would cost it
+// hundreds of cycles per pass.
+template <uint32_t ESZ, uint32_t VEC>
+__device__ __forceinline__ void store_chunk_t(uint8_t* stage, uint32_t out_type, uint8_t* c0, int64_t ld_bytes,
+                                              uint32_t rows_valid, uint32_t cols_valid, const uint32_t (&v)[32],
+                                              uint32_t lane) {
+    using T = typename VecT<VEC>::T;
+    constexpr uint32_t kRowBytes = 32u * ESZ;
+    constexpr uint32_t kLanesPerRow = kRowBytes / VEC;   // 4 .. 32
+    constexpr uint32_t kRowsPerPass = 32u / kLanesPerRow;
+    constexpr uint32_t kPasses = 32u / kRowsPerPass;
+    static_assert(VEC >= ESZ && kLanesPerRow <= 32, "vector width");
+    if (ESZ == 2) {
+        uint32_t p[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            __half2 h = __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            packed[j] = *reinterpret_cast<uint32_t*>(&h);
+            if (out_type == kOutF16) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                p[j] = *reinterpret_cast<const uint32_t*>(&h);
+            } else {
+                const __nv_bfloat162 h =
+                    __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                p[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
         }
-    } else {
+        uint8_t* rowp = stage + lane * 64u;
+        const uint32_t f = (lane >> 1) & 3u;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            packed[j] = *reinterpret_cast<uint32_t*>(&h);
+        for (uint32_t g = 0; g < 4; ++g)
+            *reinterpret_cast<uint4*>(rowp + ((g ^ f) << 4)) = make_uint4(p[4 * g], p[4 * g + 1], p[4 * g + 2], p[4 * g + 3]);
+    } else {
+        uint8_t* rowp = stage + lane * 128u;
+        const uint32_t f = lane & 7u;
+#pragma unroll
+        for (uint32_t g = 0; g < 8; ++g)
+            *reinterpret_cast<uint4*>(rowp + ((g ^ f) << 4)) = make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    }
+    __syncwarp();
+    const uint32_t row_in_pass = lane / kLanesPerRow;
+    const uint32_t byte_in_row = (lane % kLanesPerRow) * VEC;
+    const uint32_t valid_bytes = cols_valid * ESZ;
+    T val[kPasses];
+#pragma unroll
+    for (uint32_t q = 0; q < kPasses; ++q) {
+        const uint32_t r = q * kRowsPerPass + row_in_pass;
+        const uint32_t f = ESZ == 4 ? (r & 7u) : ((r >> 1) & 3u);
+        val[q] = *reinterpret_cast<const T*>(stage + r * kRowBytes + ((((byte_in_row >> 4) ^ f) << 4) | (byte_in_row & 15u)));
+    }
+    uint8_t* dst = c0 + static_cast<int64_t>(row_in_pass) * ld_bytes + byte_in_row;
+    const int64_t step = static_cast<int64_t>(kRowsPerPass) * ld_bytes;
+    if (byte_in_row + VEC <= valid_bytes) {
+#pragma unroll
+        for (uint32_t q = 0; q < kPasses; ++q) {
+            if (q * kRowsPerPass + row_in_pass < rows_valid) *reinterpret_cast<T*>(dst) = val[q];
+            dst += step;
+        }
+    } else if (byte_in_row < valid_bytes) {
+        // the ragged end of the rows: element by element
+#pragma unroll 1
+        for (uint32_t q = 0; q < kPasses; ++q) {
+            const uint32_t r = q * kRowsPerPass + row_in_pass;
+            if (r < rows_valid) {
+                const uint32_t f = ESZ == 4 ? (r & 7u) : ((r >> 1) & 3u);
+                const uint8_t* src = stage + r * kRowBytes + ((((byte_in_row >> 4) ^ f) << 4) | (byte_in_row & 15u));
+                for (uint32_t b = 0; b < valid_bytes - byte_in_row; b += ESZ) {
+                    if (ESZ == 4) *reinterpret_cast<uint32_t*>(dst + b) = *reinterpret_cast<const uint32_t*>(src + b);
+                    else *reinterpret_cast<uint16_t*>(dst + b) = *reinterpret_cast<const uint16_t*>(src + b);
+                }
+            }
+            dst += step;
         }
     }
-    uint16_t* out = reinterpret_cast<uint16_t*>(row_ptr) + col0;
-    if (c_vec && n_valid >= 32) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<uint4*>(out + 2 * j) = make_uint4(packed[j], packed[j + 1], packed[j + 2], packed[j + 3]);
+    __syncwarp();
+}
+
+__device__ __forceinline__ void store_chunk_coalesced(uint8_t* stage, uint32_t out_type, uint32_t vec, uint8_t* c0,
+                                                      int64_t ld_bytes, uint32_t rows_valid, uint32_t cols_valid,
+                                                      const uint32_t (&v)[32], uint32_t lane) {
+    if (out_type == kOutF32 || out_type == kOutS32) {
+        if (vec >= 16) store_chunk_t<4, 16>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
+        else if (vec == 8) store_chunk_t<4, 8>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
+        else store_chunk_t<4, 4>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
     } else {
-#pragma unroll
-        for (uint32_t j = 0; j < 32; ++j)
-            if (j < n_valid) out[j] = static_cast<uint16_t>(j & 1 ? packed[j >> 1] >> 16 : packed[j >> 1] & 0xFFFFu);
+        if (vec >= 16) store_chunk_t<2, 16>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
+        else if (vec == 8) store_chunk_t<2, 8>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
+        else if (vec == 4) store_chunk_t<2, 4>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
+        else store_chunk_t<2, 2>(stage, out_type, c0, ld_bytes, rows_valid, cols_valid, v, lane);
     }
 }
 
@@ -359,6 +511,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = bars + 2 * STAGES + ACC;
     uint64_t* drain = bars + 2 * STAGES + 2 * ACC;
+    uint64_t* raw_full = bars + 2 * STAGES + 2 * ACC + 1;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     uint32_t* tmem_holder = misc;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -367,6 +520,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     const bool lanes_copy = KIND == kKindMXF8 || !(a_tma && b_tma);
+    const bool lanes_copy_ops = !(a_tma && b_tma);      // an operand TMA cannot fetch
 
     GroupTable gt;
     gt.G = G;
@@ -377,7 +531,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         for (uint32_t s = 0; s < STAGES; ++s) {
             // 1 arrival from the issuing lane (+ TMA bytes), plus one per lane
             // when lanes also copy (MXFP8 scale factors, non-TMA operands)
-            mbar_init(&full[s], lanes_copy ? 33u : 1u);
+            // (MXFP8 with scale TMA: the A thread and one arrival of the scale warp)
+            mbar_init(&full[s], (KIND == kKindMXF8 && prm.g.sf_tma) ? 2u : lanes_copy ? 33u : 1u);
             mbar_init(&empty[s], 1);
         }
         for (uint32_t a = 0; a < ACC; ++a) {
@@ -385,6 +540,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             mbar_init(&tempty[a], 128);
         }
         mbar_init(drain, 1);
+        mbar_init(&raw_full[0], 1);
+        mbar_init(&raw_full[1], 1);
         *abort_flag = 0;
         *tiles_smem = prm.g.total_tiles;
         fence_barrier_init();
@@ -397,6 +554,9 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         tmem_alloc(tmem_holder, Lay::kTmemCols);
         tmem_relinquish();
     }
+    // set-up above touches no global memory: it overlaps the previous kernel
+    griddep_wait();
+    griddep_launch_dependents();
     if (mode == kModeGrouped && warp == 2)
         build_group_table(gt, prm.g.group_m, G, N, kBM, BN, sa.total_m, err, tiles_smem, lane);
     tc_fence_before();
@@ -407,7 +567,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     if (tl && threadIdx.x == 0) { tl[0] = globaltimer_ns(); tl[55] = t_entry; }
 
-    if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp)) {
+    constexpr uint32_t kBWarp = b_warp_for<KIND>();
+    if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp) || (warp == kBWarp && lane == 0 && !lanes_copy_ops)) {
         // ------------------------------------------------------ producer --
         const uint8_t* a_ptr = prm.g.a.ptr;
         const uint8_t* b_ptr = prm.g.b.ptr;
@@ -417,7 +578,6 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const uint8_t* sfa = prm.g.sfa;
         const uint8_t* sfb = prm.g.sfb;
         const uint32_t sf_ld = prm.g.sf_ld;
-        const bool plain_stores = (!a_tma && a_vec < 4) || (!b_tma && b_vec < 4);
         const uint32_t tx = (a_tma ? Lay::kABytes : 0u) + (b_tma ? Lay::kBBytes : 0u);
         // The TMA thread runs a loop of its own that contains no warp-synchronous
         // operation: mixing it with the warp-wide copy loop (whose waits end in
@@ -426,28 +586,38 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // half the time.  Lanes copy only for the MXFP8 scale factors (their own
         // warp) and for operands TMA cannot fetch (warp 0, which then also
         // carries the TMA issue).
-        const bool tma_thread = (warp == 0 && lane == 0);
+        // Both operands through TMA: lane 0 of warp 0 issues the A loads and is
+        // the one arrival on full[] (expecting the bytes of A and B), lane 0 of
+        // warp kBWarp issues the B loads; both wait for the stage to be empty.
+        // A B load may land before the A thread's expect_tx: the transaction
+        // count goes negative meanwhile and the missing arrival keeps the phase
+        // open.  Lanes copy only for the MXFP8 scale factors (their own warp)
+        // and for operands TMA cannot fetch (warp 0 then issues every load).
+        const bool tma_thread = (warp == 0 && lane == 0) || (warp == kBWarp && lane == 0);
         const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp) : (warp == 0 && lanes_copy);
         if (tma_thread && !warp_copies) {
+            const bool is_a = warp == 0;
             const bool simple = !a_mn && !b_mn && !a_rank3 && !b_rank3;
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-                if (tl && issued == 0) tl[56] = globaltimer_ns();
+                if (tl && is_a && issued == 0) tl[56] = globaltimer_ns();
                 const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
                 const uint32_t n0 = ti.n * BN;
                 const int32_t zc = static_cast<int32_t>(ti.tag);
-                if (tl && issued == 0) tl[57] = globaltimer_ns();
+                if (tl && is_a && issued == 0) tl[57] = globaltimer_ns();
                 if (simple) {
-                    // both operands K-contiguous, 2-D maps: one box each per k-block
+                    // both operands K-contiguous, 2-D maps: one box per k-block
+                    const CUtensorMap* map = is_a ? &prm.tmap_a : &prm.tmap_b;
+                    const uint32_t dst_off = is_a ? 0u : Lay::kABytes;
+                    const int32_t row = is_a ? static_cast<int32_t>(ti.row0) : static_cast<int32_t>(n0);
                     for (uint32_t kb = 0; kb < num_kb; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
-                        uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+                        uint8_t* st = smem + stage * Lay::kStageBytes;
                         const int32_t k0 = static_cast<int32_t>(kb * bk_elems);
-                        mbar_arrive_expect_tx(&full[stage], tx);
-                        tma_load_2d(sa_s, &prm.tmap_a, &full[stage], k0, ti.row0);
-                        tma_load_2d(sa_s + Lay::kABytes, &prm.tmap_b, &full[stage], k0, n0);
-                        if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
+                        if (is_a) mbar_arrive_expect_tx(&full[stage], tx);
+                        tma_load_2d(st + dst_off, map, &full[stage], k0, row);
+                        if (tl && is_a && issued < 15) tl[1 + issued] = globaltimer_ns();
                         ++issued;
                         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     }
@@ -457,10 +627,14 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     const uint32_t k0 = kb * bk_elems;
-                    mbar_arrive_expect_tx(&full[stage], tx);
-                    tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
-                    tma_tile(&prm.tmap_b, sa_s + Lay::kABytes, &full[stage], b_mn, b_rank3, n0, BN, k0, zc, bk_elems);
-                    if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
+                    if (is_a) {
+                        mbar_arrive_expect_tx(&full[stage], tx);
+                        tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
+                    } else {
+                        tma_tile(&prm.tmap_b, sa_s + Lay::kABytes, &full[stage], b_mn, b_rank3, n0, BN, k0, zc,
+                                 bk_elems);
+                    }
+                    if (tl && is_a && issued < 15) tl[1 + issued] = globaltimer_ns();
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -472,6 +646,68 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 for (uint32_t i = 0; i < pending; ++i) {
                     if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
                     mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
+                }
+            }
+        } else if (warp_copies && KIND == kKindMXF8 && prm.g.sf_tma) {
+            // Scale factors by TMA: every 4 k-blocks lane 0 loads 16 bytes of
+            // each of the tile's rows (the codes of 4 k-blocks) into one of two
+            // raw slots, one group ahead; per k-block the warp rewrites them into
+            // the stage's lines in the order tcgen05.cp 32x128b.warpx4 expects
+            // (16-byte line l holds rows l, l+32, l+64, l+96, 4 bytes each) and
+            // makes one arrival on the stage's full barrier.  Only this warp
+            // touches the raw slots, so they need no empty barrier.
+            constexpr uint32_t kRawA = Lay::kRawRowsA * 16u;
+            constexpr uint32_t raw_bytes = Lay::kRawSlotBytes;
+            uint32_t stage = 0, phase = 0;
+            uint32_t rg = 0, cg = 0;                     // raw groups issued / consumed (slot = n % 2)
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
+                const int32_t n0 = static_cast<int32_t>(ti.n * BN);
+                const uint32_t ngroups = (num_kb + 3) / 4;
+                auto issue = [&](uint32_t g) {
+                    uint8_t* slot = smem + Lay::kRawOff + (rg & 1u) * raw_bytes;
+                    fence_proxy_async_smem();            // earlier reads of this slot before the new writes
+                    mbar_arrive_expect_tx(&raw_full[rg & 1u], raw_bytes);
+                    tma_load_2d(slot, &prm.tmap_sfa, &raw_full[rg & 1u], static_cast<int32_t>(g * 16), ti.row0);
+                    tma_load_2d(slot + kRawA, &prm.tmap_sfb, &raw_full[rg & 1u], static_cast<int32_t>(g * 16), n0);
+                    ++rg;
+                };
+                if (lane == 0) issue(0);
+                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                    const uint32_t j = kb & 3u;
+                    if (j == 0) {
+                        if (lane == 0 && kb / 4 + 1 < ngroups) issue(kb / 4 + 1);
+                        if (!warp_wait(&raw_full[cg & 1u], (cg >> 1) & 1u, ctl, 6)) { ok = false; break; }
+                    }
+                    if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+                    const uint8_t* raw = smem + Lay::kRawOff + (cg & 1u) * raw_bytes + lane * 16u + j * 4u;
+                    uint8_t* sfa_s = smem + Lay::kSfOff + stage * Lay::kSfStageBytes;
+                    uint8_t* sfb_s = sfa_s + Lay::kSfaBytes;
+                    *reinterpret_cast<uint4*>(sfa_s + lane * 16u) =
+                        make_uint4(*reinterpret_cast<const uint32_t*>(raw), *reinterpret_cast<const uint32_t*>(raw + 512),
+                                   *reinterpret_cast<const uint32_t*>(raw + 1024),
+                                   *reinterpret_cast<const uint32_t*>(raw + 1536));
+#pragma unroll
+                    for (uint32_t h = 0; h < BN / 128; ++h) {
+                        const uint8_t* rb = raw + kRawA + h * 2048u;
+                        *reinterpret_cast<uint4*>(sfb_s + h * 512 + lane * 16u) =
+                            make_uint4(*reinterpret_cast<const uint32_t*>(rb), *reinterpret_cast<const uint32_t*>(rb + 512),
+                                       *reinterpret_cast<const uint32_t*>(rb + 1024),
+                                       *reinterpret_cast<const uint32_t*>(rb + 1536));
+                    }
+                    fence_proxy_async_smem();            // generic writes -> tcgen05.cp's reads
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[stage]);
+                    if (j == 3 || kb + 1 == num_kb) ++cg;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok && lane == 0) {
+                // let the raw scale copies in flight land before the CTA exits
+                while (cg < rg) {
+                    mbar_wait_drain(&raw_full[cg & 1u], (cg >> 1) & 1u, ctl.timeout_ns);
+                    ++cg;
                 }
             }
         } else if (warp_copies) {
@@ -519,13 +755,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                             load_tile_plain(sb_s,
                                             b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
                                             b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane);
-                        if (plain_stores) {
-                            cp_async_wait_all();         // the other operand may have used cp.async
-                            fence_proxy_async_smem();
-                            mbar_arrive(&full[stage]);
-                        } else {
-                            cp_async_arrive_noinc(&full[stage]);
-                        }
+                        fence_proxy_async_smem();        // generic-proxy writes -> the MMA's reads
+                        mbar_arrive(&full[stage]);
                         if (tma_thread) {                // the TMA half of a mixed stage
                             mbar_arrive_expect_tx(&full[stage], tx);
                             if (a_tma)
@@ -556,6 +787,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const uint32_t b_step = b_mn ? umma_k_bytes_mn : 32u;
         const uint32_t idesc = idesc_f16(prm.g.ab_fmt, a_mn, b_mn, kBM, BN);
         const uint32_t smem_base = smem_u32(smem);
+        const uint32_t sf_tma = prm.g.sf_tma;
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
         bool ok = true, any_mma = false;
         const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
@@ -570,9 +802,9 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
-                    // stages written by cp.async / plain stores need a proxy
-                    // fence before tcgen05 reads them
-                    if (lanes_copy) fence_proxy_async_smem();
+                    // scale factors written by cp.async need a proxy fence before
+                    // tcgen05 reads them (every other writer fences before it arrives)
+                    if (KIND == kKindMXF8 && !sf_tma) fence_proxy_async_smem();
                     {
                         if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
                         const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
@@ -619,7 +851,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         prefetch_operands(prm.g, threadIdx.x - 64, 128);
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread
-        const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
+        const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec, acc_vec = prm.g.acc_vec;
+        uint8_t* const epi_stage = smem + Lay::kEpiOff + q * kEpiWarpBytes;
         uint8_t* const C = prm.g.C;
         const int64_t ldc = prm.g.ldc, c_bs = prm.g.c_batch_stride;
         const float* scale_a = prm.g.scale_a;
@@ -643,8 +876,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             }
             const bool row_ok = r < ti.m_act;
             const uint32_t grow = ti.row0 + r;
+            const uint32_t rows_valid = ti.m_act > q * 32 ? min(32u, ti.m_act - q * 32) : 0u;   // warp-uniform
             const int64_t cbase = mode == kModeBatched ? static_cast<int64_t>(ti.tag) * c_bs : 0;
-            uint8_t* crow = C + (cbase + static_cast<int64_t>(grow) * ldc) * csize;
+            // row q*32 of the tile (lane 0's row)
+            uint8_t* const cwarp = C + (cbase + static_cast<int64_t>(ti.row0 + q * 32) * ldc) * csize;
             const uint32_t n0 = ti.n * BN;
             int32_t run[EPI == kEpiDequant ? BN : 1];
             if (EPI == kEpiDequant) {
@@ -661,8 +896,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     for (uint32_t cc = 0; cc < BN / 32; ++cc) {
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(taddr + cc * 32, v);
-                        if (row_ok && cc * 32 < ti.n_act)
-                            store_row_chunk(c_type, c_vec, crow, n0 + cc * 32, ti.n_act - cc * 32, v);
+                        if (rows_valid && cc * 32 < ti.n_act)
+                            store_chunk_coalesced(epi_stage, c_type, c_vec,
+                                                  cwarp + static_cast<int64_t>(n0 + cc * 32) * csize, ldc * csize,
+                                                  rows_valid, min(32u, ti.n_act - cc * 32), v, lane);
                     }
                 } else {
 #pragma unroll
@@ -681,8 +918,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             if (!ok) break;
             if (tl && warp == 2 && lane == 0 && ep_tile < 8) tl[40 + ep_tile] = globaltimer_ns();
             ++ep_tile;
-            if (EPI == kEpiDequant && row_ok) {
-                const float sa_row = scale_a[grow];
+            if (EPI == kEpiDequant && rows_valid) {
+                const float sa_row = row_ok ? scale_a[grow] : 0.f;
 #pragma unroll
                 for (uint32_t cc = 0; cc < BN / 32; ++cc) {
                     if (cc * 32 >= ti.n_act) break;
@@ -694,22 +931,14 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         const float sb = j < nv ? __ldg(scale_b + col0 + j) : 0.f;
                         v[j] = __float_as_uint(static_cast<float>(run[(EPI == kEpiDequant ? cc * 32 + j : 0)]) * sa_row * sb);
                     }
-                    store_row_chunk(c_type, c_vec, crow, col0, nv, v);
+                    store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(col0) * csize,
+                                          ldc * csize, rows_valid, nv, v, lane);
                     if (acc_out) {
-                        int32_t* arow = acc_out + static_cast<int64_t>(grow) * ldc + col0;
-                        if (c_vec && nv == 32) {
 #pragma unroll
-                            for (uint32_t j = 0; j < 32; j += 4)
-                                *reinterpret_cast<int4*>(arow + j) =
-                                    make_int4(run[(EPI == kEpiDequant ? cc * 32 + j : 0)],
-                                              run[(EPI == kEpiDequant ? cc * 32 + j + 1 : 0)],
-                                              run[(EPI == kEpiDequant ? cc * 32 + j + 2 : 0)],
-                                              run[(EPI == kEpiDequant ? cc * 32 + j + 3 : 0)]);
-                        } else {
-#pragma unroll
-                            for (uint32_t j = 0; j < 32; ++j)
-                                if (j < nv) arow[j] = run[(EPI == kEpiDequant ? cc * 32 + j : 0)];
-                        }
+                        for (uint32_t j = 0; j < 32; ++j)
+                            v[j] = static_cast<uint32_t>(run[(EPI == kEpiDequant ? cc * 32 + j : 0)]);
+                        uint8_t* awarp = reinterpret_cast<uint8_t*>(acc_out + static_cast<int64_t>(ti.row0 + q * 32) * ldc + col0);
+                        store_chunk_coalesced(epi_stage, kOutS32, acc_vec, awarp, ldc * 4, rows_valid, nv, v, lane);
                     }
                 }
             }

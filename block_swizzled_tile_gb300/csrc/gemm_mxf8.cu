@@ -10,13 +10,13 @@ namespace bst {
 template <uint32_t BN, uint32_t STAGES, uint32_t ACC>
 static cudaError_t launch_one(const GemmParams& p, uint32_t grid, cudaStream_t stream) {
     using Lay = GemmLayout<BN, STAGES, ACC, kKindMXF8>;
+    static_assert(Lay::smem_bytes(0) <= 232448, "shared memory per CTA");
     static std::atomic<uint64_t> attr_done{0};
     auto kern = gemm_kernel<BN, STAGES, ACC, kKindMXF8, kEpiStore>;
     const uint32_t smem = Lay::smem_bytes(0);
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, attr_done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, threads_for<kKindMXF8>(), smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_gemm(kern, p, grid, threads_for<kKindMXF8>(), smem, stream);
 }
 
 cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream) {

@@ -12,10 +12,10 @@ static cudaError_t launch_pair_one(const GemmParams& p, uint32_t max_pairs, cuda
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(kMaxGroups), attr_done);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kNumThreads);
+    cfg.blockDim = dim3(kPairThreads);
     cfg.dynamicSmemBytes = Lay::smem_bytes(p.g.mode == kModeGrouped ? p.g.G : 0);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -36,6 +36,7 @@ static cudaError_t launch_pair_one(const GemmParams& p, uint32_t max_pairs, cuda
     }
     const uint32_t pairs = std::max(1u, std::min(max_pairs, static_cast<uint32_t>(n)));
     cfg.gridDim = dim3(2 * pairs);
+    add_pdl(cfg, attr);
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -47,16 +48,26 @@ cudaError_t launch_pair(const GemmParams& p, uint32_t bn, uint32_t max_pairs, cu
     }
 }
 
-template <uint32_t S>
+// Ring depth of each split-K instantiation: what is left of the shared
+// memory after the receive slots and the epilogue staging.
+template <uint32_t BN, uint32_t S>
+struct SplitStages;
+template <> struct SplitStages<256, 2> { static constexpr uint32_t value = 4; };
+template <> struct SplitStages<128, 2> { static constexpr uint32_t value = 7; };
+template <> struct SplitStages<256, 4> { static constexpr uint32_t value = 3; };
+template <> struct SplitStages<128, 4> { static constexpr uint32_t value = 6; };
+
+template <uint32_t BN, uint32_t S>
 struct SplitLaunch {
-    using Lay = PairLayout<256, kPairStages256>;
-    static constexpr auto kern = gemm_pair_splitk_kernel<256, kPairStages256, S>;
+    static constexpr uint32_t kStages = SplitStages<BN, S>::value;
+    using Lay = SplitLayout<BN, kStages, S>;
+    static constexpr auto kern = gemm_pair_splitk_kernel<BN, kStages, S>;
 
     static cudaLaunchConfig_t config(uint32_t tiles, cudaStream_t stream, cudaLaunchAttribute* attr) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * S * tiles);
-        cfg.blockDim = dim3(kNumThreads);
-        cfg.dynamicSmemBytes = Lay::smem_bytes(0);
+        cfg.blockDim = dim3(kPairThreads);
+        cfg.dynamicSmemBytes = Lay::smem_bytes();
         cfg.stream = stream;
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2 * S;
@@ -69,7 +80,7 @@ struct SplitLaunch {
 
     static cudaError_t prepare() {
         static std::atomic<uint64_t> attr_done{0};
-        return set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(0), attr_done);
+        return set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(), attr_done);
     }
 
     // clusters of 2*S CTAs that can be resident at once on the current device
@@ -94,26 +105,35 @@ struct SplitLaunch {
     static cudaError_t launch(const GemmParams& p, uint32_t tiles, cudaStream_t stream) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         cudaLaunchConfig_t cfg = config(tiles, stream, attr);
+        add_pdl(cfg, attr);
         return cudaLaunchKernelEx(&cfg, kern, p);
     }
 };
 
-cudaError_t launch_pair_splitk(const GemmParams& p, uint32_t splits, uint32_t tiles, cudaStream_t stream) {
-    switch (splits) {
-        case 2: return SplitLaunch<2>::launch(p, tiles, stream);
-        case 4: return SplitLaunch<4>::launch(p, tiles, stream);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_pair_splitk(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream) {
+    if (bn == 256 && splits == 2) return SplitLaunch<256, 2>::launch(p, tiles, stream);
+    if (bn == 128 && splits == 2) return SplitLaunch<128, 2>::launch(p, tiles, stream);
+    if (bn == 256 && splits == 4) return SplitLaunch<256, 4>::launch(p, tiles, stream);
+    if (bn == 128 && splits == 4) return SplitLaunch<128, 4>::launch(p, tiles, stream);
+    return cudaErrorInvalidValue;
 }
 
-cudaError_t splitk_resident_clusters(uint32_t splits, uint32_t* out) {
-    switch (splits) {
-        case 2: return SplitLaunch<2>::resident(out);
-        case 4: return SplitLaunch<4>::resident(out);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t splitk_resident_clusters(uint32_t bn, uint32_t splits, uint32_t* out) {
+    if (bn == 256 && splits == 2) return SplitLaunch<256, 2>::resident(out);
+    if (bn == 128 && splits == 2) return SplitLaunch<128, 2>::resident(out);
+    if (bn == 256 && splits == 4) return SplitLaunch<256, 4>::resident(out);
+    if (bn == 128 && splits == 4) return SplitLaunch<128, 4>::resident(out);
+    return cudaErrorInvalidValue;
+}
+
+uint32_t smem_splitk(uint32_t bn, uint32_t splits) {
+    if (bn == 256 && splits == 2) return SplitLaunch<256, 2>::Lay::smem_bytes();
+    if (bn == 128 && splits == 2) return SplitLaunch<128, 2>::Lay::smem_bytes();
+    if (bn == 256 && splits == 4) return SplitLaunch<256, 4>::Lay::smem_bytes();
+    if (bn == 128 && splits == 4) return SplitLaunch<128, 4>::Lay::smem_bytes();
+    return 0;
 }
 
 uint32_t smem_pair(uint32_t bn, uint32_t groups) {

@@ -31,13 +31,20 @@
 
 namespace bst {
 
+// Warps of the CTA-pair kernels: 0 issues A loads (and the leader's arrival
+// on full[]), 1 the MMA, 2-5 the epilogue, 6 issues B loads (one thread
+// issues a TMA about every 0.1-0.15 us, so A and B get a thread each).
+constexpr uint32_t kPairThreads = 224;
+constexpr uint32_t kPairBWarp = 6;
+
 template <uint32_t BN, uint32_t STAGES>
 struct PairLayout {
     static constexpr uint32_t kACC = 2;
     static constexpr uint32_t kABytes = kBM * kLine;            // 128 A rows per CTA
     static constexpr uint32_t kBBytes = (BN / 2) * kLine;       // BN/2 B rows per CTA
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kBarOff = STAGES * kStageBytes;
+    static constexpr uint32_t kEpiOff = STAGES * kStageBytes;             // 4 epilogue warps x 4 KB staging
+    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 * kACC + 1;
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
@@ -48,7 +55,7 @@ struct PairLayout {
 };
 
 template <uint32_t BN, uint32_t STAGES>
-__global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams prm) {
+__global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams prm) {
     using Lay = PairLayout<BN, STAGES>;
     constexpr uint32_t ACC = Lay::kACC;
     constexpr uint32_t TM = 2 * kBM;
@@ -109,6 +116,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
         tmem_alloc_pair(tmem_holder, Lay::kTmemCols);
         tmem_relinquish_pair();
     }
+    // set-up above touches no global memory: it overlaps the previous kernel
+    griddep_wait();
+    griddep_launch_dependents();
     if (mode == kModeGrouped && warp == 2)
         build_group_table(gt, prm.g.group_m, G, N, TM, BN, sa.total_m, err, tiles_smem, lane);
     tc_fence_before();
@@ -120,14 +130,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
 
-    if (warp == 0) {
+    if (warp == 0 || warp == kPairBWarp) {
         // ------------------------------------------------------ producer --
-        // both CTAs: own A half and own B half, counted on the leader's full[s]
+        // both CTAs: own A half (warp 0) and own B half (warp 6), counted on
+        // the leader's full[s]; the leader's A thread is the one arrival
         const uint32_t full_leader = map_to_cta(smem_u32(full), 0);
         constexpr uint32_t tx = Lay::kABytes + Lay::kBBytes;
+        const bool is_a = warp == 0;
         uint32_t stage = 0, phase = 0, issued = 0;
         bool ok = true;
-        // a single thread issues every load (cheaper per k-block than a
+        // single threads issue the loads (cheaper per k-block than a
         // warp-wide loop with one active lane)
         for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t += nclusters) {
             const TileInfo ti = tile_info(sa, t, TM, BN, gt);
@@ -141,17 +153,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
                     uint8_t* sb_s = sa_s + Lay::kABytes;
                     const uint32_t bar = full_leader + stage * 8;
                     const int32_t k0 = kb * bk_elems;
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
-                    if (!a_mn) {
-                        if (a_rank3) tma_load_3d_pair(sa_s, &prm.tmap_a, bar, k0, a_row, zc);
-                        else tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);
-                    } else {
-                        for (uint32_t j = 0; j < kBM / bk_elems; ++j) {
-                            if (a_rank3) tma_load_3d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0, zc);
-                            else tma_load_2d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0);
+                    if (is_a) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
+                        if (!a_mn) {
+                            if (a_rank3) tma_load_3d_pair(sa_s, &prm.tmap_a, bar, k0, a_row, zc);
+                            else tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);
+                        } else {
+                            for (uint32_t j = 0; j < kBM / bk_elems; ++j) {
+                                if (a_rank3) tma_load_3d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0, zc);
+                                else tma_load_2d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0);
+                            }
                         }
-                    }
-                    if (!b_mn) {
+                    } else if (!b_mn) {
                         if (b_rank3) tma_load_3d_pair(sb_s, &prm.tmap_b, bar, k0, b_col, zc);
                         else tma_load_2d_pair(sb_s, &prm.tmap_b, bar, k0, b_col);
                     } else {
@@ -160,13 +173,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
                             else tma_load_2d_pair(sb_s + j * bk_elems * kLine, &prm.tmap_b, bar, b_col + j * bk_elems, k0);
                         }
                     }
-                    if (tl && issued < 15) tl[1 + issued] = globaltimer_ns();
+                    if (tl && is_a && issued < 15) tl[1 + issued] = globaltimer_ns();
                 }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        if (lane == 0 && !ok && rank == 0) {
+        if (lane == 0 && !ok && rank == 0 && is_a) {
             // let the copies of both CTAs already counted here land
             uint32_t s = stage, ph = phase;
             const uint32_t pending = issued < STAGES ? issued : STAGES;
@@ -222,8 +235,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
         // ---------------------------------------------- epilogue (both) --
         prefetch_operands(prm.g, threadIdx.x - 64, 128);
         const uint32_t q = warp & 3u;                    // TMEM lane quarter of this warp
-        const uint32_t r = rank * kBM + q * 32 + lane;   // row of this thread in the 256-row tile
+        const uint32_t wrow = rank * kBM + q * 32;       // first row of this warp in the 256-row tile
         const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
+        uint8_t* const epi_stage = smem + Lay::kEpiOff + q * kEpiWarpBytes;
         uint8_t* const C = prm.g.C;
         const int64_t ldc = prm.g.ldc, c_bs = prm.g.c_batch_stride;
         uint32_t* const trace = prm.g.trace;
@@ -242,10 +256,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
                     atomicOr(&err[0], kErrTraceOverflow);
                 }
             }
-            const bool row_ok = r < ti.m_act;
-            const uint32_t grow = ti.row0 + r;
+            const uint32_t rows_valid = ti.m_act > wrow ? min(32u, ti.m_act - wrow) : 0u;   // warp-uniform
             const int64_t cbase = mode == kModeBatched ? static_cast<int64_t>(ti.tag) * c_bs : 0;
-            uint8_t* crow = C + (cbase + static_cast<int64_t>(grow) * ldc) * csize;
+            uint8_t* const cwarp = C + (cbase + static_cast<int64_t>(ti.row0 + wrow) * ldc) * csize;
             const uint32_t n0 = ti.n * BN;
             if (!warp_wait(&tfull[acc], acc_phase, ctl, 4)) { ok = false; break; }
             tc_fence_after();
@@ -255,8 +268,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_kernel(const __grid_
             for (uint32_t cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + cc * 32, v);
-                if (row_ok && cc * 32 < ti.n_act)
-                    store_row_chunk(c_type, c_vec, crow, n0 + cc * 32, ti.n_act - cc * 32, v);
+                if (rows_valid && cc * 32 < ti.n_act)
+                    store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(n0 + cc * 32) * csize,
+                                          ldc * csize, rows_valid, min(32u, ti.n_act - cc * 32), v, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -285,32 +299,53 @@ namespace bst {
 // CTA pairs ("09_split_matmul" of "Block Dispatch Policies" names split
 // GEMMs; the split here is along K).  A cluster of 2*S CTAs owns one tile:
 // CTA pair p (cluster ranks 2p, 2p+1) accumulates k-blocks
-// [p*ceil(kb/S), (p+1)*ceil(kb/S)) of it exactly as gemm_pair_kernel does.
-// The S partial tiles are then summed through distributed shared memory:
-// each split finishes R = 128/S of the 128 accumulator rows its CTA holds.
-// After a cluster barrier (every pipeline of the cluster drained, so the
-// stage buffers can be reused), epilogue warp q of each CTA sends its 32
-// accumulator rows to the CTA of split 32q/R on the same half of the tile
-// (reduce-scatter); after a second barrier each CTA adds the S slots it
-// received for its R rows, rounds once and stores them.  Nothing goes
-// through global memory and no second kernel runs.
+// [p*kb/S, (p+1)*kb/S) of it exactly as gemm_pair_kernel does, into one TMEM
+// accumulator of 128 rows per CTA.
+//
+// The S fp32 partial tiles are summed on chip.  Split g finishes columns
+// [g*W, (g+1)*W) (W = BN/S) of each CTA's 128 rows.  Once its pair's MMAs are
+// done (the stage ring is then idle), every epilogue warp copies, for each
+// other split g, its 32 rows of g's columns into its own ring, and one bulk
+// copy moves them into a receive slot of the CTA of split g (same half),
+// completing on that CTA's receive barrier of the same warp.  The receive
+// slots sit outside the ring, so a sender never waits for the receiver.  The
+// warp then adds the S-1 slots it received to its own rows of its own
+// columns, rounds once and stores them through the coalesced epilogue.  All
+// four warps send and finish in parallel; nothing goes through global memory
+// and no second kernel runs.
+//
+// Shared-memory rows of a partial (W fp32) keep their 16-byte granules
+// XOR-swizzled by row (granule c at c ^ (row % 8)), so both the row-per-lane
+// writes and the row-per-lane reads are conflict-free.
 template <uint32_t BN, uint32_t STAGES, uint32_t S>
 struct SplitLayout {
-    using Pair = PairLayout<BN, STAGES>;
-    static constexpr uint32_t kRows = kBM / S;                     // rows each split finishes
-    static constexpr uint32_t kRowFloats = BN + 4;                 // padded: conflict-free 16-byte stores
-    static constexpr uint32_t kSlotBytes = kRows * kRowFloats * 4; // the rows one split sends
-    static_assert(S * kSlotBytes <= STAGES * Pair::kStageBytes, "receive slots reuse the stage buffers");
+    static constexpr uint32_t kABytes = kBM * kLine;
+    static constexpr uint32_t kBBytes = (BN / 2) * kLine;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kW = BN / S;                         // columns each split finishes
+    static constexpr uint32_t kSlotBytes = 32 * kW * 4;            // one warp's rows of W columns
+    static constexpr uint32_t kSlots = 4 * (S - 1);                // per CTA, sent and received
+    static constexpr uint32_t kRecvOff = STAGES * kStageBytes;
+    static constexpr uint32_t kRecvBytes = kSlots * kSlotBytes;
+    static constexpr uint32_t kEpiOff = kRecvOff + kRecvBytes;
+    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 4;       // full, empty, tfull, drain, recv[4]
+    static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr uint32_t kTmemCols = BN;
+    static constexpr uint32_t smem_bytes() { return 1024 + kMiscOff + 16; }
+    static_assert(S == 2 || S == 4, "splits");
+    static_assert(kW % 32 == 0, "whole 32-column chunks per split");
+    static_assert(kSlots * kSlotBytes <= STAGES * kStageBytes, "sender staging reuses the ring");
+    static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert(smem_bytes() <= 232448, "shared memory per CTA");
 };
 
 template <uint32_t BN, uint32_t STAGES, uint32_t S>
-__global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_splitk_kernel(const __grid_constant__ GemmParams prm) {
-    using Lay = PairLayout<BN, STAGES>;
+__global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const __grid_constant__ GemmParams prm) {
     using SL = SplitLayout<BN, STAGES, S>;
     constexpr uint32_t TM = 2 * kBM;
     constexpr uint32_t BH = BN / 2;
-    static_assert(S == 2 || S == 4, "splits");
-    static_assert(BN == 256, "split-K runs 256 x 256 tiles");
+    static_assert(BN == 128 || BN == 256, "BN");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -320,19 +355,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_splitk_kernel(const 
     uint32_t* const err = prm.g.err;
     constexpr uint32_t bk_elems = 64;
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL::kBarOff);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* drain = bars + 2 * STAGES + 2 * Lay::kACC;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    uint64_t* drain = bars + 2 * STAGES + 1;
+    uint64_t* recv = bars + 2 * STAGES + 2;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + SL::kMiscOff);
     uint32_t* tmem_holder = misc;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     uint64_t* const tl = prm.g.timeline ? prm.g.timeline + static_cast<uint64_t>(blockIdx.x) * 64 : nullptr;
-    if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
+    const uint64_t t_entry = globaltimer_ns();
     const uint32_t crank = cluster_rank();
     const uint32_t split = crank >> 1, half = crank & 1u, leader = crank & ~1u;
     const uint16_t pair_mask = static_cast<uint16_t>(3u << leader);
@@ -348,58 +384,69 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_splitk_kernel(const 
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(&tfull[0], 1);
+        mbar_init(tfull, 1);
         mbar_init(drain, 1);
+        for (uint32_t o = 0; o < 4; ++o) mbar_init(&recv[o], 1);
         *abort_flag = 0;
         fence_barrier_init();
+        // the receive barrier of each epilogue warp expects the S-1 partials of its rows
+        for (uint32_t o = 0; o < 4; ++o) mbar_arrive_expect_tx(&recv[o], (S - 1) * SL::kSlotBytes);
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&prm.tmap_a);
         prefetch_tmap(&prm.tmap_b);
     }
     if (warp == 1) {
-        tmem_alloc_pair(tmem_holder, Lay::kTmemCols);
+        tmem_alloc_pair(tmem_holder, SL::kTmemCols);
         tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
+    cluster_sync();                                  // barriers of every CTA initialised
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    if (tl && threadIdx.x == 0) tl[1] = globaltimer_ns();
+    // set-up above touches no global memory: it overlaps the previous kernel
+    griddep_wait();
+    griddep_launch_dependents();
+    if (tl && threadIdx.x == 0) { tl[0] = t_entry; tl[1] = globaltimer_ns(); }
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     GroupTable gt{nullptr, nullptr, 0};
     TileInfo ti{};
     if (has_tile) ti = tile_info(sa, t, TM, BN, gt);
 
-    if (warp == 0 && lane == 0 && has_tile) {
+    if ((warp == 0 || warp == kPairBWarp) && lane == 0 && has_tile) {
         // ------------------------------------------------------ producer --
+        // A half by warp 0 (the pair leader's is the one arrival), B half by warp 6
+        const bool is_a = warp == 0;
         const uint32_t full_leader = map_to_cta(smem_u32(full), leader);
-        constexpr uint32_t tx = Lay::kABytes + Lay::kBBytes;
+        constexpr uint32_t tx = SL::kABytes + SL::kBBytes;
         const uint32_t a_row = ti.row0 + half * kBM;
         const uint32_t b_col = ti.n * BN + half * BH;
         uint32_t stage = 0, phase = 0, issued = 0;
         bool ok = true;
         for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
-            uint8_t* sa_s = smem + stage * Lay::kStageBytes;
-            uint8_t* sb_s = sa_s + Lay::kABytes;
+            uint8_t* sa_s = smem + stage * SL::kStageBytes;
+            uint8_t* sb_s = sa_s + SL::kABytes;
             const uint32_t bar = full_leader + stage * 8;
             const int32_t k0 = kb * bk_elems;
-            if (half == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
-            if (!a_mn) tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);
-            else
-                for (uint32_t j = 0; j < kBM / bk_elems; ++j)
-                    tma_load_2d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0);
-            if (!b_mn) tma_load_2d_pair(sb_s, &prm.tmap_b, bar, k0, b_col);
-            else
+            if (is_a) {
+                if (half == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
+                if (!a_mn) tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);
+                else
+                    for (uint32_t j = 0; j < kBM / bk_elems; ++j)
+                        tma_load_2d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0);
+            } else if (!b_mn) {
+                tma_load_2d_pair(sb_s, &prm.tmap_b, bar, k0, b_col);
+            } else {
                 for (uint32_t j = 0; j < BH / bk_elems; ++j)
                     tma_load_2d_pair(sb_s + j * bk_elems * kLine, &prm.tmap_b, bar, b_col + j * bk_elems, k0);
-            if (tl && issued < 14) tl[2 + issued] = globaltimer_ns();
+            }
+            if (tl && is_a && issued < 14) tl[2 + issued] = globaltimer_ns();
             ++issued;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (!ok && half == 0) {
+        if (!ok && half == 0 && is_a) {
             uint32_t s = stage, ph = phase;
             const uint32_t pending = issued < STAGES ? issued : STAGES;
             for (uint32_t i = 0; i < pending; ++i) {
@@ -420,9 +467,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_splitk_kernel(const 
         for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
             if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
+            const uint32_t sa_addr = smem_base + stage * SL::kStageBytes;
             const uint64_t adesc = smem_desc(sa_addr, a_lbo, 1024, kSwizzle128B);
-            const uint64_t bdesc = smem_desc(sa_addr + Lay::kABytes, b_lbo, 1024, kSwizzle128B);
+            const uint64_t bdesc = smem_desc(sa_addr + SL::kABytes, b_lbo, 1024, kSwizzle128B);
 #pragma unroll
             for (uint32_t kk = 0; kk < 4; ++kk)
                 umma_f16_pair(tmem_base, adesc + ((kk * a_step) >> 4), bdesc + ((kk * b_step) >> 4), idesc,
@@ -432,87 +479,109 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_pair_splitk_kernel(const 
             any_mma = true;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (ok) umma_commit_pair_mc(&tfull[0], pair_mask);
+        if (ok) umma_commit_pair_mc(tfull, pair_mask);
         else if (any_mma) {
             umma_commit_pair_mc(drain, static_cast<uint16_t>(1u << crank));
             mbar_wait_drain(drain, 0, ctl.timeout_ns);
         }
-    }
-
-    // every role of every CTA of the cluster is done with the pipeline: the
-    // epilogue waits for its accumulator first
-    bool acc_ok = true;
-    if (warp >= 2 && has_tile && has_k) acc_ok = warp_wait(&tfull[0], 0, ctl, 4);
-    if (tl && warp == 2 && lane == 0) tl[32] = globaltimer_ns();
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();
-    tc_fence_after();
-    if (tl && threadIdx.x == 64) tl[33] = globaltimer_ns();
-
-    // reduce-scatter: warp q's 32 rows go to split 32q/R (same half), into
-    // the slot of the sending split
-    if (warp >= 2 && has_tile) {
-        const uint32_t q = warp & 3u;
-        const uint32_t dest = 2 * ((q * 32) / SL::kRows) + half;      // a rank of this cluster: < 2*S
-        const uint32_t row_in_slot = (q * 32) % SL::kRows + lane;
-        const uint32_t slot =
-            map_to_cta(smem_u32(smem), dest) + split * SL::kSlotBytes + row_in_slot * SL::kRowFloats * 4;
-        const bool have = acc_ok && has_k;            // an empty range sends zeros
+    } else if (warp >= 2 && warp < 6 && has_tile) {
+        // ----------------------------------------------------- epilogue --
+        const uint32_t q = warp & 3u;                    // TMEM lane quarter of this warp
         const uint32_t taddr = tmem_base + ((q * 32) << 16);
+        constexpr uint32_t W = SL::kW;
+        // this warp's rows are final once its pair's MMAs are done
+        bool acc_ok = true;
+        if (has_k) acc_ok = warp_wait(tfull, 0, ctl, 4);
+        tc_fence_after();
+        if (tl && warp == 2 && lane == 0) tl[32] = globaltimer_ns();
+        const bool own_valid = acc_ok && has_k;          // else this split's partial counts as zero
+        // send: for every other split g, this warp's rows of g's columns
+        uint32_t gi = 0;
 #pragma unroll 1
-        for (uint32_t cc = 0; cc < BN / 32; ++cc) {
-            uint32_t v[32];
-            if (have) tmem_ld_32x32b_x32(taddr + cc * 32, v);
+        for (uint32_t g = 0; g < S; ++g) {
+            if (g == split) continue;
+            uint8_t* stage_rows = smem + (q * (S - 1) + gi) * SL::kSlotBytes;
+            uint8_t* my_row = stage_rows + lane * (W * 4);
+#pragma unroll 1
+            for (uint32_t cc = 0; cc < W / 32; ++cc) {
+                uint32_t v[32];
+                if (own_valid) tmem_ld_32x32b_x32(taddr + g * W + cc * 32, v);
+                else {
 #pragma unroll
-            for (uint32_t j = 0; j < 32; j += 4) {
-                if (have) st_cluster_v4(slot + (cc * 32 + j) * 4, v[j], v[j + 1], v[j + 2], v[j + 3]);
-                else st_cluster_v4(slot + (cc * 32 + j) * 4, 0u, 0u, 0u, 0u);
+                    for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
+                }
+#pragma unroll
+                for (uint32_t gg = 0; gg < 8; ++gg) {
+                    const uint32_t granule = (cc * 8 + gg) ^ (lane & 7u);
+                    *reinterpret_cast<uint4*>(my_row + granule * 16) =
+                        make_uint4(v[4 * gg], v[4 * gg + 1], v[4 * gg + 2], v[4 * gg + 3]);
+                }
             }
+            fence_proxy_async_smem();                    // generic writes -> the bulk copy's reads
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t dest = 2 * g + half;      // split g, same half
+                const uint32_t slot = q * (S - 1) + (split < g ? split : split - 1);
+                const uint32_t dst = map_to_cta(smem_u32(smem + SL::kRecvOff + slot * SL::kSlotBytes), dest);
+                const uint32_t bar = map_to_cta(smem_u32(&recv[q]), dest);
+                bulk_copy_to_cluster(dst, stage_rows, SL::kSlotBytes, bar);
+                bulk_commit_group();
+            }
+            ++gi;
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tl && threadIdx.x == 64) tl[34] = globaltimer_ns();
-    cluster_sync();
-    if (tl && threadIdx.x == 64) tl[35] = globaltimer_ns();
-
-    // sum the S slots for rows [split*R, split*R + R) of this half and store
-    if (warp >= 2 && has_tile) {
-        const uint32_t e = threadIdx.x - 64;             // 0..127: S threads per row
-        const uint32_t row = e / S;                      // 0..R-1
-        const uint32_t c0 = (e % S) * (BN / S);          // BN/S columns per thread
-        const uint32_t r = half * kBM + split * SL::kRows + row;   // row within the 256-row tile
+        if (tl && warp == 2 && lane == 0) tl[34] = globaltimer_ns();
+        // finish: own rows of own columns plus the S-1 received partials
+        const bool got = warp_wait(&recv[q], 0, ctl, 5);
+        if (tl && warp == 2 && lane == 0) tl[33] = globaltimer_ns();
+        const uint8_t* slots = smem + SL::kRecvOff + q * (S - 1) * SL::kSlotBytes + lane * (W * 4);
+        const uint32_t wrow = half * kBM + q * 32;       // first row of this warp in the tile
+        const uint32_t rows_valid = ti.m_act > wrow ? min(32u, ti.m_act - wrow) : 0u;
         const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
         const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
-        uint8_t* crow = prm.g.C + (static_cast<int64_t>(ti.row0 + r) * prm.g.ldc) * csize;
-        const float* base = reinterpret_cast<const float*>(smem) + row * SL::kRowFloats + c0;
+        const int64_t ldc = prm.g.ldc;
+        uint8_t* const cwarp = prm.g.C + static_cast<int64_t>(ti.row0 + wrow) * ldc * csize;
+        uint8_t* const epi_stage = smem + SL::kEpiOff + q * kEpiWarpBytes;
 #pragma unroll 1
-        for (uint32_t cc = 0; cc < BN / S; cc += 32) {
+        for (uint32_t cc = 0; cc < W / 32; ++cc) {
             uint32_t v[32];
+            if (own_valid) tmem_ld_32x32b_x32(taddr + split * W + cc * 32, v);
+            else {
 #pragma unroll
-            for (uint32_t j = 0; j < 32; ++j) {
-                float acc = 0.f;
-#pragma unroll
-                for (uint32_t sidx = 0; sidx < S; ++sidx) acc += base[sidx * (SL::kSlotBytes / 4) + cc + j];
-                v[j] = __float_as_uint(acc);
+                for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
             }
-            const uint32_t col = c0 + cc;
-            if (r < ti.m_act && col < ti.n_act)
-                store_row_chunk(c_type, c_vec, crow, ti.n * BN + col, ti.n_act - col, v);
+            if (got) {
+#pragma unroll
+                for (uint32_t si = 0; si < S - 1; ++si) {
+#pragma unroll
+                    for (uint32_t gg = 0; gg < 8; ++gg) {
+                        const uint32_t granule = (cc * 8 + gg) ^ (lane & 7u);
+                        const uint4 x = *reinterpret_cast<const uint4*>(slots + si * SL::kSlotBytes + granule * 16);
+                        v[4 * gg] = __float_as_uint(__uint_as_float(v[4 * gg]) + __uint_as_float(x.x));
+                        v[4 * gg + 1] = __float_as_uint(__uint_as_float(v[4 * gg + 1]) + __uint_as_float(x.y));
+                        v[4 * gg + 2] = __float_as_uint(__uint_as_float(v[4 * gg + 2]) + __uint_as_float(x.z));
+                        v[4 * gg + 3] = __float_as_uint(__uint_as_float(v[4 * gg + 3]) + __uint_as_float(x.w));
+                    }
+                }
+            }
+            const uint32_t col = split * W + cc * 32;    // column within the tile
+            if (rows_valid && col < ti.n_act)
+                store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(ti.n * BN + col) * csize,
+                                      ldc * csize, rows_valid, min(32u, ti.n_act - col), v, lane);
         }
-        if (prm.g.trace && split == 0 && half == 0 && e == 0 && t < prm.g.trace_cap) {
+        if (lane == 0) bulk_wait_read_all();             // the ring may not be left while being read
+        if (prm.g.trace && split == 0 && half == 0 && q == 0 && lane == 0 && t < prm.g.trace_cap) {
             uint32_t* tr = prm.g.trace + static_cast<uint64_t>(t) * 5;
             tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
         }
     }
+
     if (tl && threadIdx.x == 64) tl[36] = globaltimer_ns();
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
+    cluster_sync();                                  // no CTA leaves while a peer may still touch it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc_pair(tmem_base, Lay::kTmemCols);
+        tmem_dealloc_pair(tmem_base, SL::kTmemCols);
     }
     if (tl && threadIdx.x == 0) tl[37] = globaltimer_ns();
 }

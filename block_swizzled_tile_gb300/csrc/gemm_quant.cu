@@ -19,8 +19,7 @@ cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stre
     const uint32_t smem = Lay::smem_bytes(0);
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, attr_done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kNumThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_gemm(kern, p, grid, threads_for<kKindF16>(), smem, stream);
 }
 
 uint32_t smem_dequant() { return GemmLayout<128, kDequantStages, 2, kKindF16>::smem_bytes(0); }

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 
 #include "gemm_kernel.cuh"
 
@@ -24,6 +25,43 @@ inline cudaError_t set_smem_once(const void* kern, uint32_t bytes, std::atomic<u
     return e;
 }
 
+// Programmatic dependent launch for the GEMM kernels (all of which execute
+// griddepcontrol.wait before their first global-memory access): the next
+// kernel's launch and shared-memory / TMEM set-up overlap the tail of the
+// previous one.  On unless the environment sets BST_PDL=0.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("BST_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+// Appends the programmatic-serialization attribute to `cfg` (attrs must have
+// room for one more entry).
+inline void add_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs) {
+    if (!pdl_enabled()) return;
+    cudaLaunchAttribute& a = attrs[cfg.numAttrs];
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    ++cfg.numAttrs;
+}
+
+// Launches a one-CTA GEMM kernel: `grid` CTAs of `threads` threads.
+template <typename Kern>
+inline cudaError_t launch_gemm(Kern kern, const GemmParams& p, uint32_t grid, uint32_t threads, uint32_t smem,
+                               cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[1];
+    add_pdl(cfg, attrs);
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 // Kernel launches.  Each returns the cudaError_t of the launch (attribute
 // setting included); `grid` CTAs of kNumThreads threads on `stream`.
 cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
@@ -33,9 +71,11 @@ cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stre
 // more than fit on the device at once)
 cudaError_t launch_pair(const GemmParams& p, uint32_t bn, uint32_t max_pairs, cudaStream_t stream);
 // split-K CTA pairs on 256 x 256 tiles: one cluster of 2*splits CTAs per tile
-cudaError_t launch_pair_splitk(const GemmParams& p, uint32_t splits, uint32_t tiles, cudaStream_t stream);
-// clusters of 2*splits CTAs the split-K kernel can keep resident at once
-cudaError_t splitk_resident_clusters(uint32_t splits, uint32_t* out);
+cudaError_t launch_pair_splitk(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream);
+// clusters of 2*splits CTAs the split-K kernel (tile 256 x bn) can keep resident at once
+cudaError_t splitk_resident_clusters(uint32_t bn, uint32_t splits, uint32_t* out);
+// dynamic shared memory of the split-K kernel (0: no such instantiation)
+uint32_t smem_splitk(uint32_t bn, uint32_t splits);
 
 // Shared-memory bytes a launch needs (for validation of the device limit).
 uint32_t smem_dense(uint32_t bn, uint32_t groups);
@@ -59,7 +99,7 @@ cudaError_t launch_swizzle_map_grouped(const int32_t* group_m, uint32_t G, uint3
 
 // Configurations instantiated for each kernel family.
 constexpr uint32_t kDenseStages64 = 8, kDenseStages128 = 6, kDenseStages256 = 4;
-constexpr uint32_t kMxStages128 = 6, kMxStages256 = 4;
+constexpr uint32_t kMxStages128 = 6, kMxStages256 = 3;
 constexpr uint32_t kDequantStages = 6;
 constexpr uint32_t kPairStages128 = 8, kPairStages256 = 6;
 constexpr uint32_t kDequantChunkK = 1024;  // K elements per exact fp32 chunk

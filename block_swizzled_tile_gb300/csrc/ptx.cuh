@@ -138,6 +138,18 @@ static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t pari
     return false;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+
+// Waits until every grid this one depends on (launched before it on the
+// stream with programmatic serialization) has completed and its memory is
+// visible; a no-op when the kernel was launched without that attribute.
+// Nothing before it may touch global memory written by earlier work.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next grid on the stream be scheduled (it still waits for this one
+// to complete before it touches memory).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA ----
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
@@ -178,20 +190,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  );
-}
-
-// 4-, 8- or 16-byte global->shared copy of which the first src_bytes are read
-// and the rest zero-filled
-__device__ __forceinline__ void cp_async_n(void* dst, const void* src, uint32_t n, uint32_t src_bytes) {
-    if (n == 16)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                    );
-    else if (n == 8)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                    );
-    else
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                    );
 }
 
 // waits until every cp.async issued by this thread has landed
@@ -406,10 +404,23 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t cta_
         "h"(cta_mask));
 }
 
-// 16-byte store into the shared memory of any CTA of the cluster
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into the shared memory of a CTA of the
+// cluster; completion is counted in bytes on `bar_cluster` (a barrier of the
+// destination CTA).  The source must have been written through the generic
+// proxy and fenced (fence.proxy.async) before the copy is issued.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+        : "memory");
 }
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// waits until every committed bulk copy of this thread has finished reading its source
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 }  // namespace bst

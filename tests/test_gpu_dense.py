@@ -30,7 +30,9 @@ def run_dense(w, out="f16", sched=None, ldc=None):
              w["ldb"], C, DT[out], ldc, sched=sched)
     bst.check_async()
     assert canary_intact(cbuf, CANARY), "write outside C"
-    raw = host(C, np.uint8).view(np.float32 if out == "f32" else np.uint16).reshape(M, ldc)[:, :N]
+    rows = host(C, np.uint8).reshape(M, ldc * OUT_BYTES[out])
+    assert (rows[:, N * OUT_BYTES[out]:] == 0x5A).all(), "write into the padding between N and ldc"
+    raw = rows.view(np.float32 if out == "f32" else np.uint16)[:, :N]
     return decode_out(raw.copy(), out)
 
 
@@ -147,6 +149,18 @@ def test_padded_and_unaligned_leading_dims(lda_pad, ldb_pad, ldc_pad):
     assert_close_f16(got, oracle_dense(w, "f16"))
 
 
+@pytest.mark.parametrize("tm", [128, 256])
+@pytest.mark.parametrize("out,ldc_pad", [("f16", 1), ("f16", 2), ("bf16", 4), ("f16", 8), ("f32", 1), ("f32", 2),
+                                         ("f32", 4)])
+def test_output_pitch_vector_widths(tm, out, ldc_pad):
+    """Every output pitch (2-, 4-, 8- and 16-byte aligned rows) goes through the
+    staged epilogue's widest legal store; the padding columns stay untouched."""
+    M, N, K = 333, 290, 200
+    w = wl.dense16(M, N, K, "f16", b_col_major=True, seed=ldc_pad + tm, lda=208, ldb=208)
+    got = run_dense(w, out, bst.sched(2, 1, tile_m=tm), ldc=N + ldc_pad)
+    assert_close_f16(got, oracle_dense(w, out))
+
+
 def test_k_zero_writes_zeros_and_empty_is_noop():
     w = wl.dense16(70, 50, 0, "f16", seed=1, lda=1)
     got = run_dense(w, "f32")
@@ -193,6 +207,30 @@ def test_batched(acol, bcol):
         assert_close_f16(got[i], decode_out(og.gemm(a, b, "bf16"), "bf16"))
     tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
     assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, 128, 1, 0, batch=batch), dtype=np.uint32))
+
+
+@pytest.mark.parametrize("tm", [128, 256])
+def test_batched_unaligned_c_batch_stride(tm):
+    """A C batch stride of an odd number of elements limits every store to
+    2 bytes; the gaps between the batches stay untouched."""
+    M, N, K, batch = 150, 100, 128, 3
+    gap = 3
+    w = wl.dense16(M, N, K, "f16", b_col_major=True, seed=10, batch=batch)
+    A, B = dev(w["a"]), dev(w["b"])
+    sc = M * N + gap
+    cbuf, C = empty_bytes(batch * sc * 2, CANARY)
+    bst.gemm_batched(M, N, K, A, bst.F16, bst.ROW_MAJOR, w["lda"], w["a"][0].size, B, bst.F16, bst.COL_MAJOR,
+                     w["ldb"], w["b"][0].size, C, bst.F16, N, sc, batch, sched=bst.sched(2, 0, tile_m=tm))
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY)
+    raw = host(C, np.uint8)
+    for i in range(batch):
+        blk = raw[i * sc * 2:(i * sc + M * N) * 2]
+        assert (raw[(i * sc + M * N) * 2:(i + 1) * sc * 2] == 0x5A).all()
+        got = decode_out(blk.view(np.uint16).reshape(M, N).copy(), "f16")
+        a = og.as_logical(og.decode(w["a"][i], "f16"), M, K, w["lda"], False)
+        b = og.as_logical(og.decode(w["b"][i], "f16"), K, N, w["ldb"], True)
+        assert_close_f16(got, decode_out(og.gemm(a, b, "f16"), "f16"))
 
 
 # ------------------------------------------------- CTA-pair (256-row) ------
@@ -257,17 +295,35 @@ def test_pair_batched():
 @pytest.mark.parametrize("mnk", [(256, 256, 512), (300, 500, 1000), (1024, 1024, 2048), (17, 260, 4096)])
 @pytest.mark.parametrize("acol,bcol", [(False, True), (True, False), (False, False), (True, True)])
 @pytest.mark.parametrize("splits", [2, 4])
-def test_splitk_shapes_layouts(mnk, acol, bcol, splits):
+@pytest.mark.parametrize("tn", [256, 128])
+def test_splitk_shapes_layouts(mnk, acol, bcol, splits, tn):
     M, N, K = mnk
     up8 = lambda x: -(-x // 8) * 8
     w = wl.dense16(M, N, K, "f16", a_col_major=acol, b_col_major=bcol, seed=M + N + K + splits,
                    lda=up8(M if acol else K), ldb=up8(K if bcol else N), dist="normal")
-    lm, ln = -(-M // 256), -(-N // 256)
+    lm, ln = -(-M // 256), -(-N // tn)
     trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
-    got = run_dense(w, "f16", bst.sched(3, 1, split_k=splits, trace=trace))
+    got = run_dense(w, "f16", bst.sched(3, 1, split_k=splits, tile_n=tn, trace=trace))
     assert_close_f16(got, oracle_dense(w, "f16"))
     tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
-    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 256, 256, 3, 1), dtype=np.uint32))
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 256, tn, 3, 1), dtype=np.uint32))
+
+
+@pytest.mark.parametrize("tn,splits", [(256, 2), (128, 2), (128, 4)])
+@pytest.mark.parametrize("out,ldc_pad", [("f16", 1), ("bf16", 2), ("f16", 4), ("f32", 1), ("f32", 2)])
+def test_splitk_output_pitches(tn, splits, out, ldc_pad):
+    M, N, K = 300, 270, 1024
+    w = wl.dense16(M, N, K, "bf16", b_col_major=True, seed=tn + splits, dist="normal")
+    got = run_dense(w, out, bst.sched(2, 0, split_k=splits, tile_n=tn), ldc=N + ldc_pad)
+    assert_close_f16(got, oracle_dense(w, out))
+
+
+def test_splitk_auto_choice_matches_oracle():
+    # the headline shape with the automatic split choice (and the timeline debug output)
+    w = wl.fp16_square()
+    tl = torch.zeros(160 * 64, dtype=torch.int64, device="cuda")
+    got = run_dense(w, "f16", bst.sched(1, 1, timeline=tl))
+    assert_close_f16(got, oracle_dense(w, "f16"))
 
 
 def test_splitk_more_splits_than_kblocks_and_f32_out():

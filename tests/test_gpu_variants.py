@@ -133,6 +133,24 @@ def test_mxfp8_unit_scales_and_single_block():
     assert_close_fro(got, ref, 1e-5)
 
 
+@pytest.mark.parametrize("tn", [128, 256])
+def test_mxfp8_scale_placement_tma_path(tn):
+    """K = 1024 (scale rows of 32 bytes: the scale factors arrive by TMA in
+    16-byte groups of 4 k-blocks): single bumped codes in different groups and
+    sub-blocks reach exactly their own row / column and 32-element block."""
+    M, N, K = 300, 300, 1024
+    w = wl.mxfp8(M, N, K, seed=4)
+    w["sa"][:] = 127
+    w["sb"][:] = 127
+    w["sa"][37, 13] = 130          # x8 on row 37, K 416..447 (k-block 3, group 0)
+    w["sa"][160, 20] = 125         # /4 on row 160, K 640..671 (k-block 5, group 1)
+    w["sb"][200, 30] = 124         # /8 on column 200, K 960..991 (k-block 7, group 1)
+    w["sb"][299, 1] = 129          # x4 on the last column, K 32..63
+    got = run_mx(w, bst.sched(1, 0, tile_n=tn), out="f32")
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"], "f32"), "f32")
+    assert_close_fro(got, ref, 1e-5)
+
+
 def test_mxfp8_full_workload():
     """e4m3 1024x2048x4096 with E8M0 scales 2^U{-4..4} per 32 K."""
     w = wl.mxfp8()

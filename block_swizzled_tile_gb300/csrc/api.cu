@@ -433,6 +433,46 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     return cuda_status(launch_dense(p, bn, grid, stream));
 }
 
+// MXFP8 tile width and split-K.  One thread issues every MMA of a CTA, and
+// the issue cost per k-block (about 0.42 us at 128 columns, 0.45 us at 256)
+// barely depends on the width, so wide tiles win whenever they can fill the
+// GPU; split-K over clusters of S CTAs (one tile per cluster) lets 128 x 256
+// tiles do so.  Cost = waves x k-blocks per CTA x per-k-block time, plus about
+// 7 us for a split (the exchange and finish of the partials through
+// distributed shared memory, and the cluster launch, measured on a 128 x 256
+// tile).  splits = 0 on return: a forced split this problem cannot take.
+bst_status choose_mx(const Sched& sch, uint64_t loops_m, uint64_t N, uint32_t num_kb, uint32_t sms, uint32_t& bn,
+                     uint32_t& splits) {
+    auto tiles_of = [&](uint32_t w) { return loops_m * ((N + w - 1) / w); };
+    auto split_ok = [&](uint32_t w, uint32_t s) {
+        uint32_t resident = 0;
+        if (mxf8_split_resident(w, s, &resident) != cudaSuccess) { cudaGetLastError(); return false; }
+        return resident > 0 && tiles_of(w) <= resident && tiles_of(w) * s <= sms;
+    };
+    if (sch.split_k >= 2) {
+        bn = sch.tile_n ? sch.tile_n : (sch.split_k == 2 ? 256u : 128u);
+        splits = sch.split_k;
+        uint32_t resident = 0;
+        if (mxf8_split_resident(bn, splits, &resident) != cudaSuccess || resident == 0) {
+            cudaGetLastError();
+            return BST_ERR_UNSUPPORTED;
+        }
+        return BST_OK;
+    }
+    double best = 1e300;
+    for (uint32_t w : {128u, 256u}) {
+        if (sch.tile_n && sch.tile_n != w) continue;
+        for (uint32_t s : {1u, 2u, 4u}) {
+            if (s > 1 && (sch.split_k == 1 || num_kb < 4 * s || !split_ok(w, s))) continue;
+            const uint64_t ctas = s > 1 ? tiles_of(w) * s : tiles_of(w);
+            const double waves = static_cast<double>((ctas + sms - 1) / sms);
+            const double cost = waves * ((num_kb + s - 1) / s) * (w == 256 ? 0.45 : 0.42) + (s > 1 ? 7.0 : 0.0);
+            if (cost < best * 0.999) { best = cost; bn = w; splits = s; }
+        }
+    }
+    return bn ? BST_OK : BST_ERR_UNSUPPORTED;
+}
+
 bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout la, int64_t lda, const void* B,
                     bst_layout lb, int64_t ldb, void* C, bst_dtype ct, int64_t ldc, const uint8_t* sfa,
                     const uint8_t* sfb, const bst_sched* sched_in, void* stream_v) {
@@ -460,9 +500,11 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     const uint32_t csize = dtype_bytes(ct);
     if (K == 0) return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, M, N, 1, csize, dev.sms, stream));
     const uint64_t loops_m = (M + kBM - 1) / kBM;
-    const uint32_t bn = sch.tile_n ? sch.tile_n : choose_bn(loops_m, N, dev.sms, false);
+    const uint32_t num_kb = static_cast<uint32_t>(K / 128);
+    uint32_t bn = 0, splits = 1;
+    if (bst_status s = choose_mx(sch, loops_m, N, num_kb, dev.sms, bn, splits)) return s;
     const uint64_t tiles = loops_m * ((N + bn - 1) / bn);
-    if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    if (tiles >= (1ull << 31)) return BST_ERR_INVALID_ARG;
     if (smem_mxf8(bn) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     GemmParams p;
@@ -512,6 +554,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
     set_prefetch(p.g, a, b, sfa, static_cast<uint64_t>(M) * (K / 32), sfb, static_cast<uint64_t>(N) * (K / 32));
+    if (splits > 1) return cuda_status(launch_mxf8_split(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_mxf8(p, bn, grid, stream));

@@ -127,7 +127,7 @@ struct GemmParams {
     GemmArgs g;
 };
 
-template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND>
+template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND, uint32_t SPLIT = 1>
 struct GemmLayout {
     static constexpr uint32_t kABytes = kBM * kLine;
     static constexpr uint32_t kBBytes = BN * kLine;
@@ -143,7 +143,7 @@ struct GemmLayout {
     static constexpr uint32_t kRawOff = (kSfOff + STAGES * kSfStageBytes + 1023) & ~1023u;
     static constexpr uint32_t kEpiOff = kRawOff + 2 * kRawSlotBytes;       // 4 epilogue warps x 4 KB staging
     static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2;     // ..., drain, raw_full[2]
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2 + 4; // ..., drain, raw_full[2], recv[4]
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
     // TMEM: ACC accumulators of BN fp32 columns, then (MXFP8) per stage 4
@@ -154,6 +154,16 @@ struct GemmLayout {
         kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM budget");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+    // split-K over a cluster of SPLIT CTAs: after the main loop the ring holds
+    // the receive slots, then the send staging, of the column-ownership
+    // reduction (4 warps x (SPLIT-1) slots of 32 rows x BN/SPLIT fp32 each)
+    static constexpr uint32_t kSplitW = BN / SPLIT;
+    static constexpr uint32_t kSplitSlotBytes = 32 * kSplitW * 4;
+    static constexpr uint32_t kSplitSlots = 4 * (SPLIT - 1);
+    static constexpr uint32_t kSplitSendOff = kSplitSlots * kSplitSlotBytes;
+    static_assert(SPLIT == 1 || (ACC == 1 && kSplitW % 32 == 0 &&
+                                 2 * kSplitSlots * kSplitSlotBytes <= STAGES * kStageBytes),
+                  "split-K slots reuse the ring");
     static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
 };
 
@@ -485,9 +495,13 @@ __device__ __forceinline__ void store_chunk_coalesced(uint8_t* stage, uint32_t o
     }
 }
 
-template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND, uint32_t EPI>
+// SPLIT > 1: split-K over clusters of SPLIT CTAs, one output tile per cluster
+// (cluster rank = split); the partial tiles are summed through distributed
+// shared memory by column ownership (see the end of the kernel).
+template <uint32_t BN, uint32_t STAGES, uint32_t ACC, uint32_t KIND, uint32_t EPI, uint32_t SPLIT = 1>
 __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __grid_constant__ GemmParams prm) {
-    using Lay = GemmLayout<BN, STAGES, ACC, KIND>;
+    using Lay = GemmLayout<BN, STAGES, ACC, KIND, SPLIT>;
+    static_assert(SPLIT == 1 || (EPI == kEpiStore && (SPLIT == 2 || SPLIT == 4)), "split-K: plain stores, 2 or 4");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
     static_assert(EPI == kEpiStore || BN == 128, "dequant epilogue keeps 128 int32 per thread");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -512,6 +526,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     uint64_t* tempty = bars + 2 * STAGES + ACC;
     uint64_t* drain = bars + 2 * STAGES + 2 * ACC;
     uint64_t* raw_full = bars + 2 * STAGES + 2 * ACC + 1;
+    uint64_t* recv = bars + 2 * STAGES + 2 * ACC + 3;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     uint32_t* tmem_holder = misc;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -542,9 +557,13 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         mbar_init(drain, 1);
         mbar_init(&raw_full[0], 1);
         mbar_init(&raw_full[1], 1);
+        for (uint32_t o = 0; o < 4; ++o) mbar_init(&recv[o], 1);
         *abort_flag = 0;
         *tiles_smem = prm.g.total_tiles;
         fence_barrier_init();
+        // split-K: each epilogue warp's receive barrier expects SPLIT-1 partials
+        if (SPLIT > 1)
+            for (uint32_t o = 0; o < 4; ++o) mbar_arrive_expect_tx(&recv[o], (SPLIT - 1) * Lay::kSplitSlotBytes);
     }
     if (warp == 0 && lane == 0) {
         if (a_tma) prefetch_tmap(&prm.tmap_a);
@@ -566,6 +585,21 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     const uint32_t total_tiles = *tiles_smem;
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     if (tl && threadIdx.x == 0) { tl[0] = globaltimer_ns(); tl[55] = t_entry; }
+    // tiles of this CTA and its k-block range: persistent stride, or (split-K)
+    // the cluster's one tile and this split's share of K, in whole 4-k-block
+    // groups when the MXFP8 scale factors come by TMA
+    const uint32_t split = SPLIT > 1 ? cluster_rank() : 0u;
+    const uint32_t t_first = SPLIT > 1 ? cluster_id_x() : blockIdx.x;
+    const uint32_t t_step = SPLIT > 1 ? total_tiles : gridDim.x;
+    uint32_t kb_lo = 0, kb_hi = num_kb;
+    if (SPLIT > 1) {
+        const uint32_t gran = (KIND == kKindMXF8 && prm.g.sf_tma) ? 4u : 1u;
+        const uint32_t units = (num_kb + gran - 1) / gran;
+        kb_lo = min(num_kb, (split * units / SPLIT) * gran);
+        kb_hi = min(num_kb, ((split + 1) * units / SPLIT) * gran);
+    }
+    const bool has_k = kb_hi > kb_lo;
+    bool acc_ok = true;                                  // split-K: this CTA's partial is complete
 
     constexpr uint32_t kBWarp = b_warp_for<KIND>();
     if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp) || (warp == kBWarp && lane == 0 && !lanes_copy_ops)) {
@@ -600,7 +634,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             const bool simple = !a_mn && !b_mn && !a_rank3 && !b_rank3;
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            for (uint32_t t = t_first; ok && t < total_tiles; t += t_step) {
                 if (tl && is_a && issued == 0) tl[56] = globaltimer_ns();
                 const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
                 const uint32_t n0 = ti.n * BN;
@@ -611,7 +645,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     const CUtensorMap* map = is_a ? &prm.tmap_a : &prm.tmap_b;
                     const uint32_t dst_off = is_a ? 0u : Lay::kABytes;
                     const int32_t row = is_a ? static_cast<int32_t>(ti.row0) : static_cast<int32_t>(n0);
-                    for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                    for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                         uint8_t* st = smem + stage * Lay::kStageBytes;
                         const int32_t k0 = static_cast<int32_t>(kb * bk_elems);
@@ -623,7 +657,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     }
                     continue;
                 }
-                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     const uint32_t k0 = kb * bk_elems;
@@ -661,10 +695,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             uint32_t stage = 0, phase = 0;
             uint32_t rg = 0, cg = 0;                     // raw groups issued / consumed (slot = n % 2)
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            for (uint32_t t = t_first; ok && t < total_tiles; t += t_step) {
                 const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
                 const int32_t n0 = static_cast<int32_t>(ti.n * BN);
-                const uint32_t ngroups = (num_kb + 3) / 4;
+                const uint32_t ngroups = (kb_hi + 3) / 4;      // groups are absolute: kb / 4
                 auto issue = [&](uint32_t g) {
                     uint8_t* slot = smem + Lay::kRawOff + (rg & 1u) * raw_bytes;
                     fence_proxy_async_smem();            // earlier reads of this slot before the new writes
@@ -673,8 +707,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     tma_load_2d(slot + kRawA, &prm.tmap_sfb, &raw_full[rg & 1u], static_cast<int32_t>(g * 16), n0);
                     ++rg;
                 };
-                if (lane == 0) issue(0);
-                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                if (lane == 0 && has_k) issue(kb_lo / 4);
+                for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     const uint32_t j = kb & 3u;
                     if (j == 0) {
                         if (lane == 0 && kb / 4 + 1 < ngroups) issue(kb / 4 + 1);
@@ -699,7 +733,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     fence_proxy_async_smem();            // generic writes -> tcgen05.cp's reads
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&full[stage]);
-                    if (j == 3 || kb + 1 == num_kb) ++cg;
+                    if (j == 3 || kb + 1 == kb_hi) ++cg;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -713,11 +747,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         } else if (warp_copies) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            for (uint32_t t = t_first; ok && t < total_tiles; t += t_step) {
                 const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
                 const uint32_t n0 = ti.n * BN;
                 const int32_t zc = static_cast<int32_t>(ti.tag);
-                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     uint8_t* sb_s = sa_s + Lay::kABytes;
@@ -790,12 +824,12 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const uint32_t sf_tma = prm.g.sf_tma;
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
         bool ok = true, any_mma = false;
-        const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
+        const uint32_t nchunks = SPLIT > 1 ? (has_k ? 1u : 0u) : (num_kb + chunk_kb - 1) / chunk_kb;
         // one thread issues every MMA (a single-lane loop, see the producer)
-        for (uint32_t t = blockIdx.x; lane == 0 && ok && t < total_tiles; t += gridDim.x) {
+        for (uint32_t t = t_first; lane == 0 && ok && t < total_tiles; t += t_step) {
             for (uint32_t c = 0; ok && c < nchunks; ++c) {
-                const uint32_t kb_begin = c * chunk_kb;
-                const uint32_t kb_end = min(num_kb, kb_begin + chunk_kb);
+                const uint32_t kb_begin = SPLIT > 1 ? kb_lo : c * chunk_kb;
+                const uint32_t kb_end = SPLIT > 1 ? kb_hi : min(num_kb, kb_begin + chunk_kb);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -846,6 +880,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             umma_commit(drain);
             mbar_wait_drain(drain, 0, ctl.timeout_ns);
         }
+    } else if (SPLIT > 1 && warp >= 2 && warp < 6) {
+        // ------------------------------------- split-K epilogue, part 1 --
+        // this CTA's partial is final once its MMAs are done; the exchange
+        // follows the cluster barrier below
+        if (has_k && t_first < total_tiles) acc_ok = warp_wait(&tfull[0], 0, ctl, 4);
     } else if (warp >= 2 && warp < 6) {
         // ----------------------------------------------------- epilogue --
         prefetch_operands(prm.g, threadIdx.x - 64, 128);
@@ -864,7 +903,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
         uint32_t acc = 0, acc_phase = 0, ep_tile = 0;
         bool ok = true;
-        for (uint32_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        for (uint32_t t = t_first; ok && t < total_tiles; t += t_step) {
             const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
             if (trace && warp == 2 && lane == 0) {
                 if (t < trace_cap) {
@@ -945,6 +984,104 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         }
     }
 
+    if (SPLIT > 1) {
+        // ------------------------------------- split-K epilogue, part 2 --
+        // Every CTA of the cluster is past its main loop (its ring is idle)
+        // once this barrier completes.  Split g finishes columns [g*W,
+        // (g+1)*W) of the tile.  Every epilogue warp stages, for each other
+        // split g, its 32 rows of g's columns in its own ring (row per lane,
+        // 16-byte granules XOR-swizzled by row) and bulk-copies them into a
+        // receive slot of CTA g, completing on that CTA's receive barrier of
+        // the same warp; it then adds the SPLIT-1 partials it received to its
+        // own rows of its own columns, rounds once and stores.
+        tc_fence_before();
+        __syncthreads();
+        cluster_sync();
+        tc_fence_after();
+        if (warp >= 2 && warp < 6 && t_first < total_tiles) {
+            constexpr uint32_t W = Lay::kSplitW;
+            constexpr uint32_t kSlot = Lay::kSplitSlotBytes;
+            const uint32_t q = warp & 3u;
+            const uint32_t taddr = tmem_base + ((q * 32) << 16);
+            const bool own_valid = acc_ok && has_k;      // else this split's partial counts as zero
+            uint32_t gi = 0;
+#pragma unroll 1
+            for (uint32_t g = 0; g < SPLIT; ++g) {
+                if (g == split) continue;
+                uint8_t* stage_rows = smem + Lay::kSplitSendOff + (q * (SPLIT - 1) + gi) * kSlot;
+                uint8_t* my_row = stage_rows + lane * (W * 4);
+#pragma unroll 1
+                for (uint32_t cc = 0; cc < W / 32; ++cc) {
+                    uint32_t v[32];
+                    if (own_valid) tmem_ld_32x32b_x32(taddr + g * W + cc * 32, v);
+                    else {
+#pragma unroll
+                        for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
+                    }
+#pragma unroll
+                    for (uint32_t gg = 0; gg < 8; ++gg) {
+                        const uint32_t granule = (cc * 8 + gg) ^ (lane & 7u);
+                        *reinterpret_cast<uint4*>(my_row + granule * 16) =
+                            make_uint4(v[4 * gg], v[4 * gg + 1], v[4 * gg + 2], v[4 * gg + 3]);
+                    }
+                }
+                fence_proxy_async_smem();                // generic writes -> the bulk copy's reads
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t slot = q * (SPLIT - 1) + (split < g ? split : split - 1);
+                    const uint32_t dst = map_to_cta(smem_u32(smem + slot * kSlot), g);
+                    const uint32_t bar = map_to_cta(smem_u32(&recv[q]), g);
+                    bulk_copy_to_cluster(dst, stage_rows, kSlot, bar);
+                    bulk_commit_group();
+                }
+                ++gi;
+            }
+            const bool got = warp_wait(&recv[q], 0, ctl, 5);
+            const TileInfo ti = tile_info(sa, t_first, kBM, BN, gt);
+            const uint8_t* slots = smem + q * (SPLIT - 1) * kSlot + lane * (W * 4);
+            const uint32_t rows_valid = ti.m_act > q * 32 ? min(32u, ti.m_act - q * 32) : 0u;
+            const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
+            const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
+            const int64_t ldc = prm.g.ldc;
+            uint8_t* const cwarp = prm.g.C + static_cast<int64_t>(ti.row0 + q * 32) * ldc * csize;
+            uint8_t* const epi_stage = smem + Lay::kEpiOff + q * kEpiWarpBytes;
+#pragma unroll 1
+            for (uint32_t cc = 0; cc < W / 32; ++cc) {
+                uint32_t v[32];
+                if (own_valid) tmem_ld_32x32b_x32(taddr + split * W + cc * 32, v);
+                else {
+#pragma unroll
+                    for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
+                }
+                if (got) {
+#pragma unroll
+                    for (uint32_t si = 0; si < SPLIT - 1; ++si) {
+#pragma unroll
+                        for (uint32_t gg = 0; gg < 8; ++gg) {
+                            const uint32_t granule = (cc * 8 + gg) ^ (lane & 7u);
+                            const uint4 x = *reinterpret_cast<const uint4*>(slots + si * kSlot + granule * 16);
+                            v[4 * gg] = __float_as_uint(__uint_as_float(v[4 * gg]) + __uint_as_float(x.x));
+                            v[4 * gg + 1] = __float_as_uint(__uint_as_float(v[4 * gg + 1]) + __uint_as_float(x.y));
+                            v[4 * gg + 2] = __float_as_uint(__uint_as_float(v[4 * gg + 2]) + __uint_as_float(x.z));
+                            v[4 * gg + 3] = __float_as_uint(__uint_as_float(v[4 * gg + 3]) + __uint_as_float(x.w));
+                        }
+                    }
+                }
+                const uint32_t col = split * W + cc * 32;    // column within the tile
+                if (rows_valid && col < ti.n_act)
+                    store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(ti.n * BN + col) * csize,
+                                          ldc * csize, rows_valid, min(32u, ti.n_act - col), v, lane);
+            }
+            if (lane == 0) bulk_wait_read_all();         // the ring may not be left while being read
+            if (prm.g.trace && split == 0 && q == 0 && lane == 0 && t_first < prm.g.trace_cap) {
+                uint32_t* tr = prm.g.trace + static_cast<uint64_t>(t_first) * 5;
+                tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        cluster_sync();                                  // no CTA leaves while a peer may still touch it
+    }
     if (tl && lane == 0 && warp <= 2) tl[48 + warp] = globaltimer_ns();
     tc_fence_before();
     __syncthreads();

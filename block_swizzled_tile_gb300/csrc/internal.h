@@ -66,6 +66,10 @@ inline cudaError_t launch_gemm(Kern kern, const GemmParams& p, uint32_t grid, ui
 // setting included); `grid` CTAs of kNumThreads threads on `stream`.
 cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
 cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
+// MXFP8 split-K over clusters of `splits` CTAs (tile 128 x bn), one tile per cluster
+cudaError_t launch_mxf8_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream);
+// clusters the MXFP8 split-K kernel keeps resident at once (0: no such shape)
+cudaError_t mxf8_split_resident(uint32_t bn, uint32_t splits, uint32_t* out);
 cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stream);
 // CTA-pair kernel: launches clusters of 2, at most max_pairs of them (and no
 // more than fit on the device at once)

@@ -151,6 +151,36 @@ def test_mxfp8_scale_placement_tma_path(tn):
     assert_close_fro(got, ref, 1e-5)
 
 
+@pytest.mark.parametrize("tn,splits", [(256, 2), (128, 2), (128, 4)])
+@pytest.mark.parametrize("mnk", [(200, 300, 1024), (129, 257, 512), (300, 520, 384), (1024, 512, 4096)])
+def test_mxfp8_split_k(tn, splits, mnk):
+    """Split-K over clusters of 2 or 4 CTAs (one 128 x tn tile per cluster,
+    partials summed in distributed shared memory).  K = 1024 and 512 take the
+    TMA scale path in 4-k-block groups, so some splits get no k-blocks; K = 384
+    takes the row-by-row scale path."""
+    M, N, K = mnk
+    w = wl.mxfp8(M, N, K, seed=M + tn + splits)
+    lm, ln = -(-M // 128), -(-N // tn)
+    trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
+    got = run_mx(w, bst.sched(2, 1, tile_n=tn, split_k=splits, trace=trace))
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"]), "bf16")
+    assert_close_fro(got, ref, FRO_MX)
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, tn, 2, 1), dtype=np.uint32))
+
+
+def test_mxfp8_split_k_f32_out_unit_scales():
+    M, N, K = 256, 256, 2048
+    w = wl.mxfp8(M, N, K, seed=11)
+    w["sa"][:] = 127
+    w["sb"][:] = 127
+    w["sa"][5, 60] = 129            # second half of K: the other split
+    w["sb"][250, 3] = 126           # first half of K
+    got = run_mx(w, bst.sched(1, 0, tile_n=256, split_k=2), out="f32")
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"], "f32"), "f32")
+    assert_close_fro(got, ref, 1e-5)
+
+
 def test_mxfp8_full_workload():
     """e4m3 1024x2048x4096 with E8M0 scales 2^U{-4..4} per 32 K."""
     w = wl.mxfp8()

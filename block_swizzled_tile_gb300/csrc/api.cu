@@ -683,7 +683,10 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     if (b_layout != BST_ROW_MAJOR && b_layout != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
     Sched sch;
     if (bst_status s = read_sched(sched_in, sch)) return s;
-    if ((sch.tile_n != 0 && sch.tile_n != 128) || sch.tile_m == 256) return BST_ERR_UNSUPPORTED;
+    // tiles: 256 x 256 CTA pairs (the default) or 128 x 128 single CTAs
+    if (sch.tile_m != 0 && sch.tile_m != 128 && sch.tile_m != 256) return BST_ERR_UNSUPPORTED;
+    if (sch.tile_n != 0 && sch.tile_n != 128 && sch.tile_n != 256) return BST_ERR_UNSUPPORTED;
+    if ((sch.tile_m == 256 && sch.tile_n == 128) || (sch.tile_m == 128 && sch.tile_n == 256)) return BST_ERR_UNSUPPORTED;
     if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
     if (lda < 1 || lda < K) return BST_ERR_INVALID_ARG;
     if (ldb < 1 || ldb < (b_layout == BST_COL_MAJOR ? K : N)) return BST_ERR_INVALID_ARG;
@@ -707,10 +710,12 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     uint16_t* wb = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + round256(static_cast<size_t>(M) * kp * 2));
     const bool b_kmajor = b_layout == BST_COL_MAJOR;   // stored [N, K]
     const int64_t ldwb = b_kmajor ? kp : np;
-    const uint64_t loops_m = (M + kBM - 1) / kBM;
-    const uint64_t tiles = loops_m * ((N + 127) / 128);
+    const bool pair = sch.tile_m == 256 || sch.tile_n == 256 ||
+                      (sch.tile_m == 0 && sch.tile_n == 0 && M > kBM && N > 128);
+    const uint32_t tm = pair ? 2 * kBM : kBM, tn = pair ? 256u : 128u;
+    const uint64_t tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
     if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
-    if (smem_dequant() > dev.max_smem) return BST_ERR_UNSUPPORTED;
+    if ((pair ? smem_pair_dequant() : smem_dequant()) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     cudaError_t e = launch_widen_s8_bf16(A, lda, wa, kp, M, K, dev.sms, stream);
     if (e == cudaSuccess)
@@ -748,6 +753,9 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    if (pair)
+        return cuda_status(launch_pair_dequant(p, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
+                                               stream));
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_dequant(p, grid, stream));
 }

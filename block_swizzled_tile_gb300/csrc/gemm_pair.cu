@@ -4,15 +4,16 @@
 
 namespace bst {
 
-template <uint32_t BN, uint32_t STAGES>
+template <uint32_t BN, uint32_t STAGES, uint32_t EPI = kEpiStore>
 static cudaError_t launch_pair_one(const GemmParams& p, uint32_t max_pairs, cudaStream_t stream) {
-    using Lay = PairLayout<BN, STAGES>;
+    using Lay = PairLayout<BN, STAGES, EPI>;
+    static_assert(Lay::smem_bytes(kMaxGroups) <= 232448, "shared memory per CTA");
     static std::atomic<uint64_t> attr_done{0};
-    auto kern = gemm_pair_kernel<BN, STAGES>;
+    auto kern = gemm_pair_kernel<BN, STAGES, EPI>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(kMaxGroups), attr_done);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kPairThreads);
+    cfg.blockDim = dim3(pair_threads<EPI>());
     cfg.dynamicSmemBytes = Lay::smem_bytes(p.g.mode == kModeGrouped ? p.g.G : 0);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -135,6 +136,12 @@ uint32_t smem_splitk(uint32_t bn, uint32_t splits) {
     if (bn == 128 && splits == 4) return SplitLaunch<128, 4>::Lay::smem_bytes();
     return 0;
 }
+
+cudaError_t launch_pair_dequant(const GemmParams& p, uint32_t max_pairs, cudaStream_t stream) {
+    return launch_pair_one<256, kPairDequantStages, kEpiDequant>(p, max_pairs, stream);
+}
+
+uint32_t smem_pair_dequant() { return PairLayout<256, kPairDequantStages, kEpiDequant>::smem_bytes(0); }
 
 uint32_t smem_pair(uint32_t bn, uint32_t groups) {
     switch (bn) {

@@ -36,27 +36,39 @@ namespace bst {
 // issues a TMA about every 0.1-0.15 us, so A and B get a thread each).
 constexpr uint32_t kPairThreads = 224;
 constexpr uint32_t kPairBWarp = 6;
+// The int8 per-token-dequant variant keeps 128 int32 running sums per thread,
+// so its 256-column tiles take two epilogue warps per TMEM lane quarter:
+// warps 2-5 finish columns 0-127, warps 7-10 columns 128-255.
+template <uint32_t EPI>
+constexpr uint32_t pair_threads() { return EPI == kEpiDequant ? 352u : kPairThreads; }
+template <uint32_t EPI>
+constexpr uint32_t pair_epi_warps() { return EPI == kEpiDequant ? 8u : 4u; }
 
-template <uint32_t BN, uint32_t STAGES>
+// Dequant: one fp32 accumulator (the current K-chunk) in TMEM columns
+// [0, BN) and the exact int32 running sums in [BN, 2*BN); otherwise two fp32
+// accumulators, so the epilogue of one tile overlaps the MMAs of the next.
+template <uint32_t BN, uint32_t STAGES, uint32_t EPI = kEpiStore>
 struct PairLayout {
-    static constexpr uint32_t kACC = 2;
+    static constexpr uint32_t EPI_WARPS = pair_epi_warps<EPI>();
+    static constexpr uint32_t kACC = EPI == kEpiDequant ? 1 : 2;
     static constexpr uint32_t kABytes = kBM * kLine;            // 128 A rows per CTA
     static constexpr uint32_t kBBytes = (BN / 2) * kLine;       // BN/2 B rows per CTA
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kEpiOff = STAGES * kStageBytes;             // 4 epilogue warps x 4 KB staging
-    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
+    static constexpr uint32_t kEpiOff = STAGES * kStageBytes;             // epilogue warps x 4 KB staging
+    static constexpr uint32_t kBarOff = kEpiOff + EPI_WARPS * kEpiWarpBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 * kACC + 1;
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
-    static constexpr uint32_t kTmemCols = kACC * BN <= 256 ? 256 : 512;
-    static_assert(kACC * BN <= 512, "TMEM budget");
+    static constexpr uint32_t kTmemCols = EPI == kEpiDequant ? 512 : (kACC * BN <= 256 ? 256 : 512);
+    static_assert(kACC * BN <= 512 && (EPI == kEpiStore || BN == 256), "TMEM budget");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
     static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
 };
 
-template <uint32_t BN, uint32_t STAGES>
-__global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams prm) {
-    using Lay = PairLayout<BN, STAGES>;
+template <uint32_t BN, uint32_t STAGES, uint32_t EPI = kEpiStore>
+__global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const __grid_constant__ GemmParams prm) {
+    using Lay = PairLayout<BN, STAGES, EPI>;
+    static_assert(EPI == kEpiStore || BN == 256, "dequant: 256-column tiles, 128 columns per epilogue warp");
     constexpr uint32_t ACC = Lay::kACC;
     constexpr uint32_t TM = 2 * kBM;
     constexpr uint32_t BH = BN / 2;                  // B columns held by each CTA
@@ -101,7 +113,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         }
         for (uint32_t a = 0; a < ACC; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 8);
+            mbar_init(&tempty[a], 2 * pair_epi_warps<EPI>());   // one arrival per epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -199,11 +211,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             const uint32_t smem_base = smem_u32(smem);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
             bool ok = true, any_mma = false;
+            const uint32_t chunk_kb = prm.g.chunk_kb;
+            const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
             for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t += nclusters) {
+              // K-chunks (one for plain stores): each fills one accumulator
+              for (uint32_t c = 0; ok && c < nchunks; ++c) {
+                const uint32_t kb_begin = c * chunk_kb;
+                const uint32_t kb_end = min(num_kb, kb_begin + chunk_kb);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (uint32_t kb = 0; kb < num_kb; ++kb) {
+                for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
                     {
@@ -214,7 +232,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 #pragma unroll
                         for (uint32_t kk = 0; kk < 4; ++kk)
                             umma_f16_pair(d_tmem, adesc + ((kk * a_step) >> 4), bdesc + ((kk * b_step) >> 4), idesc,
-                                          (kb > 0 || kk > 0) ? 1u : 0u);
+                                          (kb > kb_begin || kk > 0) ? 1u : 0u);
                         umma_commit_pair_mc(&empty[stage], 0x3);
                     }
                     ++mma_kb;
@@ -224,6 +242,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (!ok) break;
                 umma_commit_pair_mc(&tfull[acc], 0x3);
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+              }
             }
             if (lane == 0 && !ok && any_mma) {
                 // every tcgen05 op issued so far must finish before TMEM is freed
@@ -231,19 +250,27 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 mbar_wait_drain(drain, 0, ctl.timeout_ns);
             }
         }
-    } else {
+    } else if ((warp >= 2 && warp < 6) || (EPI == kEpiDequant && warp >= 7 && warp < 11)) {
         // ---------------------------------------------- epilogue (both) --
-        prefetch_operands(prm.g, threadIdx.x - 64, 128);
+        const bool hi = warp >= 7;                       // dequant: the upper 128 columns
+        if (!hi) prefetch_operands(prm.g, threadIdx.x - 64, 128);
+        constexpr uint32_t kCols = EPI == kEpiDequant ? BN / 2 : BN;   // columns this warp finishes
+        const uint32_t col_off = hi ? BN / 2 : 0u;
         const uint32_t q = warp & 3u;                    // TMEM lane quarter of this warp
         const uint32_t wrow = rank * kBM + q * 32;       // first row of this warp in the 256-row tile
-        const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
-        uint8_t* const epi_stage = smem + Lay::kEpiOff + q * kEpiWarpBytes;
+        const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec, acc_vec = prm.g.acc_vec;
+        uint8_t* const epi_stage = smem + Lay::kEpiOff + (hi ? 4u + q : q) * kEpiWarpBytes;
         uint8_t* const C = prm.g.C;
         const int64_t ldc = prm.g.ldc, c_bs = prm.g.c_batch_stride;
+        const float* scale_a = prm.g.scale_a;
+        const float* scale_b = prm.g.scale_b;
+        int32_t* const acc_out = prm.g.acc_out;
         uint32_t* const trace = prm.g.trace;
         const uint32_t trace_cap = prm.g.trace_cap;
         const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
         const uint32_t tempty_leader = map_to_cta(smem_u32(tempty), 0);
+        const uint32_t chunk_kb = prm.g.chunk_kb;
+        const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
         uint32_t acc = 0, acc_phase = 0, ep_tile = 0;
         bool ok = true;
         for (uint32_t t = cid; ok && t < total_tiles; t += nclusters) {
@@ -259,25 +286,72 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             const uint32_t rows_valid = ti.m_act > wrow ? min(32u, ti.m_act - wrow) : 0u;   // warp-uniform
             const int64_t cbase = mode == kModeBatched ? static_cast<int64_t>(ti.tag) * c_bs : 0;
             uint8_t* const cwarp = C + (cbase + static_cast<int64_t>(ti.row0 + wrow) * ldc) * csize;
-            const uint32_t n0 = ti.n * BN;
-            if (!warp_wait(&tfull[acc], acc_phase, ctl, 4)) { ok = false; break; }
-            tc_fence_after();
-            if (tl && warp == 2 && lane == 0 && ep_tile < 8) tl[32 + ep_tile] = globaltimer_ns();
-            const uint32_t taddr = tmem_base + ((q * 32) << 16) + acc * BN;
+            const uint32_t n0 = ti.n * BN + col_off;     // first output column of this warp
+            const uint32_t n_act = ti.n_act > col_off ? ti.n_act - col_off : 0u;
+            // dequant: exact int32 running sums of this warp's rows and columns
+            const uint32_t run_t = tmem_base + ((q * 32) << 16) + BN + col_off;
+            for (uint32_t c = 0; c < nchunks; ++c) {
+                if (!warp_wait(&tfull[acc], acc_phase, ctl, 4)) { ok = false; break; }
+                tc_fence_after();
+                if (tl && warp == 2 && lane == 0 && c == 0 && ep_tile < 8) tl[32 + ep_tile] = globaltimer_ns();
+                const uint32_t taddr = tmem_base + ((q * 32) << 16) + acc * BN + col_off;
+                if (EPI == kEpiStore) {
 #pragma unroll 1
-            for (uint32_t cc = 0; cc < BN / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + cc * 32, v);
-                if (rows_valid && cc * 32 < ti.n_act)
-                    store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(n0 + cc * 32) * csize,
-                                          ldc * csize, rows_valid, min(32u, ti.n_act - cc * 32), v, lane);
+                    for (uint32_t cc = 0; cc < kCols / 32; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(taddr + cc * 32, v);
+                        if (rows_valid && cc * 32 < n_act)
+                            store_chunk_coalesced(epi_stage, c_type, c_vec,
+                                                  cwarp + static_cast<int64_t>(n0 + cc * 32) * csize, ldc * csize,
+                                                  rows_valid, min(32u, n_act - cc * 32), v, lane);
+                    }
+                } else {
+                    // fold the chunk (an exact integer in fp32) into the running sums
+#pragma unroll 1
+                    for (uint32_t cc = 0; cc < kCols / 32; ++cc) {
+                        uint32_t v[32], r[32];
+                        tmem_ld_32x32b_x32(taddr + cc * 32, v);
+                        if (c > 0) tmem_ld_32x32b_x32(run_t + cc * 32, r);
+#pragma unroll
+                        for (uint32_t j = 0; j < 32; ++j)
+                            r[j] = static_cast<uint32_t>((c > 0 ? static_cast<int32_t>(r[j]) : 0) +
+                                                         __float2int_rn(__uint_as_float(v[j])));
+                        tmem_st_32x32b_x32(run_t + cc * 32, r);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+                if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+            if (!ok) break;
             if (tl && warp == 2 && lane == 0 && ep_tile < 8) tl[40 + ep_tile] = globaltimer_ns();
             ++ep_tile;
-            if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+            if (EPI == kEpiDequant && rows_valid) {
+                // acc * scale_a[row] * scale_b[col] in fp32, rounded once to bf16
+                tc_fence_after();
+                const uint32_t grow = ti.row0 + wrow + lane;
+                const float sa_row = lane < rows_valid ? scale_a[grow] : 0.f;
+#pragma unroll 1
+                for (uint32_t cc = 0; cc < kCols / 32; ++cc) {
+                    if (cc * 32 >= n_act) break;
+                    const uint32_t col0 = n0 + cc * 32;
+                    const uint32_t nv = min(32u, n_act - cc * 32);
+                    uint32_t r[32], v[32];
+                    tmem_ld_32x32b_x32(run_t + cc * 32, r);
+#pragma unroll
+                    for (uint32_t j = 0; j < 32; ++j) {
+                        const float sb = j < nv ? __ldg(scale_b + col0 + j) : 0.f;
+                        v[j] = __float_as_uint(static_cast<float>(static_cast<int32_t>(r[j])) * sa_row * sb);
+                    }
+                    store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(col0) * csize,
+                                          ldc * csize, rows_valid, nv, v, lane);
+                    if (acc_out) {
+                        uint8_t* awarp = reinterpret_cast<uint8_t*>(acc_out + static_cast<int64_t>(ti.row0 + wrow) * ldc + col0);
+                        store_chunk_coalesced(epi_stage, kOutS32, acc_vec, awarp, ldc * 4, rows_valid, nv, r, lane);
+                    }
+                }
+            }
         }
     }
 

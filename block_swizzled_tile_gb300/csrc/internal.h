@@ -76,6 +76,9 @@ cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stre
 cudaError_t launch_pair(const GemmParams& p, uint32_t bn, uint32_t max_pairs, cudaStream_t stream);
 // split-K CTA pairs on 256 x 256 tiles: one cluster of 2*splits CTAs per tile
 cudaError_t launch_pair_splitk(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream);
+// int8 per-token dequant on 256 x 256 CTA-pair tiles (bf16-widened operands)
+cudaError_t launch_pair_dequant(const GemmParams& p, uint32_t max_pairs, cudaStream_t stream);
+uint32_t smem_pair_dequant();
 // clusters of 2*splits CTAs the split-K kernel (tile 256 x bn) can keep resident at once
 cudaError_t splitk_resident_clusters(uint32_t bn, uint32_t splits, uint32_t* out);
 // dynamic shared memory of the split-K kernel (0: no such instantiation)
@@ -106,6 +109,7 @@ constexpr uint32_t kDenseStages64 = 8, kDenseStages128 = 6, kDenseStages256 = 4;
 constexpr uint32_t kMxStages128 = 6, kMxStages256 = 3;
 constexpr uint32_t kDequantStages = 6;
 constexpr uint32_t kPairStages128 = 8, kPairStages256 = 6;
+constexpr uint32_t kPairDequantStages = 5;
 constexpr uint32_t kDequantChunkK = 1024;  // K elements per exact fp32 chunk
 
 }  // namespace bst

@@ -216,12 +216,15 @@ def oracle_int8_rows(w, rows):
     return acc, decode_out(out, "bf16")
 
 
-@pytest.mark.parametrize("mnk", [(128, 128, 64), (300, 200, 2100), (1, 130, 1024), (257, 129, 40)])
+@pytest.mark.parametrize("mnk", [(128, 128, 64), (300, 200, 2100), (1, 130, 1024), (257, 129, 40), (520, 700, 3100)])
 @pytest.mark.parametrize("bcol", [True, False])
-def test_int8_small(mnk, bcol):
+@pytest.mark.parametrize("tile", [(0, 0), (128, 128), (256, 256)])
+def test_int8_small(mnk, bcol, tile):
+    """Single-CTA 128 x 128 and CTA-pair 256 x 256 tiles (K-chunks of 1024
+    folded into exact int32 sums: K = 2100 and 3100 take 3 and 4 chunks)."""
     M, N, K = mnk
     w = wl.int8_per_token(M, N, K, seed=M + K)
-    out, acc = run_int8(w, bcol, bst.sched(2, 1))
+    out, acc = run_int8(w, bcol, bst.sched(2, 1, tile_m=tile[0], tile_n=tile[1]))
     racc, rout = oracle_int8_rows(w, np.arange(M))
     assert np.array_equal(acc, racc)
     assert_close_fro(out, rout, FRO_MX)
@@ -237,10 +240,11 @@ def test_int8_extreme_sums_exact():
     w["a"][1::2] = -127
     w["b"][:] = 127
     w["b"][:, ::3] = -127
-    out, acc = run_int8(w, True, bst.sched(1, 0))
-    racc, rout = oracle_int8_rows(w, np.arange(M))
-    assert np.array_equal(acc, racc)
-    assert_close_fro(out, rout, FRO_MX)
+    for tile in [(128, 128), (256, 256)]:
+        out, acc = run_int8(w, True, bst.sched(1, 0, tile_m=tile[0], tile_n=tile[1]))
+        racc, rout = oracle_int8_rows(w, np.arange(M))
+        assert np.array_equal(acc, racc)
+        assert_close_fro(out, rout, FRO_MX)
 
 
 def test_int8_full_workload():

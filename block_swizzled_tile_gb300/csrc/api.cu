@@ -194,23 +194,6 @@ bst_status fill_operand(OperandDesc& d, CUtensorMap* map, const OperandSpec& o, 
     return encode(map, o, tile_mn, dt);
 }
 
-// Picks the tile width by a small cost model: tiles per SM wave times the
-// per-tile time, with narrow tiles derated because tcgen05 reads more
-// shared-memory bytes per flop for them.
-uint32_t choose_bn(uint64_t loops_m_total, uint64_t N, uint32_t sms, bool allow64) {
-    static const uint32_t cand[3] = {256, 128, 64};
-    static const double eff[3] = {1.0, 0.9, 0.67};
-    uint32_t best = 256;
-    double best_cost = 1e300;
-    for (int i = 0; i < 3; ++i) {
-        if (cand[i] == 64 && !allow64) continue;
-        const uint64_t tiles = loops_m_total * ((N + cand[i] - 1) / cand[i]);
-        const uint64_t waves = (tiles + sms - 1) / sms;
-        const double cost = static_cast<double>(waves) * cand[i] / eff[i];
-        if (cost < best_cost * 0.999) { best_cost = cost; best = cand[i]; }
-    }
-    return best;
-}
 
 // fp16/bf16 tile choice among one-CTA 128 x {64,128,256} tiles and CTA-pair
 // 256 x {128,256} tiles.  Cost = waves of tiles over the SMs (pairs count as
@@ -410,6 +393,7 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.esize = 2;
     p.g.swz_offset = sch.offset;
     p.g.swz_dir = sch.dir;
+    p.g.ps.init(static_cast<uint32_t>(M), static_cast<uint32_t>(N), tc.tm, bn, sch.offset, sch.dir);
     p.g.num_kb = (K + 63) / 64;
     p.g.chunk_kb = p.g.num_kb;
     p.g.total_tiles = static_cast<uint32_t>(tiles);
@@ -517,6 +501,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.esize = 1;
     p.g.swz_offset = sch.offset;
     p.g.swz_dir = sch.dir;
+    p.g.ps.init(static_cast<uint32_t>(M), static_cast<uint32_t>(N), kBM, bn, sch.offset, sch.dir);
     p.g.num_kb = K / 128;
     p.g.chunk_kb = p.g.num_kb;
     p.g.total_tiles = static_cast<uint32_t>(tiles);
@@ -736,6 +721,7 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     p.g.esize = 2;
     p.g.swz_offset = sch.offset;
     p.g.swz_dir = sch.dir;
+    p.g.ps.init(static_cast<uint32_t>(M), static_cast<uint32_t>(N), tm, tn, sch.offset, sch.dir);
     p.g.num_kb = (K + 63) / 64;
     p.g.chunk_kb = kDequantChunkK / 64;
     p.g.total_tiles = static_cast<uint32_t>(tiles);
@@ -773,8 +759,8 @@ bst_status bst_swizzle_map(uint32_t M, uint32_t N, uint32_t tile_m, uint32_t til
     if (total >= (1ull << 32)) return BST_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (bst_status s = device_info(dev)) return s;
-    SwizzleSched s;
-    s.update(M, N, tile_m, tile_n, sch.offset, sch.dir);
+    PlainSched s;
+    s.init(M, N, tile_m, tile_n, sch.offset, sch.dir);
     return cuda_status(launch_swizzle_map(s, static_cast<uint32_t>(total), out, static_cast<cudaStream_t>(stream)));
 }
 

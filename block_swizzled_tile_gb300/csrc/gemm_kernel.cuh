@@ -85,6 +85,7 @@ struct GemmArgs {
     int64_t ldc;
     int64_t c_batch_stride;
     uint32_t c_type;
+    PlainSched ps;          // plain / batched: the scheduler for the launched tile shape
     uint32_t c_vec;         // widest store (16, 8, 4 or 2 bytes) C's base, pitch and batch stride allow
     uint32_t acc_vec;       // the same for acc_out (int32 accumulators)
     const float* scale_a;
@@ -181,6 +182,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitCt
 // What the scheduler needs, in registers.
 struct SchedArgs {
     uint32_t M, N, swz_offset, swz_dir, mode, total_m;
+    const PlainSched* ps;   // plain / batched: the host-prepared scheduler
 };
 
 struct TileInfo {
@@ -206,10 +208,7 @@ __device__ __forceinline__ TileInfo tile_info(const SchedArgs& sa, uint32_t t, u
         ti.row0 = gt.row_off[g] + ti.m * TM;
         ti.m_lim = sa.total_m;
     } else {
-        s.update(sa.M, sa.N, TM, BN, sa.swz_offset, sa.swz_dir);
-        ti.tag = s.batch_idx(t);
-        s.block_coord(t, ti.m, ti.n);
-        s.actual_shape(ti.m, ti.n, ti.m_act, ti.n_act);
+        sa.ps->coord(t, ti.tag, ti.m, ti.n, ti.m_act, ti.n_act);
         ti.row0 = ti.m * TM;
         ti.m_lim = sa.M;
     }
@@ -509,7 +508,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
 
     // ---- arguments into registers, once
     const uint64_t t_entry = globaltimer_ns();
-    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m};
+    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m, &prm.g.ps};
     const uint32_t N = prm.g.N, K = prm.g.K, mode = prm.g.mode, esize = prm.g.esize;
     const uint32_t num_kb = prm.g.num_kb, chunk_kb = prm.g.chunk_kb, G = prm.g.G;
     const uint32_t a_tma = prm.g.a.use_tma, b_tma = prm.g.b.use_tma;

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m};
+    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m, &prm.g.ps};
     const uint32_t N = prm.g.N, mode = prm.g.mode, num_kb = prm.g.num_kb, G = prm.g.G;
     const uint32_t a_mn = prm.g.a.mn_major, b_mn = prm.g.b.mn_major;
     const uint32_t a_rank3 = prm.g.a.tma_rank == 3, b_rank3 = prm.g.b.tma_rank == 3;
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m};
+    const SchedArgs sa{prm.g.M, prm.g.N, prm.g.swz_offset, prm.g.swz_dir, prm.g.mode, prm.g.total_m, &prm.g.ps};
     const uint32_t num_kb = prm.g.num_kb;
     const uint32_t a_mn = prm.g.a.mn_major, b_mn = prm.g.b.mn_major;
     uint32_t* const err = prm.g.err;

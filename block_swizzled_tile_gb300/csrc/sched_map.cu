@@ -6,13 +6,13 @@
 
 namespace bst {
 
-__global__ void swizzle_map_kernel(SwizzleSched s, uint32_t total, uint32_t* __restrict__ out) {
+// Plain / batched: the host-prepared scheduler the GEMM kernels use.
+__global__ void swizzle_map_kernel(PlainSched s, uint32_t total, uint32_t* __restrict__ out) {
     for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
-        uint32_t m, n, ma, na;
-        s.block_coord(t, m, n);
-        s.actual_shape(m, n, ma, na);
+        uint32_t b, m, n, ma, na;
+        s.coord(t, b, m, n, ma, na);
         uint32_t* o = out + static_cast<uint64_t>(t) * 5;
-        o[0] = s.batch_idx(t);
+        o[0] = b;
         o[1] = m;
         o[2] = n;
         o[3] = ma;
@@ -20,7 +20,7 @@ __global__ void swizzle_map_kernel(SwizzleSched s, uint32_t total, uint32_t* __r
     }
 }
 
-cudaError_t launch_swizzle_map(const SwizzleSched& s, uint32_t total, uint32_t* out, cudaStream_t stream) {
+cudaError_t launch_swizzle_map(const PlainSched& s, uint32_t total, uint32_t* out, cudaStream_t stream) {
     if (total == 0) return cudaSuccess;
     const uint32_t blocks = min((total + 255) / 256, 4096u);
     swizzle_map_kernel<<<blocks, 256, 0, stream>>>(s, total, out);

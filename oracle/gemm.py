@@ -165,3 +165,32 @@ def gemm_quant_per_token(a, b, scale_a, scale_b, out_dtype="bf16"):
     sb = np.asarray(scale_b, dtype=np.float32).astype(np.float64)
     out = acc.astype(np.float64) * sa[:, None] * sb[None, :]
     return acc.astype(np.int32), round_out(out, out_dtype)
+
+
+def gemm_grouped_quant_per_token(a, b, group_m, scale_a, scale_b, out_dtype="bf16"):
+    """10_grouped_matmul_slice_m_per_token_dequant: the row slices of
+    02_grouped_matmul_slice_m combined with the per-token dequant of
+    12_quant_matmul.  Rows [off_g, off_g + M_g) of a (int8 [sum M_g, K]) use
+    b[g] (int8 [K, N], logical) and scale_b[g] ([N]); scale_a holds one scale
+    per row of a.  acc[i, j] = sum_k a[i,k] * b[g][k,j] exactly;
+    C[i, j] = round_out(acc[i, j] * scale_a[i] * scale_b[g][j]) with the
+    products in float64.  Returns (acc as int32, C)."""
+    a = np.asarray(a)
+    total = int(sum(group_m))
+    if total != a.shape[0]:
+        raise ValueError("group sizes do not add up to the rows of a")
+    n = np.asarray(b[0]).shape[1] if len(b) else 0
+    acc = np.zeros((total, n), dtype=np.int64)
+    out = np.zeros((total, n), dtype=np.float64)
+    sa = np.asarray(scale_a, dtype=np.float32).astype(np.float64)
+    off = 0
+    for g, mg in enumerate(group_m):
+        if mg:
+            acc_g = int_gemm_exact(a[off:off + mg], b[g])
+            sb = np.asarray(scale_b[g], dtype=np.float32).astype(np.float64)
+            acc[off:off + mg] = acc_g
+            out[off:off + mg] = acc_g.astype(np.float64) * sa[off:off + mg, None] * sb[None, :]
+        off += mg
+    if acc.size and (acc.max() > 2**31 - 1 or acc.min() < -2**31):
+        raise ValueError("accumulator does not fit int32")
+    return acc.astype(np.int32), round_out(out, out_dtype)

@@ -166,6 +166,46 @@ def test_quant_scales_are_row_and_column():
     assert np.array_equal(formats.bf16_bits_to_f64(out), base * sa[:, None] * sb[None, :])
 
 
+def test_grouped_quant_single_group_is_plain_quant():
+    g = wl._gen(21)
+    a = wl.uniform_int8((10, 48), g)
+    b = wl.uniform_int8((48, 9), g)
+    sa = wl.uniform_f32((10,), 1e-3, 1e-2, g)
+    sb = wl.uniform_f32((9,), 1e-3, 1e-2, g)
+    acc1, out1 = og.gemm_quant_per_token(a, b, sa, sb)
+    acc2, out2 = og.gemm_grouped_quant_per_token(a, b[None], [10], sa, sb[None])
+    assert np.array_equal(acc1, acc2) and np.array_equal(out1, out2)
+
+
+def test_grouped_quant_brute_force_and_empty_groups():
+    """Python-integer brute force on a tiny problem with empty groups; a
+    power-of-two change of one group's column scale moves only that group's
+    rows of that column."""
+    g = wl._gen(22)
+    gm = [2, 0, 3, 0, 1]
+    K, N = 5, 4
+    a = wl.uniform_int8((6, K), g)
+    b = wl.uniform_int8((5, K, N), g)
+    sa = np.array([1, 2, 4, 0.5, 8, 0.25], np.float32)
+    sb = np.array([[1, 2, 4, 8]] * 5, np.float32)
+    acc, out = og.gemm_grouped_quant_per_token(a, b, gm, sa, sb)
+    off = np.concatenate([[0], np.cumsum(gm)])
+    for gi in range(5):
+        for i in range(off[gi], off[gi + 1]):
+            for j in range(N):
+                want = sum(int(a[i, k]) * int(b[gi][k, j]) for k in range(K))
+                assert acc[i, j] == want
+                assert out[i, j] == formats.f64_to_bf16_bits(np.array([want * float(sa[i]) * float(sb[gi][j])]))[0]
+    sb2 = sb.copy()
+    sb2[2, 1] *= 4
+    acc2, out2 = og.gemm_grouped_quant_per_token(a, b, gm, sa, sb2)
+    changed = out2 != out
+    rows = set(np.nonzero(changed)[0]) | set()
+    assert rows <= set(range(off[2], off[3])) and set(np.nonzero(changed)[1]) <= {1}
+    assert np.array_equal(formats.bf16_bits_to_f64(out2[off[2]:off[3], 1]),
+                          formats.bf16_bits_to_f64(out[off[2]:off[3], 1]) * 4)
+
+
 # ---- planted mistakes in the oracle must fail the pins above ---------------
 
 def test_planted_transpose_is_caught(monkeypatch):

@@ -135,13 +135,24 @@ class Workload:
             self.dtype = "s8"
             self.desc = "int8 GEMM M=%d N=%d K=%d, int32 accumulate, per-token dequant, bf16 out" % (M, N, K)
             self.kernel_key = "gemm_int8_dequant_%dx%dx%d" % (M, N, K)
+        elif name == "grouped_int8_per_token":
+            w = wl.grouped_int8_per_token(seed=seed)
+            self.w = w
+            gm, N, K = w["group_m"], w["N"], w["K"]
+            self.flops = 2.0 * sum(gm) * N * K
+            self.in_bytes = w["x"].nbytes + sum(N * K for m in gm if m) + w["sa"].nbytes + w["sb"].nbytes
+            self.out_bytes = sum(gm) * N * 2
+            self.dtype = "s8"
+            self.desc = ("grouped int8 GEMM slice-M with per-token dequant, G=%d sizes %s, K=%d N=%d, int32 "
+                         "accumulate, bf16 out" % (len(gm), gm, K, N))
+            self.kernel_key = "gemm_grouped_int8_dequant_%dx%dx%d" % (sum(gm), N, K)
         else:
             raise SystemExit("unknown workload " + name)
         per_set = self.in_bytes + self.out_bytes
         # enough copies that the bytes between two uses of one copy exceed L2
         self.copies = copies or max(1, min(4096, math.ceil(2 * L2_BYTES / per_set)))
         self.sched = bst.sched(1, 0)
-        self.launches_per_step = 3 if name == "int8_per_token" else 1
+        self.launches_per_step = 3 if name in ("int8_per_token", "grouped_int8_per_token") else 1
         self._alloc()
 
     def _alloc(self):
@@ -163,6 +174,15 @@ class Workload:
                 s["X"], s["W"] = to_dev(w["x"]), to_dev(w["w"])
                 s["G"] = torch.tensor(w["group_m"], dtype=torch.int32, device="cuda")
                 s["C"] = torch.empty(sum(w["group_m"]) * w["N"], dtype=torch.int16, device="cuda")
+            elif self.name == "grouped_int8_per_token":
+                gm = w["group_m"]
+                s["X"], s["W"] = to_dev(w["x"]), to_dev(w["w"])
+                s["SA"], s["SB"] = to_dev(w["sa"]), to_dev(w["sb"])
+                s["G"] = torch.tensor(gm, dtype=torch.int32, device="cuda")
+                s["C"] = torch.empty(sum(gm) * w["N"], dtype=torch.int16, device="cuda")
+                nb = self.bst.gemm_grouped_quant_per_token_workspace_size(len(gm), sum(gm), w["N"], w["K"])
+                s["WS"] = torch.empty(nb, dtype=torch.uint8, device="cuda")
+                s["WSB"] = nb
             else:
                 s["A"], s["B"] = to_dev(w["a"]), to_dev(w["b"])
                 s["SA"], s["SB"] = to_dev(w["sa"]), to_dev(w["sb"])
@@ -186,6 +206,11 @@ class Workload:
             gm = w["group_m"]
             bst.gemm_grouped(len(gm), s["G"], sum(gm), w["N"], w["K"], s["X"], w["K"], s["W"], bst.ROW_MAJOR,
                              w["N"], w["K"] * w["N"], s["C"], w["N"], bst.BF16, bst.BF16, sched=sched)
+        elif self.name == "grouped_int8_per_token":
+            gm, N, K = w["group_m"], w["N"], w["K"]
+            bst.gemm_grouped_quant_per_token(len(gm), s["G"], sum(gm), N, K, s["X"], K, s["W"], bst.COL_MAJOR, K,
+                                             N * K, s["SA"], s["SB"], N, s["C"], N, None, s["WS"], s["WSB"],
+                                             sched=sched)
         else:
             bst.gemm_quant_per_token(w["M"], w["N"], w["K"], s["A"], w["K"], s["B"], bst.COL_MAJOR, w["K"],
                                      s["SA"], s["SB"], s["C"], w["N"], None, s["WS"], s["WSB"], sched=sched)
@@ -326,12 +351,20 @@ def oracle_rows(work, rows):
         x = og.decode(w["x"][off:off + take], "bf16")
         og.gemm(x, og.decode(w["w"][g], "bf16"), "bf16")
         return 2.0 * take * w["N"] * w["K"]
+    if work.name == "grouped_int8_per_token":
+        gm = w["group_m"]
+        g = next(i for i, m in enumerate(gm) if m)
+        take = min(rows, gm[g])
+        off = sum(gm[:g])
+        og.gemm_grouped_quant_per_token(w["x"][off:off + take], [w["w"][g].T], [take], w["sa"][off:off + take],
+                                        w["sb"][g:g + 1])
+        return 2.0 * take * w["N"] * w["K"]
     og.gemm_quant_per_token(w["a"][:rows], w["b"].T, w["sa"][:rows], w["sb"])
     return 2.0 * rows * w["N"] * w["K"]
 
 
 def total_rows(work):
-    return sum(work.w["group_m"]) if work.name == "grouped_bf16" else work.w["M"]
+    return sum(work.w["group_m"]) if work.name in ("grouped_bf16", "grouped_int8_per_token") else work.w["M"]
 
 
 def cpu_rate(work, budget_s):
@@ -362,7 +395,8 @@ def reference_arm(args, work_name):
     from block_swizzled_tile_gb300 import workloads as wl
     work.name = work_name
     work.w = {"fp16_square": wl.fp16_square, "fp16_tail": wl.fp16_tail, "mxfp8": wl.mxfp8,
-              "grouped_bf16": wl.grouped_bf16, "int8_per_token": wl.int8_per_token}[work_name]()
+              "grouped_bf16": wl.grouped_bf16, "int8_per_token": wl.int8_per_token,
+              "grouped_int8_per_token": wl.grouped_int8_per_token}[work_name]()
     desc = {"fp16_square": "fp16 GEMM M=1024 N=1024 K=2048, A row-major, B col-major, fp32 accumulate, fp16 out"}
     # size the per-step sample so that warmup + steps take about two minutes
     budget = min(20.0, 120.0 / max(1, args.steps + args.warmup))
@@ -400,7 +434,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="fp16_square",
-                    choices=["fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token"])
+                    choices=["fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token",
+                             "grouped_int8_per_token"])
     ap.add_argument("--lite", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.0)
     ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (64/128/256); 0 = automatic")
@@ -514,7 +549,9 @@ def main():
     if rank != 0:
         return
     peaks, src = measured_peaks()
-    per_launch_ms = ms / args.steps / work.launches_per_step
+    # int8 steps are three launches (two widenings and the GEMM) inside one
+    # C-ABI call: their roofline covers the whole step, not the GEMM alone
+    per_launch_ms = ms / args.steps
     value = whole_job_tflops(world, work.flops, args.steps, ms)
     # the sustained cuBLAS figure was taken under the power cap: use it when
     # the cap was active during this run's timed region, else the burst one
@@ -545,6 +582,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": stored_traffic(work.kernel_key),
                      "peak_source": peak_note, "kernel": work.kernel_key,
+                     "launches_covered": work.launches_per_step,
                      "per_launch_us": per_launch_ms * 1e3},
         "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
         "gpu_launches": args.steps * work.launches_per_step,

@@ -19,7 +19,8 @@ ROW_MAJOR, COL_MAJOR = 0, 1
 # bst_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(7)
 
-EXPORTED = ["bst_gemm", "bst_gemm_batched", "bst_gemm_grouped", "bst_gemm_quant_per_token",
+EXPORTED = ["bst_gemm", "bst_gemm_batched", "bst_gemm_grouped", "bst_gemm_grouped_quant_per_token",
+            "bst_gemm_grouped_quant_per_token_workspace_size", "bst_gemm_quant_per_token",
             "bst_gemm_quant_per_token_noalloc", "bst_gemm_quant_per_token_workspace_size", "bst_swizzle_map",
             "bst_swizzle_map_grouped", "bst_check_async", "bst_status_string", "bst_set_wait_timeout_ns"]
 # BST_NOALLOC_SCRATCH_BYTES: the scratch limit of gemm_quant_per_token_noalloc
@@ -58,6 +59,9 @@ _SIGS = {
     "bst_gemm_quant_per_token_workspace_size": [_i64, _i64, _i64],
     "bst_gemm_quant_per_token": [_i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _sz,
                                  ctypes.POINTER(Sched), _vp],
+    "bst_gemm_grouped_quant_per_token_workspace_size": [_i32, _i64, _i64, _i64],
+    "bst_gemm_grouped_quant_per_token": [_i32, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _i64, _vp, _vp,
+                                         _i64, _vp, _i64, _vp, _vp, _sz, ctypes.POINTER(Sched), _vp],
     "bst_gemm_quant_per_token_noalloc": [_i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64, _vp,
                                          ctypes.POINTER(Sched), _vp],
     "bst_swizzle_map": [_u32, _u32, _u32, _u32, _u32, ctypes.POINTER(Sched), _vp, _vp],
@@ -80,6 +84,7 @@ def lib():
             f.argtypes = args
             f.restype = ctypes.c_int
         L.bst_gemm_quant_per_token_workspace_size.restype = ctypes.c_size_t
+        L.bst_gemm_grouped_quant_per_token_workspace_size.restype = ctypes.c_size_t
         L.bst_status_string.restype = ctypes.c_char_p
         L.bst_set_wait_timeout_ns.restype = None
         _lib = L
@@ -146,6 +151,19 @@ def gemm_quant_per_token(M, N, K, A, lda, B, b_layout, ldb, scale_a, scale_b, C,
                                           _ptr(scale_b), _ptr(C), ldc, _ptr(acc_out), _ptr(workspace),
                                           workspace_bytes, _sched(sched), _stream(stream)),
            "bst_gemm_quant_per_token")
+
+
+def gemm_grouped_quant_per_token_workspace_size(G, total_m, N, K):
+    return lib().bst_gemm_grouped_quant_per_token_workspace_size(G, total_m, N, K)
+
+
+def gemm_grouped_quant_per_token(G, group_m, total_m, N, K, A, lda, B, b_layout, ldb, stride_b, scale_a, scale_b,
+                                 stride_sb, C, ldc, acc_out, workspace, workspace_bytes, sched=None, stream=None):
+    _check(lib().bst_gemm_grouped_quant_per_token(G, _ptr(group_m), total_m, N, K, _ptr(A), lda, _ptr(B), b_layout,
+                                                  ldb, stride_b, _ptr(scale_a), _ptr(scale_b), stride_sb, _ptr(C),
+                                                  ldc, _ptr(acc_out), _ptr(workspace), workspace_bytes,
+                                                  _sched(sched), _stream(stream)),
+           "bst_gemm_grouped_quant_per_token")
 
 
 def gemm_quant_per_token_noalloc(M, N, K, A, lda, B, b_layout, ldb, scale_a, scale_b, C, ldc, acc_out,

@@ -746,6 +746,102 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     return cuda_status(launch_dequant(p, grid, stream));
 }
 
+size_t bst_gemm_grouped_quant_per_token_workspace_size(int32_t G, int64_t total_m, int64_t N, int64_t K) {
+    if (G < 1 || total_m < 0 || N < 0 || K < 0) return 0;
+    const size_t kp = static_cast<size_t>((K + 7) / 8 * 8);
+    const size_t np = static_cast<size_t>((N + 7) / 8 * 8);
+    const size_t a = static_cast<size_t>(total_m) * kp * 2;
+    const size_t per_group = std::max(static_cast<size_t>(N) * kp, static_cast<size_t>(K) * np);
+    return round256(a) + round256(static_cast<size_t>(G) * per_group * 2);
+}
+
+bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, int64_t total_m, int64_t N, int64_t K,
+                                            const int8_t* A, int64_t lda, const int8_t* B, bst_layout b_layout,
+                                            int64_t ldb, int64_t stride_b, const float* scale_a, const float* scale_b,
+                                            int64_t stride_sb, void* C, int64_t ldc, int32_t* acc_out,
+                                            void* workspace, size_t workspace_bytes, const bst_sched* sched_in,
+                                            void* stream_v) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups || total_m < 0 || N < 0 || K < 0) return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(total_m) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(K) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    if (b_layout != BST_ROW_MAJOR && b_layout != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    // 256 x 256 CTA-pair tiles only
+    if ((sch.tile_m != 0 && sch.tile_m != 256) || (sch.tile_n != 0 && sch.tile_n != 256)) return BST_ERR_UNSUPPORTED;
+    const bool b_kmajor = b_layout == BST_COL_MAJOR;   // each B_g stored [N, K]
+    const int64_t b_rows = b_kmajor ? N : K, b_cols = b_kmajor ? K : N;
+    if (ldc < N || ldc < 1 || lda < 1 || lda < K || ldb < 1 || ldb < b_cols) return BST_ERR_INVALID_ARG;
+    if (G > 1 && (stride_b < b_rows * ldb || stride_sb < N)) return BST_ERR_INVALID_ARG;
+    if (total_m == 0 || N == 0) return BST_OK;
+    if (!group_m || !C || !scale_a || !scale_b || (K > 0 && (!A || !B))) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    if (K == 0) {
+        cudaError_t e = launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, total_m, N, 1, 2, dev.sms, stream);
+        if (e == cudaSuccess && acc_out)
+            e = launch_zero_fill(reinterpret_cast<uint8_t*>(acc_out), ldc, 0, total_m, N, 1, 4, dev.sms, stream);
+        return cuda_status(e);
+    }
+    const size_t need = bst_gemm_grouped_quant_per_token_workspace_size(G, total_m, N, K);
+    if (!workspace || workspace_bytes < need) return BST_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return BST_ERR_ALIGNMENT;
+    const int64_t kp = (K + 7) / 8 * 8;
+    const int64_t np = (N + 7) / 8 * 8;
+    const int64_t per_group = std::max(N * kp, K * np);          // widened elements between groups
+    uint16_t* wa = static_cast<uint16_t*>(workspace);
+    uint16_t* wb = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) +
+                                               round256(static_cast<size_t>(total_m) * kp * 2));
+    const int64_t ldwb = b_kmajor ? kp : np;
+    const uint64_t tiles_bound = ((total_m + 255) / 256 + G) * ((N + 255) / 256);
+    if (tiles_bound >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    if (smem_pair_dequant() + 8 * (static_cast<uint32_t>(G) + 1) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+
+    cudaError_t e = launch_widen_s8_bf16(A, lda, wa, kp, total_m, K, dev.sms, stream);
+    if (e == cudaSuccess)
+        e = launch_widen_s8_bf16(B, ldb, wb, ldwb, b_rows, b_cols, dev.sms, stream, G, G > 1 ? stride_b : 0, per_group);
+    if (e != cudaSuccess) return BST_ERR_CUDA;
+
+    OperandSpec a{wa, 2, static_cast<uint64_t>(total_m), static_cast<uint64_t>(K), kp, 0, 1, false};
+    OperandSpec b{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(K), ldwb, per_group,
+                  static_cast<uint64_t>(G), !b_kmajor};
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, 128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, true)) return s;
+    p.g.M = 0; p.g.N = N; p.g.K = K;
+    p.g.batch = 1;
+    p.g.mode = kModeGrouped;
+    p.g.ab_fmt = 1;
+    p.g.esize = 2;
+    p.g.swz_offset = sch.offset;
+    p.g.swz_dir = sch.dir;
+    p.g.num_kb = (K + 63) / 64;
+    p.g.chunk_kb = kDequantChunkK / 64;
+    p.g.group_m = group_m;
+    p.g.G = static_cast<uint32_t>(G);
+    p.g.total_m = static_cast<uint32_t>(total_m);
+    p.g.C = static_cast<uint8_t*>(C);
+    p.g.ldc = ldc;
+    p.g.c_type = kOutBF16;
+    p.g.c_vec = store_vec(C, ldc * 2, 0, 2);
+    p.g.acc_vec = acc_out ? store_vec(acc_out, ldc * 4, 0, 4) : 4u;
+    p.g.scale_a = scale_a;
+    p.g.scale_b = scale_b;
+    p.g.sb_group_stride = G > 1 ? stride_sb : 0;
+    p.g.acc_out = acc_out;
+    p.g.trace = sch.trace;
+    p.g.timeline = sch.timeline;
+    p.g.trace_cap = static_cast<uint32_t>(tiles_bound);
+    p.g.err = dev.err;
+    p.g.timeout_ns = timeout_ns();
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    return cuda_status(
+        launch_pair_dequant(p, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles_bound)), stream));
+}
+
 bst_status bst_swizzle_map(uint32_t M, uint32_t N, uint32_t tile_m, uint32_t tile_n, uint32_t batch,
                            const bst_sched* sched_in, uint32_t* out, void* stream) {
     if (tile_m < 1 || tile_n < 1 || batch < 1) return BST_ERR_INVALID_ARG;

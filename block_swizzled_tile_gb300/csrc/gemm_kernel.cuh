@@ -90,6 +90,7 @@ struct GemmArgs {
     uint32_t acc_vec;       // the same for acc_out (int32 accumulators)
     const float* scale_a;
     const float* scale_b;
+    int64_t sb_group_stride;   // grouped dequant: elements between the groups' scale_b rows
     int32_t* acc_out;
     const uint8_t* sfa;
     const uint8_t* sfb;

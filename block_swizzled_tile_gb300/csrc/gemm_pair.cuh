@@ -332,6 +332,8 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                 tc_fence_after();
                 const uint32_t grow = ti.row0 + wrow + lane;
                 const float sa_row = lane < rows_valid ? scale_a[grow] : 0.f;
+                // grouped: this group's column scales (tag = group; 0 for plain problems)
+                const float* sb_row = scale_b + static_cast<int64_t>(ti.tag) * prm.g.sb_group_stride;
 #pragma unroll 1
                 for (uint32_t cc = 0; cc < kCols / 32; ++cc) {
                     if (cc * 32 >= n_act) break;
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                     tmem_ld_32x32b_x32(run_t + cc * 32, r);
 #pragma unroll
                     for (uint32_t j = 0; j < 32; ++j) {
-                        const float sb = j < nv ? __ldg(scale_b + col0 + j) : 0.f;
+                        const float sb = j < nv ? __ldg(sb_row + col0 + j) : 0.f;
                         v[j] = __float_as_uint(static_cast<float>(static_cast<int32_t>(r[j])) * sa_row * sb);
                     }
                     store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(col0) * csize,

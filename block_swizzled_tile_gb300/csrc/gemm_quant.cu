@@ -26,44 +26,50 @@ uint32_t smem_dequant() { return GemmLayout<128, kDequantStages, 2, kKindF16>::s
 
 // Widens int8 to bf16, 16 elements per thread per step when the rows allow
 // 16-byte loads, element by element otherwise.  Bandwidth bound.
-__global__ void widen_s8_bf16_kernel(const int8_t* __restrict__ src, int64_t ld_src, uint16_t* __restrict__ dst,
-                                     int64_t ld_dst, int64_t rows, int64_t cols, int vec) {
+__global__ void widen_s8_bf16_kernel(const int8_t* __restrict__ src, int64_t ld_src, int64_t bs_src,
+                                     uint16_t* __restrict__ dst, int64_t ld_dst, int64_t bs_dst, int64_t rows,
+                                     int64_t cols, int64_t batch, int vec) {
+    // rows of all batches in one index space: global row R = b * rows + r
+    const int64_t all_rows = rows * batch;
     const int64_t chunks_per_row = vec ? cols / 16 : 0;
-    const int64_t total_vec = rows * chunks_per_row;
+    const int64_t total_vec = all_rows * chunks_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total_vec; i += stride) {
-        const int64_t r = i / chunks_per_row;
-        const int64_t c = (i - r * chunks_per_row) * 16;
-        const int4 raw = __ldg(reinterpret_cast<const int4*>(src + r * ld_src + c));
-        const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+        const int64_t R = i / chunks_per_row;
+        const int64_t c = (i - R * chunks_per_row) * 16;
+        const int64_t b = R / rows, r = R - b * rows;
+        const int4 raw = __ldg(reinterpret_cast<const int4*>(src + b * bs_src + r * ld_src + c));
+        const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
         uint32_t w[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(b[2 * j]), static_cast<float>(b[2 * j + 1]));
+            const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(q[2 * j]), static_cast<float>(q[2 * j + 1]));
             w[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        uint4* d = reinterpret_cast<uint4*>(dst + r * ld_dst + c);
+        uint4* d = reinterpret_cast<uint4*>(dst + b * bs_dst + r * ld_dst + c);
         d[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
     // columns not covered by 16-wide chunks
     const int64_t tail0 = chunks_per_row * 16;
     const int64_t tail_cols = cols - tail0;
-    const int64_t total_tail = rows * tail_cols;
+    const int64_t total_tail = all_rows * tail_cols;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total_tail; i += stride) {
-        const int64_t r = i / tail_cols;
-        const int64_t c = tail0 + (i - r * tail_cols);
-        const __nv_bfloat16 h = __float2bfloat16_rn(static_cast<float>(src[r * ld_src + c]));
-        dst[r * ld_dst + c] = *reinterpret_cast<const uint16_t*>(&h);
+        const int64_t R = i / tail_cols;
+        const int64_t c = tail0 + (i - R * tail_cols);
+        const int64_t b = R / rows, r = R - b * rows;
+        const __nv_bfloat16 h = __float2bfloat16_rn(static_cast<float>(src[b * bs_src + r * ld_src + c]));
+        dst[b * bs_dst + r * ld_dst + c] = *reinterpret_cast<const uint16_t*>(&h);
     }
 }
 
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
-                                 int64_t cols, uint32_t sms, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld_src % 16 == 0) &&
-                    (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (ld_dst % 8 == 0);
-    widen_s8_bf16_kernel<<<sms * 4, 256, 0, stream>>>(src, ld_src, dst, ld_dst, rows, cols, vec);
+                                 int64_t cols, uint32_t sms, cudaStream_t stream, int64_t batch, int64_t bs_src,
+                                 int64_t bs_dst) {
+    if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
+    const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld_src % 16 == 0) && (bs_src % 16 == 0) &&
+                    (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (ld_dst % 8 == 0) && (bs_dst % 8 == 0);
+    widen_s8_bf16_kernel<<<sms * 4, 256, 0, stream>>>(src, ld_src, bs_src, dst, ld_dst, bs_dst, rows, cols, batch, vec);
     return cudaGetLastError();
 }
 

@@ -92,7 +92,8 @@ uint32_t smem_pair(uint32_t bn, uint32_t groups);
 
 // int8 [rows, cols] (ld_src elements) -> bf16 [rows, cols] (ld_dst elements)
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
-                                 int64_t cols, uint32_t sms, cudaStream_t stream);
+                                 int64_t cols, uint32_t sms, cudaStream_t stream, int64_t batch = 1,
+                                 int64_t bs_src = 0, int64_t bs_dst = 0);
 
 // zero an [rows, cols] row-major output of `esize`-byte elements, `batch`
 // times at `batch_stride` elements apart

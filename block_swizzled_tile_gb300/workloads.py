@@ -147,3 +147,19 @@ def int8_per_token(M=8192, N=8192, K=8192, seed=0):
     return dict(kind="int8", M=M, N=N, K=K,
                 a=uniform_int8((M, K), g), b=uniform_int8((N, K), g),   # b is B^T: K contiguous
                 sa=uniform_f32((M,), 1e-3, 1e-2, g), sb=uniform_f32((N,), 1e-3, 1e-2, g))
+
+
+def grouped_int8_per_token(group_m=None, G=8, total_m=8192, N=4096, K=4096, seed=0):
+    """Grouped slice-M int8 with per-token dequant: the group sizes of the
+    grouped workload, the value distributions of the int8 one.  w holds each
+    group's B^T ([G, N, K], K contiguous); sb one row of column scales per
+    group."""
+    g = _gen(seed)
+    if group_m is None:
+        group_m = multinomial_groups(total_m, G, g)
+    group_m = [int(v) for v in group_m]
+    total = sum(group_m)
+    G = len(group_m)
+    return dict(kind="grouped_int8", group_m=group_m, G=G, N=N, K=K,
+                x=uniform_int8((total, K), g), w=uniform_int8((G, N, K), g),
+                sa=uniform_f32((total,), 1e-3, 1e-2, g), sb=uniform_f32((G, N), 1e-3, 1e-2, g))

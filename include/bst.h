@@ -198,6 +198,38 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K,
                                     const bst_sched* sched, void* stream);
 
 /*
+ * bst_gemm_grouped_quant_per_token -- grouped slice-M int8 GEMM with
+ * per-token dequant ("Block Dispatch Policies",
+ * 10_grouped_matmul_slice_m_per_token_dequant): for every group g, rows
+ * [off_g, off_g + M_g) of A and C (off_g = the sum of the earlier sizes) use
+ * B_g and the column scales of group g:
+ *
+ *   acc[i,j] = sum_k A[i,k] * B_g[k,j]         exactly, in int32
+ *   C[i,j]   = bf16( acc[i,j] * scale_a[i] * scale_b[g*stride_sb + j] )
+ *
+ * group_m: DEVICE int32 [G] (zero-size groups allowed; 1 <= G <= 1024), whose
+ * sum must equal total_m (else bst_check_async reports BST_ERR_DEVICE and no
+ * tile is computed).  A int8 [total_m, K] row-major (lda).  B: G matrices
+ * int8, stride_b elements apart, each [N, K] (BST_COL_MAJOR) or [K, N]
+ * (BST_ROW_MAJOR) with leading dimension ldb.  scale_a fp32 [total_m];
+ * scale_b fp32 [G, N] with row stride stride_sb.  C bf16 [total_m, N] (ldc);
+ * acc_out optional int32 [total_m, N] with ldc.  workspace: DEVICE scratch of
+ * bst_gemm_grouped_quant_per_token_workspace_size(G, total_m, N, K) bytes,
+ * 256-byte aligned, caller-owned; the operands are widened to bf16 there and
+ * multiplied exactly on 256 x 256 CTA-pair tiles (as bst_gemm_quant_per_token
+ * does), tasks numbered group-major with the swizzle restarted per group.
+ */
+size_t bst_gemm_grouped_quant_per_token_workspace_size(int32_t G, int64_t total_m, int64_t N, int64_t K);
+
+bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, int64_t total_m, int64_t N, int64_t K,
+                                            const int8_t* A, int64_t lda,
+                                            const int8_t* B, bst_layout b_layout, int64_t ldb, int64_t stride_b,
+                                            const float* scale_a, const float* scale_b, int64_t stride_sb,
+                                            void* C, int64_t ldc, int32_t* acc_out,
+                                            void* workspace, size_t workspace_bytes,
+                                            const bst_sched* sched, void* stream);
+
+/*
  * bst_gemm_quant_per_token_noalloc -- the same int8 GEMM with per-token
  * dequant as bst_gemm_quant_per_token (same arguments, results and errors),
  * for callers that cannot allocate device memory at the point of the call:

@@ -256,3 +256,85 @@ def test_int8_full_workload():
     racc, rout = oracle_int8_rows(w, rows)
     assert np.array_equal(acc[rows], racc)
     assert_close_fro(out[rows], rout, FRO_MX)
+
+
+# ------------------------------------------- grouped int8, per-token dequant -
+
+def run_grouped_int8(w, b_col_major=True, sched=None, gdev=None):
+    gm, N, K = w["group_m"], w["N"], w["K"]
+    G = len(gm)
+    total = sum(gm)
+    X = dev(w["x"])
+    W = w["w"] if b_col_major else np.ascontiguousarray(np.transpose(w["w"], (0, 2, 1)))   # [G, N, K] or [G, K, N]
+    Wd, SA, SB = dev(W), dev(w["sa"]), dev(w["sb"])
+    gdev = torch.tensor(gm, dtype=torch.int32, device="cuda") if gdev is None else gdev
+    cbuf, C = empty_bytes(max(total, 1) * N * 2, CANARY)
+    abuf, ACC = empty_bytes(max(total, 1) * N * 4, CANARY)
+    ws_bytes = bst.gemm_grouped_quant_per_token_workspace_size(G, total, N, K)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    bst.gemm_grouped_quant_per_token(G, gdev, total, N, K, X, K, Wd, bst.COL_MAJOR if b_col_major else bst.ROW_MAJOR,
+                                     K if b_col_major else N, N * K, SA, SB, N, C, N, ACC, ws, ws_bytes, sched=sched)
+    bst.check_async()
+    assert canary_intact(cbuf, CANARY) and canary_intact(abuf, CANARY)
+    out = decode_out(host(C, np.uint16).reshape(-1, N)[:total].copy(), "bf16")
+    acc = host(ACC, np.int32).reshape(-1, N)[:total].copy()
+    return out, acc
+
+
+def oracle_grouped_int8(w, rows=None):
+    gm = w["group_m"]
+    b = [np.ascontiguousarray(w["w"][g].T) for g in range(len(gm))]     # logical [K, N] per group
+    acc, out = og.gemm_grouped_quant_per_token(w["x"], b, gm, w["sa"], w["sb"])
+    out = decode_out(out, "bf16")
+    return (acc, out) if rows is None else (acc[rows], out[rows])
+
+
+@pytest.mark.parametrize("gm", [[3, 0, 130, 1, 0, 257], [0, 0, 64], [300], [1] * 9, [300, 0, 513]])
+@pytest.mark.parametrize("bcol", [True, False])
+def test_grouped_int8_small(gm, bcol):
+    """Empty groups, single-row groups, ragged tiles; K = 2100 takes three
+    K-chunks of the exact int32 accumulation."""
+    w = wl.grouped_int8_per_token(group_m=gm, N=300, K=2100, seed=len(gm) + 7)
+    G = len(gm)
+    total = sum(gm)
+    cap = (-(-total // 256) + G) * -(-300 // 256)
+    trace = torch.full((cap * 5,), -1, dtype=torch.int32, device="cuda")
+    out, acc = run_grouped_int8(w, bcol, bst.sched(2, 1, trace=trace))
+    racc, rout = oracle_grouped_int8(w)
+    assert np.array_equal(acc, racc)
+    assert_close_fro(out, rout, FRO_MX)
+    want = np.array(osw.grouped_swizzle_map(gm, 300, 256, 256, 2, 1), dtype=np.uint32).reshape(-1, 5)
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)[:len(want)]
+    assert np.array_equal(tr, want)
+
+
+def test_grouped_int8_inconsistent_sizes_reported():
+    w = wl.grouped_int8_per_token(group_m=[100, 100], N=64, K=64, seed=3)
+    gdev = torch.tensor([100, 300], dtype=torch.int32, device="cuda")   # sums past total_m = 200
+    with pytest.raises(bst.BstError) as e:
+        run_grouped_int8(w, True, gdev=gdev)
+    assert e.value.status == bst.ERR_DEVICE
+    bst.check_async()      # the error word was cleared
+
+
+@pytest.mark.parametrize("forced", [None, [0, 2048, 0, 1024, 3072, 0, 2048, 0]])
+def test_grouped_int8_full_workload(forced):
+    """G = 8 groups summing to 8192 rows, K = N = 4096; exact int32
+    accumulators and bf16 outputs on a seeded sample of whole rows."""
+    w = wl.grouped_int8_per_token(group_m=forced)
+    out, acc = run_grouped_int8(w, True)
+    rows = np.sort(np.random.default_rng(2).choice(sum(w["group_m"]), 256, replace=False))
+    gm = w["group_m"]
+    off = np.concatenate([[0], np.cumsum(gm)])
+    racc = np.zeros((len(rows), w["N"]), np.int64)
+    rout = np.zeros((len(rows), w["N"]))
+    for g in range(len(gm)):
+        sel = np.nonzero((rows >= off[g]) & (rows < off[g + 1]))[0]
+        if len(sel):
+            a, ro = og.gemm_quant_per_token(w["x"][rows[sel]], np.ascontiguousarray(w["w"][g].T),
+                                            w["sa"][rows[sel]], w["sb"][g])
+            racc[sel] = a
+            rout[sel] = decode_out(ro, "bf16")
+    assert np.array_equal(acc[rows], racc)
+    assert_close_fro(out[rows], rout, FRO_MX)
+

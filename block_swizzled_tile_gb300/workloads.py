@@ -163,3 +163,18 @@ def grouped_int8_per_token(group_m=None, G=8, total_m=8192, N=4096, K=4096, seed
     return dict(kind="grouped_int8", group_m=group_m, G=G, N=N, K=K,
                 x=uniform_int8((total, K), g), w=uniform_int8((G, N, K), g),
                 sa=uniform_f32((total,), 1e-3, 1e-2, g), sb=uniform_f32((G, N), 1e-3, 1e-2, g))
+
+
+def grouped_slice_k_bf16(group_k=None, G=8, total_k=8192, M=4096, N=4096, seed=0):
+    """Grouped slice-K, bf16: the token dimension is K and is split into G
+    groups (sizes drawn like the grouped slice-M workload's), as in a weight
+    gradient dW_g = X_g^T . dY_g.  x holds A^T ([sum K_g, M], M contiguous:
+    A is MN-major) and dy holds B ([sum K_g, N], N contiguous: MN-major), both
+    N(0, 1); the output is [G, M, N]."""
+    g = _gen(seed)
+    if group_k is None:
+        group_k = multinomial_groups(total_k, G, g)
+    group_k = [int(v) for v in group_k]
+    total = sum(group_k)
+    return dict(kind="slice_k", dtype="bf16", group_k=group_k, G=len(group_k), M=M, N=N,
+                x=normal16((total, M), 1.0, "bf16", g), dy=normal16((total, N), 1.0, "bf16", g))

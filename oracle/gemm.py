@@ -22,6 +22,13 @@ Variants, as the example list of "Block Dispatch Policies" names them:
                     10_grouped_matmul_slice_m_per_token_dequant: int8 operands,
                     int32 accumulators, one fp32 scale per row of A (the
                     "token") and one per column of B.
+* ``gemm_grouped_slice_k`` 05_grouped_matmul_slice_k: consecutive column
+                    slices of A times the matching row slices of B, one output
+                    matrix per group
+* ``gemm_grouped_slice_k_quant_per_token``
+                    11_grouped_matmul_slice_k_per_token_dequant: the same
+                    slices on int8 operands with each group dequantised by its
+                    own per-row and per-column scales
 * ``gemm_mxfp8``    the MXFP8 GEMM of "MI450 WMMA and ds_load Scheduling via a
                     DAG Mutation" (float8 e4m3 A and B with one E8M0 scale per
                     32 consecutive K elements of each row of A and column of B).
@@ -193,4 +200,65 @@ def gemm_grouped_quant_per_token(a, b, group_m, scale_a, scale_b, out_dtype="bf1
         off += mg
     if acc.size and (acc.max() > 2**31 - 1 or acc.min() < -2**31):
         raise ValueError("accumulator does not fit int32")
+    return acc.astype(np.int32), round_out(out, out_dtype)
+
+
+def _k_offsets(group_k, k_total):
+    """Exclusive prefix sums of the group K sizes; they must cover exactly
+    k_total columns of A (rows of B)."""
+    sizes = [int(k) for k in group_k]
+    if any(k < 0 for k in sizes):
+        raise ValueError("negative group size")
+    if sum(sizes) != k_total:
+        raise ValueError("group sizes do not add up to K")
+    offs = [0]
+    for k in sizes:
+        offs.append(offs[-1] + k)
+    return sizes, offs
+
+
+def gemm_grouped_slice_k_f64(a, b, group_k):
+    """The unrounded products of 05_grouped_matmul_slice_k: for group g with
+    K slice [off_g, off_g + K_g), part[g] = sum over k in the slice of
+    a[i, k] * b[k, j] in float64.  a is [M, sum K_g], b is [sum K_g, N];
+    returns [G, M, N].  A group with K_g = 0 gives a zero matrix."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    sizes, offs = _k_offsets(group_k, a.shape[1])
+    if b.shape[0] != a.shape[1]:
+        raise ValueError("inner dimensions differ")
+    out = np.zeros((len(sizes), a.shape[0], b.shape[1]), dtype=np.float64)
+    for g, kg in enumerate(sizes):
+        if kg:
+            out[g] = gemm_f64(a[:, offs[g]:offs[g + 1]], b[offs[g]:offs[g + 1], :])
+    return out
+
+
+def gemm_grouped_slice_k(a, b, group_k, out_dtype):
+    """05_grouped_matmul_slice_k: C[g] = round_out(A[:, slice g] . B[slice g, :]),
+    each group's float64 sum rounded once."""
+    return round_out(gemm_grouped_slice_k_f64(a, b, group_k), out_dtype)
+
+
+def gemm_grouped_slice_k_quant_per_token(a, b, group_k, scale_a, scale_b, out_dtype="bf16"):
+    """11_grouped_matmul_slice_k_per_token_dequant: the K slices of
+    05_grouped_matmul_slice_k on int8 a [M, sum K_g] and b [sum K_g, N]
+    (logical), each group dequantised as 12_quant_matmul does:
+    acc[g][i, j] = sum over k in slice g of a[i,k] * b[k,j] exactly (it must
+    fit int32), C[g][i, j] = round_out(acc[g][i, j] * scale_a[g][i] *
+    scale_b[g][j]) with the products in float64.  scale_a is [G, M] and
+    scale_b [G, N].  Returns (acc as int32 [G, M, N], C)."""
+    a = np.asarray(a)
+    b = np.asarray(b)
+    sizes, offs = _k_offsets(group_k, a.shape[1])
+    G, M, N = len(sizes), a.shape[0], b.shape[1]
+    acc = np.zeros((G, M, N), dtype=np.int64)
+    for g, kg in enumerate(sizes):
+        if kg:
+            acc[g] = int_gemm_exact(a[:, offs[g]:offs[g + 1]], b[offs[g]:offs[g + 1], :])
+    if acc.size and (acc.max() > 2**31 - 1 or acc.min() < -2**31):
+        raise ValueError("accumulator does not fit int32")
+    sa = np.asarray(scale_a, dtype=np.float32).astype(np.float64).reshape(G, M)
+    sb = np.asarray(scale_b, dtype=np.float32).astype(np.float64).reshape(G, N)
+    out = acc.astype(np.float64) * sa[:, :, None] * sb[:, None, :]
     return acc.astype(np.int32), round_out(out, out_dtype)

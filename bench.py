@@ -146,13 +146,25 @@ class Workload:
             self.desc = ("grouped int8 GEMM slice-M with per-token dequant, G=%d sizes %s, K=%d N=%d, int32 "
                          "accumulate, bf16 out" % (len(gm), gm, K, N))
             self.kernel_key = "gemm_grouped_int8_dequant_%dx%dx%d" % (sum(gm), N, K)
+        elif name == "grouped_slice_k_bf16":
+            w = wl.grouped_slice_k_bf16(seed=seed)
+            self.w = w
+            gk, M, N = w["group_k"], w["M"], w["N"]
+            self.flops = 2.0 * M * N * sum(gk)
+            self.in_bytes = w["x"].nbytes + w["dy"].nbytes
+            self.out_bytes = len(gk) * M * N * 2
+            self.dtype = "bf16"
+            self.desc = ("grouped bf16 GEMM slice-K (C_g = X_g^T dY_g), G=%d K sizes %s, M=%d N=%d, A and B "
+                         "MN-major, bf16 out" % (len(gk), gk, M, N))
+            self.kernel_key = "gemm_slice_k_bf16_%dx%dx%dx%d" % (len(gk), M, N, sum(gk))
         else:
             raise SystemExit("unknown workload " + name)
         per_set = self.in_bytes + self.out_bytes
         # enough copies that the bytes between two uses of one copy exceed L2
         self.copies = copies or max(1, min(4096, math.ceil(2 * L2_BYTES / per_set)))
         self.sched = bst.sched(1, 0)
-        self.launches_per_step = 3 if name in ("int8_per_token", "grouped_int8_per_token") else 1
+        self.launches_per_step = (3 if name in ("int8_per_token", "grouped_int8_per_token") else
+                                  2 if name == "grouped_slice_k_bf16" else 1)
         self._alloc()
 
     def _alloc(self):
@@ -183,6 +195,14 @@ class Workload:
                 nb = self.bst.gemm_grouped_quant_per_token_workspace_size(len(gm), sum(gm), w["N"], w["K"])
                 s["WS"] = torch.empty(nb, dtype=torch.uint8, device="cuda")
                 s["WSB"] = nb
+            elif self.name == "grouped_slice_k_bf16":
+                gk = w["group_k"]
+                s["X"], s["DY"] = to_dev(w["x"]), to_dev(w["dy"])
+                s["G"] = torch.tensor(gk, dtype=torch.int32, device="cuda")
+                s["C"] = torch.empty(len(gk) * w["M"] * w["N"], dtype=torch.int16, device="cuda")
+                nb = self.bst.gemm_grouped_slice_k_workspace_size(len(gk))
+                s["WS"] = torch.empty(nb, dtype=torch.uint8, device="cuda")
+                s["WSB"] = nb
             else:
                 s["A"], s["B"] = to_dev(w["a"]), to_dev(w["b"])
                 s["SA"], s["SB"] = to_dev(w["sa"]), to_dev(w["sb"])
@@ -211,6 +231,10 @@ class Workload:
             bst.gemm_grouped_quant_per_token(len(gm), s["G"], sum(gm), N, K, s["X"], K, s["W"], bst.COL_MAJOR, K,
                                              N * K, s["SA"], s["SB"], N, s["C"], N, None, s["WS"], s["WSB"],
                                              sched=sched)
+        elif self.name == "grouped_slice_k_bf16":
+            gk, M, N = w["group_k"], w["M"], w["N"]
+            bst.gemm_grouped_slice_k(len(gk), s["G"], M, N, sum(gk), s["X"], bst.COL_MAJOR, M, s["DY"], bst.ROW_MAJOR,
+                                     N, s["C"], N, M * N, bst.BF16, bst.BF16, s["WS"], s["WSB"], sched=sched)
         else:
             bst.gemm_quant_per_token(w["M"], w["N"], w["K"], s["A"], w["K"], s["B"], bst.COL_MAJOR, w["K"],
                                      s["SA"], s["SB"], s["C"], w["N"], None, s["WS"], s["WSB"], sched=sched)
@@ -351,6 +375,11 @@ def oracle_rows(work, rows):
         x = og.decode(w["x"][off:off + take], "bf16")
         og.gemm(x, og.decode(w["w"][g], "bf16"), "bf16")
         return 2.0 * take * w["N"] * w["K"]
+    if work.name == "grouped_slice_k_bf16":
+        take = min(rows, w["M"])
+        a = og.decode(np.ascontiguousarray(w["x"][:, :take].T), "bf16")
+        og.gemm_grouped_slice_k(a, og.decode(w["dy"], "bf16"), w["group_k"], "bf16")
+        return 2.0 * take * w["N"] * sum(w["group_k"])
     if work.name == "grouped_int8_per_token":
         gm = w["group_m"]
         g = next(i for i, m in enumerate(gm) if m)
@@ -396,7 +425,8 @@ def reference_arm(args, work_name):
     work.name = work_name
     work.w = {"fp16_square": wl.fp16_square, "fp16_tail": wl.fp16_tail, "mxfp8": wl.mxfp8,
               "grouped_bf16": wl.grouped_bf16, "int8_per_token": wl.int8_per_token,
-              "grouped_int8_per_token": wl.grouped_int8_per_token}[work_name]()
+              "grouped_int8_per_token": wl.grouped_int8_per_token,
+              "grouped_slice_k_bf16": wl.grouped_slice_k_bf16}[work_name]()
     desc = {"fp16_square": "fp16 GEMM M=1024 N=1024 K=2048, A row-major, B col-major, fp32 accumulate, fp16 out"}
     # size the per-step sample so that warmup + steps take about two minutes
     budget = min(20.0, 120.0 / max(1, args.steps + args.warmup))
@@ -435,7 +465,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="fp16_square",
                     choices=["fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token",
-                             "grouped_int8_per_token"])
+                             "grouped_int8_per_token", "grouped_slice_k_bf16"])
     ap.add_argument("--lite", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.0)
     ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (64/128/256); 0 = automatic")
@@ -549,8 +579,9 @@ def main():
     if rank != 0:
         return
     peaks, src = measured_peaks()
-    # int8 steps are three launches (two widenings and the GEMM) inside one
-    # C-ABI call: their roofline covers the whole step, not the GEMM alone
+    # int8 steps are three launches (two widenings and the GEMM) and slice-K
+    # steps two (the per-group map set-up and the GEMM) inside one C-ABI
+    # call: their roofline covers the whole step, not the GEMM alone
     per_launch_ms = ms / args.steps
     value = whole_job_tflops(world, work.flops, args.steps, ms)
     # the sustained cuBLAS figure was taken under the power cap: use it when

@@ -20,7 +20,9 @@ ROW_MAJOR, COL_MAJOR = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(7)
 
 EXPORTED = ["bst_gemm", "bst_gemm_batched", "bst_gemm_grouped", "bst_gemm_grouped_quant_per_token",
-            "bst_gemm_grouped_quant_per_token_workspace_size", "bst_gemm_quant_per_token",
+            "bst_gemm_grouped_quant_per_token_workspace_size", "bst_gemm_grouped_slice_k",
+            "bst_gemm_grouped_slice_k_workspace_size", "bst_gemm_grouped_slice_k_quant_per_token",
+            "bst_gemm_grouped_slice_k_quant_per_token_workspace_size", "bst_gemm_quant_per_token",
             "bst_gemm_quant_per_token_noalloc", "bst_gemm_quant_per_token_workspace_size", "bst_swizzle_map",
             "bst_swizzle_map_grouped", "bst_check_async", "bst_status_string", "bst_set_wait_timeout_ns"]
 # BST_NOALLOC_SCRATCH_BYTES: the scratch limit of gemm_quant_per_token_noalloc
@@ -62,6 +64,13 @@ _SIGS = {
     "bst_gemm_grouped_quant_per_token_workspace_size": [_i32, _i64, _i64, _i64],
     "bst_gemm_grouped_quant_per_token": [_i32, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _i64, _vp, _vp,
                                          _i64, _vp, _i64, _vp, _vp, _sz, ctypes.POINTER(Sched), _vp],
+    "bst_gemm_grouped_slice_k_workspace_size": [_i32],
+    "bst_gemm_grouped_slice_k": [_i32, _vp, _i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64, _vp, _i64, _i64,
+                                 _i32, _i32, _vp, _sz, ctypes.POINTER(Sched), _vp],
+    "bst_gemm_grouped_slice_k_quant_per_token_workspace_size": [_i32, _i64, _i64, _i64],
+    "bst_gemm_grouped_slice_k_quant_per_token": [_i32, _vp, _i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64,
+                                                 _vp, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _sz,
+                                                 ctypes.POINTER(Sched), _vp],
     "bst_gemm_quant_per_token_noalloc": [_i64, _i64, _i64, _vp, _i64, _vp, _i32, _i64, _vp, _vp, _vp, _i64, _vp,
                                          ctypes.POINTER(Sched), _vp],
     "bst_swizzle_map": [_u32, _u32, _u32, _u32, _u32, ctypes.POINTER(Sched), _vp, _vp],
@@ -85,6 +94,8 @@ def lib():
             f.restype = ctypes.c_int
         L.bst_gemm_quant_per_token_workspace_size.restype = ctypes.c_size_t
         L.bst_gemm_grouped_quant_per_token_workspace_size.restype = ctypes.c_size_t
+        L.bst_gemm_grouped_slice_k_workspace_size.restype = ctypes.c_size_t
+        L.bst_gemm_grouped_slice_k_quant_per_token_workspace_size.restype = ctypes.c_size_t
         L.bst_status_string.restype = ctypes.c_char_p
         L.bst_set_wait_timeout_ns.restype = None
         _lib = L
@@ -164,6 +175,33 @@ def gemm_grouped_quant_per_token(G, group_m, total_m, N, K, A, lda, B, b_layout,
                                                   ldc, _ptr(acc_out), _ptr(workspace), workspace_bytes,
                                                   _sched(sched), _stream(stream)),
            "bst_gemm_grouped_quant_per_token")
+
+
+def gemm_grouped_slice_k_workspace_size(G):
+    return lib().bst_gemm_grouped_slice_k_workspace_size(G)
+
+
+def gemm_grouped_slice_k(G, group_k, M, N, total_k, A, a_layout, lda, B, b_layout, ldb, C, ldc, stride_c, ab_type,
+                         c_type, workspace, workspace_bytes, sched=None, stream=None):
+    _check(lib().bst_gemm_grouped_slice_k(G, _ptr(group_k), M, N, total_k, _ptr(A), a_layout, lda, _ptr(B), b_layout,
+                                          ldb, _ptr(C), ldc, stride_c, ab_type, c_type, _ptr(workspace),
+                                          workspace_bytes, _sched(sched), _stream(stream)),
+           "bst_gemm_grouped_slice_k")
+
+
+def gemm_grouped_slice_k_quant_per_token_workspace_size(G, M, N, total_k):
+    return lib().bst_gemm_grouped_slice_k_quant_per_token_workspace_size(G, M, N, total_k)
+
+
+def gemm_grouped_slice_k_quant_per_token(G, group_k, M, N, total_k, A, a_layout, lda, B, b_layout, ldb, scale_a,
+                                         stride_sa, scale_b, stride_sb, C, ldc, stride_c, acc_out, workspace,
+                                         workspace_bytes, sched=None, stream=None):
+    _check(lib().bst_gemm_grouped_slice_k_quant_per_token(G, _ptr(group_k), M, N, total_k, _ptr(A), a_layout, lda,
+                                                          _ptr(B), b_layout, ldb, _ptr(scale_a), stride_sa,
+                                                          _ptr(scale_b), stride_sb, _ptr(C), ldc, stride_c,
+                                                          _ptr(acc_out), _ptr(workspace), workspace_bytes,
+                                                          _sched(sched), _stream(stream)),
+           "bst_gemm_grouped_slice_k_quant_per_token")
 
 
 def gemm_quant_per_token_noalloc(M, N, K, A, lda, B, b_layout, ldb, scale_a, scale_b, C, ldc, acc_out,

@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libbst.so")
-UNITS = ["api.cu", "gemm_dense.cu", "gemm_pair.cu", "gemm_mxf8.cu", "gemm_quant.cu", "sched_map.cu", "noalloc.cu"]
+UNITS = ["api.cu", "gemm_dense.cu", "gemm_pair.cu", "gemm_mxf8.cu", "gemm_quant.cu", "sched_map.cu", "noalloc.cu", "slice_k.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

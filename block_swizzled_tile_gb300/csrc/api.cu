@@ -552,6 +552,92 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 using namespace bst;
 
+namespace {
+
+// Shared by the bf16 and the int8 slice-K entry points once the operands are
+// 16-bit and TMA-addressable: builds the whole-operand maps, launches the
+// per-group set-up and then the CTA-pair GEMM in slice-K mode.
+struct SliceKRun {
+    OperandSpec a, b;      // A: MN extent M, K total_k; B: MN extent N
+    uint32_t ab_fmt;       // kind::f16 format: 0 f16, 1 bf16
+    CUtensorMapDataType dt;
+    uint32_t c_code, csize;
+    void* C;
+    int64_t ldc, stride_c;
+    const float* scale_a = nullptr;
+    const float* scale_b = nullptr;
+    int64_t stride_sa = 0, stride_sb = 0;
+    int32_t* acc_out = nullptr;
+    bool dequant = false;
+};
+
+bst_status run_slice_k(const SliceKRun& r, int32_t G, const int32_t* group_k, int64_t M, int64_t N,
+                       int64_t total_k, uint8_t* meta, const Sched& sch, const DeviceInfo& dev, cudaStream_t stream) {
+    uint32_t bn = 256;
+    if (r.dequant) {
+        if (sch.tile_n != 0 && sch.tile_n != 256) return BST_ERR_UNSUPPORTED;
+    } else {
+        Sched pair_only = sch;
+        pair_only.tile_m = 256;
+        TileChoice tc;
+        if (bst_status s = choose_tile(pair_only, true, false, M, G, N, dev.sms, tc)) return s;
+        bn = tc.bn;
+    }
+    const uint64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn) * static_cast<uint64_t>(G);
+    if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
+    const uint32_t smem_need = r.dequant ? smem_pair_dequant() + 8 * (static_cast<uint32_t>(G) + 1)
+                                         : smem_pair(bn, static_cast<uint32_t>(G));
+    if (smem_need > dev.max_smem) return BST_ERR_UNSUPPORTED;
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (bst_status s = fill_operand(p.g.a, &p.tmap_a, r.a, kBM, r.dt, true)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, r.b, bn / 2, r.dt, true)) return s;
+    uint8_t* maps = meta;
+    uint32_t* group_kb = reinterpret_cast<uint32_t*>(meta + static_cast<size_t>(G) * 256);
+    // bytes between consecutive K indices, and which map dimension runs along K
+    const uint64_t a_kstep = r.a.mn_major ? static_cast<uint64_t>(r.a.ld) * r.a.esize : r.a.esize;
+    const uint64_t b_kstep = r.b.mn_major ? static_cast<uint64_t>(r.b.ld) * r.b.esize : r.b.esize;
+    cudaError_t e = launch_slice_k_prep(p.tmap_a, p.tmap_b, group_k, static_cast<uint32_t>(G),
+                                        static_cast<uint64_t>(total_k), r.a.ptr, a_kstep, r.a.mn_major ? 1u : 0u,
+                                        r.b.ptr, b_kstep, r.b.mn_major ? 1u : 0u, maps, group_kb, dev.err, stream);
+    if (e != cudaSuccess) return BST_ERR_CUDA;
+    p.g.M = M; p.g.N = N; p.g.K = total_k;
+    p.g.batch = static_cast<uint32_t>(G);
+    p.g.mode = kModeSliceK;
+    p.g.ab_fmt = r.ab_fmt;
+    p.g.esize = 2;
+    p.g.swz_offset = sch.offset;
+    p.g.swz_dir = sch.dir;
+    p.g.ps.init(static_cast<uint32_t>(M), static_cast<uint32_t>(N), 256, bn, sch.offset, sch.dir);
+    p.g.num_kb = (total_k + 63) / 64;
+    p.g.chunk_kb = r.dequant ? kDequantChunkK / 64 : p.g.num_kb;
+    p.g.total_tiles = static_cast<uint32_t>(tiles);
+    p.g.G = static_cast<uint32_t>(G);
+    p.g.kmaps = maps;
+    p.g.group_kb = group_kb;
+    p.g.C = static_cast<uint8_t*>(r.C);
+    p.g.ldc = r.ldc;
+    p.g.c_batch_stride = r.stride_c;
+    p.g.c_type = r.c_code;
+    p.g.c_vec = store_vec(r.C, r.ldc * r.csize, r.stride_c * r.csize, r.csize);
+    p.g.scale_a = r.scale_a;
+    p.g.scale_b = r.scale_b;
+    p.g.sa_group_stride = r.stride_sa;
+    p.g.sb_group_stride = r.stride_sb;
+    p.g.acc_out = r.acc_out;
+    p.g.acc_vec = r.acc_out ? store_vec(r.acc_out, r.ldc * 4, r.stride_c * 4, 4) : 4u;
+    p.g.trace = sch.trace;
+    p.g.timeline = sch.timeline;
+    p.g.trace_cap = static_cast<uint32_t>(tiles);
+    p.g.err = dev.err;
+    p.g.timeout_ns = timeout_ns();
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    const uint32_t pairs = static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles));
+    return cuda_status(r.dequant ? launch_pair_dequant(p, pairs, stream) : launch_pair(p, bn, pairs, stream));
+}
+
+}  // namespace
+
 extern "C" {
 
 bst_status bst_gemm(int64_t M, int64_t N, int64_t K, const void* A, bst_dtype a_type, bst_layout a_layout,
@@ -840,6 +926,135 @@ bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, i
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     return cuda_status(
         launch_pair_dequant(p, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles_bound)), stream));
+}
+
+size_t bst_gemm_grouped_slice_k_workspace_size(int32_t G) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups) return 0;
+    return static_cast<size_t>(G) * 256 + round256(4 * (static_cast<size_t>(G) + 1));
+}
+
+
+bst_status bst_gemm_grouped_slice_k(int32_t G, const int32_t* group_k, int64_t M, int64_t N, int64_t total_k,
+                                    const void* A, bst_layout a_layout, int64_t lda, const void* B,
+                                    bst_layout b_layout, int64_t ldb, void* C, int64_t ldc, int64_t stride_c,
+                                    bst_dtype ab_type, bst_dtype c_type, void* workspace, size_t workspace_bytes,
+                                    const bst_sched* sched_in, void* stream_v) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups || M < 0 || N < 0 || total_k < 0) return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(M) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(total_k) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    if (ab_type != BST_F16 && ab_type != BST_BF16) return BST_ERR_UNSUPPORTED;
+    uint32_t c_code;
+    if (!out_code(c_type, c_code)) return BST_ERR_UNSUPPORTED;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if ((sch.tile_m != 0 && sch.tile_m != 256) || sch.split_k > 1) return BST_ERR_UNSUPPORTED;
+    if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
+    if (G > 1 && stride_c < M * ldc) return BST_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BST_OK;
+    if (!C || !group_k || (total_k > 0 && (!A || !B))) return BST_ERR_INVALID_ARG;
+    OperandSpec a, b;
+    if (bst_status s = make_specs(M, N, total_k, A, a_layout, lda, 0, B, b_layout, ldb, 0, 2, 1, a, b)) return s;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const uint32_t csize = dtype_bytes(c_type);
+    if (total_k == 0)   // every group is empty
+        return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, stride_c, M, N, G, csize, dev.sms, stream));
+    if (!tma_ok(a) || !tma_ok(b)) return BST_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < bst_gemm_grouped_slice_k_workspace_size(G)) return BST_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return BST_ERR_ALIGNMENT;
+    SliceKRun r;
+    r.a = a;
+    r.b = b;
+    r.ab_fmt = ab_type == BST_BF16 ? 1u : 0u;
+    r.dt = tmap_type(ab_type);
+    r.c_code = c_code;
+    r.csize = csize;
+    r.C = C;
+    r.ldc = ldc;
+    r.stride_c = G > 1 ? stride_c : 0;
+    return run_slice_k(r, G, group_k, M, N, total_k, static_cast<uint8_t*>(workspace), sch, dev, stream);
+}
+
+size_t bst_gemm_grouped_slice_k_quant_per_token_workspace_size(int32_t G, int64_t M, int64_t N, int64_t total_k) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups || M < 0 || N < 0 || total_k < 0) return 0;
+    const size_t kp = static_cast<size_t>((total_k + 7) / 8 * 8);
+    const size_t mp = static_cast<size_t>((M + 7) / 8 * 8);
+    const size_t np = static_cast<size_t>((N + 7) / 8 * 8);
+    const size_t a = std::max(static_cast<size_t>(M) * kp, static_cast<size_t>(total_k) * mp) * 2;
+    const size_t b = std::max(static_cast<size_t>(N) * kp, static_cast<size_t>(total_k) * np) * 2;
+    return round256(bst_gemm_grouped_slice_k_workspace_size(G)) + round256(a) + round256(b);
+}
+
+bst_status bst_gemm_grouped_slice_k_quant_per_token(int32_t G, const int32_t* group_k, int64_t M, int64_t N,
+                                                    int64_t total_k, const int8_t* A, bst_layout a_layout,
+                                                    int64_t lda, const int8_t* B, bst_layout b_layout, int64_t ldb,
+                                                    const float* scale_a, int64_t stride_sa, const float* scale_b,
+                                                    int64_t stride_sb, void* C, int64_t ldc, int64_t stride_c,
+                                                    int32_t* acc_out, void* workspace, size_t workspace_bytes,
+                                                    const bst_sched* sched_in, void* stream_v) {
+    if (G < 1 || static_cast<uint32_t>(G) > kMaxGroups || M < 0 || N < 0 || total_k < 0) return BST_ERR_INVALID_ARG;
+    if (static_cast<uint64_t>(M) > kMaxDim || static_cast<uint64_t>(N) > kMaxDim ||
+        static_cast<uint64_t>(total_k) > kMaxDim)
+        return BST_ERR_INVALID_ARG;
+    if (a_layout != BST_ROW_MAJOR && a_layout != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
+    if (b_layout != BST_ROW_MAJOR && b_layout != BST_COL_MAJOR) return BST_ERR_INVALID_ARG;
+    Sched sch;
+    if (bst_status s = read_sched(sched_in, sch)) return s;
+    if ((sch.tile_m != 0 && sch.tile_m != 256) || (sch.tile_n != 0 && sch.tile_n != 256) || sch.split_k > 1)
+        return BST_ERR_UNSUPPORTED;
+    const bool a_kmajor = a_layout == BST_ROW_MAJOR;   // A stored [M, total_k]
+    const bool b_kmajor = b_layout == BST_COL_MAJOR;   // B stored [N, total_k]
+    if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
+    if (lda < 1 || lda < (a_kmajor ? total_k : M) || ldb < 1 || ldb < (b_kmajor ? total_k : N))
+        return BST_ERR_INVALID_ARG;
+    if (G > 1 && (stride_c < M * ldc || stride_sa < 0 || stride_sb < 0)) return BST_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BST_OK;
+    if (!C || !group_k || !scale_a || !scale_b || (total_k > 0 && (!A || !B))) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const int64_t sc = G > 1 ? stride_c : 0;
+    if (total_k == 0) {
+        cudaError_t e = launch_zero_fill(static_cast<uint8_t*>(C), ldc, sc, M, N, G, 2, dev.sms, stream);
+        if (e == cudaSuccess && acc_out)
+            e = launch_zero_fill(reinterpret_cast<uint8_t*>(acc_out), ldc, sc, M, N, G, 4, dev.sms, stream);
+        return cuda_status(e);
+    }
+    if (!workspace || workspace_bytes < bst_gemm_grouped_slice_k_quant_per_token_workspace_size(G, M, N, total_k))
+        return BST_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return BST_ERR_ALIGNMENT;
+    const int64_t kp = (total_k + 7) / 8 * 8, mp = (M + 7) / 8 * 8, np = (N + 7) / 8 * 8;
+    uint8_t* meta = static_cast<uint8_t*>(workspace);
+    const size_t meta_bytes = round256(bst_gemm_grouped_slice_k_workspace_size(G));
+    const size_t a_bytes = round256(std::max(static_cast<size_t>(M) * kp, static_cast<size_t>(total_k) * mp) * 2);
+    uint16_t* wa = reinterpret_cast<uint16_t*>(meta + meta_bytes);
+    uint16_t* wb = reinterpret_cast<uint16_t*>(meta + meta_bytes + a_bytes);
+    const int64_t ldwa = a_kmajor ? kp : mp, ldwb = b_kmajor ? kp : np;
+    cudaError_t e = a_kmajor ? launch_widen_s8_bf16(A, lda, wa, ldwa, M, total_k, dev.sms, stream)
+                             : launch_widen_s8_bf16(A, lda, wa, ldwa, total_k, M, dev.sms, stream);
+    if (e == cudaSuccess)
+        e = b_kmajor ? launch_widen_s8_bf16(B, ldb, wb, ldwb, N, total_k, dev.sms, stream)
+                     : launch_widen_s8_bf16(B, ldb, wb, ldwb, total_k, N, dev.sms, stream);
+    if (e != cudaSuccess) return BST_ERR_CUDA;
+    SliceKRun r;
+    r.a = OperandSpec{wa, 2, static_cast<uint64_t>(M), static_cast<uint64_t>(total_k), ldwa, 0, 1, !a_kmajor};
+    r.b = OperandSpec{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(total_k), ldwb, 0, 1, !b_kmajor};
+    r.ab_fmt = 1;
+    r.dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    r.c_code = kOutBF16;
+    r.csize = 2;
+    r.C = C;
+    r.ldc = ldc;
+    r.stride_c = sc;
+    r.scale_a = scale_a;
+    r.scale_b = scale_b;
+    r.stride_sa = G > 1 ? stride_sa : 0;
+    r.stride_sb = G > 1 ? stride_sb : 0;
+    r.acc_out = acc_out;
+    r.dequant = true;
+    return run_slice_k(r, G, group_k, M, N, total_k, meta, sch, dev, stream);
 }
 
 bst_status bst_swizzle_map(uint32_t M, uint32_t N, uint32_t tile_m, uint32_t tile_n, uint32_t batch,

@@ -37,7 +37,10 @@ namespace bst {
 
 enum : uint32_t { kKindF16 = 0, kKindMXF8 = 1 };
 enum : uint32_t { kEpiStore = 0, kEpiDequant = 1 };
-enum : uint32_t { kModePlain = 0, kModeBatched = 1, kModeGrouped = 2 };
+// kModeSliceK: groups along K ("Block Dispatch Policies",
+// 05_grouped_matmul_slice_k); group g is batch g of the scheduler, with its
+// own tensor maps (kmaps) and k-block count (group_kb).
+enum : uint32_t { kModePlain = 0, kModeBatched = 1, kModeGrouped = 2, kModeSliceK = 3 };
 enum : uint32_t { kOutF16 = 0, kOutBF16 = 1, kOutF32 = 2, kOutS32 = 3 };   // kOutS32: raw int32 (device side only)
 
 constexpr uint32_t kBM = 128;          // tile rows = TMEM lanes
@@ -91,6 +94,9 @@ struct GemmArgs {
     const float* scale_a;
     const float* scale_b;
     int64_t sb_group_stride;   // grouped dequant: elements between the groups' scale_b rows
+    int64_t sa_group_stride;   // slice-K dequant: elements between the groups' scale_a rows
+    const uint8_t* kmaps;      // slice-K: per group 256 bytes, the A then the B tensor map
+    const uint32_t* group_kb;  // slice-K: k-blocks of each group, then a status word (non-zero: bad sizes)
     int32_t* acc_out;
     const uint8_t* sfa;
     const uint8_t* sfb;

@@ -14,7 +14,7 @@ static cudaError_t launch_pair_one(const GemmParams& p, uint32_t max_pairs, cuda
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(pair_threads<EPI>());
-    cfg.dynamicSmemBytes = Lay::smem_bytes(p.g.mode == kModeGrouped ? p.g.G : 0);
+    cfg.dynamicSmemBytes = Lay::smem_bytes((p.g.mode == kModeGrouped || p.g.mode == kModeSliceK) ? p.g.G : 0);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -105,6 +105,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
     gt.G = G;
     gt.tile_off = reinterpret_cast<uint32_t*>(smem + Lay::kTableOff);
     gt.row_off = gt.tile_off + (mode == kModeGrouped ? G + 1 : 0);
+    // k-blocks of a tile: the group's own count for slice-K (kept in the
+    // group table's first G words), else every tile's
+    auto tile_kb = [&](uint32_t tag) -> uint32_t { return mode == kModeSliceK ? gt.tile_off[tag] : num_kb; };
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < STAGES; ++s) {
@@ -133,6 +136,12 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
     griddep_launch_dependents();
     if (mode == kModeGrouped && warp == 2)
         build_group_table(gt, prm.g.group_m, G, N, TM, BN, sa.total_m, err, tiles_smem, lane);
+    if (mode == kModeSliceK && warp == 2) {
+        // the set-up kernel's per-group k-block counts; bad sizes: no tasks
+        const uint32_t bad = prm.g.group_kb[G];
+        for (uint32_t g = lane; g < G; g += 32) gt.tile_off[g] = bad ? 0u : prm.g.group_kb[g];
+        if (lane == 0 && bad) *tiles_smem = 0;
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -149,8 +158,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
         const uint32_t full_leader = map_to_cta(smem_u32(full), 0);
         constexpr uint32_t tx = Lay::kABytes + Lay::kBBytes;
         const bool is_a = warp == 0;
-        uint32_t stage = 0, phase = 0, issued = 0;
+        uint32_t stage = 0, phase = 0, issued = 0, map_group = 0xFFFFFFFFu;
         bool ok = true;
+        const CUtensorMap* map_a = &prm.tmap_a;
+        const CUtensorMap* map_b = &prm.tmap_b;
         // single threads issue the loads (cheaper per k-block than a
         // warp-wide loop with one active lane)
         for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t += nclusters) {
@@ -158,7 +169,17 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
             const uint32_t a_row = ti.row0 + rank * kBM;
             const uint32_t b_col = ti.n * BN + rank * BH;
             const int32_t zc = static_cast<int32_t>(ti.tag);
-            for (uint32_t kb = 0; kb < num_kb; ++kb) {
+            const uint32_t tkb = tile_kb(ti.tag);
+            if (mode == kModeSliceK && tkb && ti.tag != map_group) {
+                // this group's maps (base at its first K element, K extent
+                // its size), written by the set-up kernel
+                const uint8_t* gm = prm.g.kmaps + static_cast<uint64_t>(ti.tag) * 256u;
+                map_a = reinterpret_cast<const CUtensorMap*>(gm);
+                map_b = reinterpret_cast<const CUtensorMap*>(gm + 128);
+                tmap_acquire(is_a ? gm : gm + 128);
+                map_group = ti.tag;
+            }
+            for (uint32_t kb = 0; kb < tkb; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                 {
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
@@ -168,21 +189,21 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                     if (is_a) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                         if (!a_mn) {
-                            if (a_rank3) tma_load_3d_pair(sa_s, &prm.tmap_a, bar, k0, a_row, zc);
-                            else tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);
+                            if (a_rank3) tma_load_3d_pair(sa_s, map_a, bar, k0, a_row, zc);
+                            else tma_load_2d_pair(sa_s, map_a, bar, k0, a_row);
                         } else {
                             for (uint32_t j = 0; j < kBM / bk_elems; ++j) {
-                                if (a_rank3) tma_load_3d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0, zc);
-                                else tma_load_2d_pair(sa_s + j * bk_elems * kLine, &prm.tmap_a, bar, a_row + j * bk_elems, k0);
+                                if (a_rank3) tma_load_3d_pair(sa_s + j * bk_elems * kLine, map_a, bar, a_row + j * bk_elems, k0, zc);
+                                else tma_load_2d_pair(sa_s + j * bk_elems * kLine, map_a, bar, a_row + j * bk_elems, k0);
                             }
                         }
                     } else if (!b_mn) {
-                        if (b_rank3) tma_load_3d_pair(sb_s, &prm.tmap_b, bar, k0, b_col, zc);
-                        else tma_load_2d_pair(sb_s, &prm.tmap_b, bar, k0, b_col);
+                        if (b_rank3) tma_load_3d_pair(sb_s, map_b, bar, k0, b_col, zc);
+                        else tma_load_2d_pair(sb_s, map_b, bar, k0, b_col);
                     } else {
                         for (uint32_t j = 0; j < BH / bk_elems; ++j) {
-                            if (b_rank3) tma_load_3d_pair(sb_s + j * bk_elems * kLine, &prm.tmap_b, bar, b_col + j * bk_elems, k0, zc);
-                            else tma_load_2d_pair(sb_s + j * bk_elems * kLine, &prm.tmap_b, bar, b_col + j * bk_elems, k0);
+                            if (b_rank3) tma_load_3d_pair(sb_s + j * bk_elems * kLine, map_b, bar, b_col + j * bk_elems, k0, zc);
+                            else tma_load_2d_pair(sb_s + j * bk_elems * kLine, map_b, bar, b_col + j * bk_elems, k0);
                         }
                     }
                     if (tl && is_a && issued < 15) tl[1 + issued] = globaltimer_ns();
@@ -212,12 +233,14 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
             bool ok = true, any_mma = false;
             const uint32_t chunk_kb = prm.g.chunk_kb;
-            const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
             for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t += nclusters) {
+              // an empty slice-K group has no MMAs: its epilogue stores zeros
+              const uint32_t tkb = mode == kModeSliceK ? tile_kb(tile_info(sa, t, TM, BN, gt).tag) : num_kb;
+              const uint32_t nchunks = (tkb + chunk_kb - 1) / chunk_kb;
               // K-chunks (one for plain stores): each fills one accumulator
               for (uint32_t c = 0; ok && c < nchunks; ++c) {
                 const uint32_t kb_begin = c * chunk_kb;
-                const uint32_t kb_end = min(num_kb, kb_begin + chunk_kb);
+                const uint32_t kb_end = min(tkb, kb_begin + chunk_kb);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -270,7 +293,6 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
         const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
         const uint32_t tempty_leader = map_to_cta(smem_u32(tempty), 0);
         const uint32_t chunk_kb = prm.g.chunk_kb;
-        const uint32_t nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
         uint32_t acc = 0, acc_phase = 0, ep_tile = 0;
         bool ok = true;
         for (uint32_t t = cid; ok && t < total_tiles; t += nclusters) {
@@ -284,12 +306,31 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                 }
             }
             const uint32_t rows_valid = ti.m_act > wrow ? min(32u, ti.m_act - wrow) : 0u;   // warp-uniform
-            const int64_t cbase = mode == kModeBatched ? static_cast<int64_t>(ti.tag) * c_bs : 0;
+            const int64_t cbase = (mode == kModeBatched || mode == kModeSliceK) ? static_cast<int64_t>(ti.tag) * c_bs : 0;
             uint8_t* const cwarp = C + (cbase + static_cast<int64_t>(ti.row0 + wrow) * ldc) * csize;
             const uint32_t n0 = ti.n * BN + col_off;     // first output column of this warp
             const uint32_t n_act = ti.n_act > col_off ? ti.n_act - col_off : 0u;
             // dequant: exact int32 running sums of this warp's rows and columns
             const uint32_t run_t = tmem_base + ((q * 32) << 16) + BN + col_off;
+            const uint32_t nchunks = (tile_kb(ti.tag) + chunk_kb - 1) / chunk_kb;
+            if (nchunks == 0) {
+                // an empty slice-K group: C_g (and its accumulators) are zero
+                uint32_t z[32];
+#pragma unroll
+                for (uint32_t j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll 1
+                for (uint32_t cc = 0; rows_valid && cc < kCols / 32 && cc * 32 < n_act; ++cc) {
+                    store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(n0 + cc * 32) * csize,
+                                          ldc * csize, rows_valid, min(32u, n_act - cc * 32), z, lane);
+                    if (EPI == kEpiDequant && acc_out) {
+                        uint8_t* awarp = reinterpret_cast<uint8_t*>(
+                            acc_out + cbase + static_cast<int64_t>(ti.row0 + wrow) * ldc + n0 + cc * 32);
+                        store_chunk_coalesced(epi_stage, kOutS32, acc_vec, awarp, ldc * 4, rows_valid,
+                                              min(32u, n_act - cc * 32), z, lane);
+                    }
+                }
+                continue;
+            }
             for (uint32_t c = 0; c < nchunks; ++c) {
                 if (!warp_wait(&tfull[acc], acc_phase, ctl, 4)) { ok = false; break; }
                 tc_fence_after();
@@ -331,7 +372,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                 // acc * scale_a[row] * scale_b[col] in fp32, rounded once to bf16
                 tc_fence_after();
                 const uint32_t grow = ti.row0 + wrow + lane;
-                const float sa_row = lane < rows_valid ? scale_a[grow] : 0.f;
+                // slice-K: this group's row scales (sa_group_stride 0 otherwise)
+                const float sa_row =
+                    lane < rows_valid ? scale_a[static_cast<int64_t>(ti.tag) * prm.g.sa_group_stride + grow] : 0.f;
                 // grouped: this group's column scales (tag = group; 0 for plain problems)
                 const float* sb_row = scale_b + static_cast<int64_t>(ti.tag) * prm.g.sb_group_stride;
 #pragma unroll 1
@@ -349,7 +392,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                     store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(col0) * csize,
                                           ldc * csize, rows_valid, nv, v, lane);
                     if (acc_out) {
-                        uint8_t* awarp = reinterpret_cast<uint8_t*>(acc_out + static_cast<int64_t>(ti.row0 + wrow) * ldc + col0);
+                        uint8_t* awarp = reinterpret_cast<uint8_t*>(acc_out + cbase + static_cast<int64_t>(ti.row0 + wrow) * ldc + col0);
                         store_chunk_coalesced(epi_stage, kOutS32, acc_vec, awarp, ldc * 4, rows_valid, nv, r, lane);
                     }
                 }

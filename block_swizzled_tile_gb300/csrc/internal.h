@@ -95,6 +95,15 @@ cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* ds
                                  int64_t cols, uint32_t sms, cudaStream_t stream, int64_t batch = 1,
                                  int64_t bs_src = 0, int64_t bs_dst = 0);
 
+// grouped slice-K: per-group tensor maps (G x 256 bytes at `maps`) and
+// k-block counts plus a status word (G + 1 words at `group_kb`), from the
+// whole-operand maps; a_kstep / b_kstep are the bytes between consecutive K
+// indices and a_kdim / b_kdim the map dimension along K
+cudaError_t launch_slice_k_prep(const CUtensorMap& tmpl_a, const CUtensorMap& tmpl_b, const int32_t* group_k,
+                                uint32_t G, uint64_t total_k, const void* a, uint64_t a_kstep, uint32_t a_kdim,
+                                const void* b, uint64_t b_kstep, uint32_t b_kdim, uint8_t* maps, uint32_t* group_kb,
+                                uint32_t* err, cudaStream_t stream);
+
 // zero an [rows, cols] row-major output of `esize`-byte elements, `batch`
 // times at `batch_stride` elements apart
 cudaError_t launch_zero_fill(uint8_t* C, int64_t ldc, int64_t batch_stride, int64_t rows, int64_t cols,

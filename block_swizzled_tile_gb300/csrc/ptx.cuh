@@ -156,6 +156,27 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Tensor maps rewritten on the device (grouped slice-K: one map per group,
+// its base moved to the group's first K element and its K extent cut to the
+// group's size, so TMA fills the group's ragged last k-block with zeros).
+// The map lives in global memory; the writer releases it to the tensor-map
+// proxy and every thread that issues copies with it acquires it first.
+__device__ __forceinline__ void tmap_replace_address(void* gmap, uint64_t addr) {
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(gmap), "l"(addr) : "memory");
+}
+template <int ORD>
+__device__ __forceinline__ void tmap_replace_dim(void* gmap, uint32_t extent) {
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], %1, %2;" ::"l"(gmap), "n"(ORD),
+                 "r"(extent)
+                 : "memory");
+}
+__device__ __forceinline__ void tmap_release() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void tmap_acquire(const void* gmap) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(gmap) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(

@@ -178,3 +178,19 @@ def grouped_slice_k_bf16(group_k=None, G=8, total_k=8192, M=4096, N=4096, seed=0
     total = sum(group_k)
     return dict(kind="slice_k", dtype="bf16", group_k=group_k, G=len(group_k), M=M, N=N,
                 x=normal16((total, M), 1.0, "bf16", g), dy=normal16((total, N), 1.0, "bf16", g))
+
+
+def grouped_slice_k_int8(group_k=None, G=8, total_k=8192, M=4096, N=4096, seed=0):
+    """Grouped slice-K int8 with per-token dequant: the group sizes of the
+    slice-K workload, the value distributions of the int8 one.  a is the
+    logical A [M, sum K_g] and b the logical B [sum K_g, N] (U{-127..127});
+    sa [G, M] and sb [G, N] hold each group's row and column scales."""
+    g = _gen(seed)
+    if group_k is None:
+        group_k = multinomial_groups(total_k, G, g)
+    group_k = [int(v) for v in group_k]
+    total = sum(group_k)
+    G = len(group_k)
+    return dict(kind="slice_k_int8", group_k=group_k, G=G, M=M, N=N,
+                a=uniform_int8((M, total), g), b=uniform_int8((total, N), g),
+                sa=uniform_f32((G, M), 1e-3, 1e-2, g), sb=uniform_f32((G, N), 1e-3, 1e-2, g))

@@ -230,6 +230,80 @@ bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, i
                                             const bst_sched* sched, void* stream);
 
 /*
+ * bst_gemm_grouped_slice_k -- grouped GEMM with groups along K ("Block
+ * Dispatch Policies", 05_grouped_matmul_slice_k).  Group g owns the K_g
+ * consecutive K indices [off_g, off_g + K_g) of A and B, off_g = K_0 + ... +
+ * K_{g-1}, and produces its own output matrix:
+ *
+ *   C_g = A[:, off_g : off_g + K_g] . B[off_g : off_g + K_g, :]      ([M, N])
+ *
+ * (e.g. a weight gradient X_g^T . dY_g whose groups are runs of tokens).
+ * group_k  DEVICE int32[G], 1 <= G <= 1024.  Zero-size groups give C_g = 0.
+ *          The kernel checks the sizes (none negative, sum <= total_k, and,
+ *          where an operand is K-contiguous, every non-empty group starting
+ *          on a 16-byte boundary: off_g a multiple of 8); otherwise nothing is
+ *          written and bst_check_async reports BST_ERR_DEVICE.  K indices past
+ *          the sum are not read.
+ * A        logical [M, total_k]; a_layout BST_ROW_MAJOR: stored [M, total_k]
+ *          (K contiguous); BST_COL_MAJOR: stored [total_k, M] (M contiguous,
+ *          the layout of X in X^T . dY).  Leading dimension lda.
+ * B        logical [total_k, N]; BST_ROW_MAJOR: stored [total_k, N] (N
+ *          contiguous); BST_COL_MAJOR: stored [N, total_k].  Leading dim ldb.
+ * C        G row-major [M, N] matrices (ldc), C_g at C + g*stride_c elements
+ *          (stride_c >= M*ldc when G > 1).
+ * dtype    ab_type BST_F16 or BST_BF16; c_type BST_F16, BST_BF16 or BST_F32.
+ * workspace DEVICE scratch of bst_gemm_grouped_slice_k_workspace_size(G)
+ *          bytes, 256-byte aligned, caller-owned: per group a copy of each
+ *          operand's TMA map rewritten on the device (base at off_g, K extent
+ *          K_g, so a group's ragged last k-block reads zeros), and the
+ *          groups' k-block counts.
+ * Runs on 256 x 256 or 256 x 128 CTA-pair tiles; tasks are numbered
+ * group-major (task t belongs to group t / (loopsM*loopsN), as batches are in
+ * "Block Scheduler Code Explained" section 4.4) with the swizzle of every
+ * group over the same M x N grid.  Operands must be TMA-addressable (16-byte
+ * aligned base and leading dimension), else BST_ERR_ALIGNMENT.  total_k = 0:
+ * every C_g is zeroed.
+ */
+size_t bst_gemm_grouped_slice_k_workspace_size(int32_t G);
+
+bst_status bst_gemm_grouped_slice_k(int32_t G, const int32_t* group_k, int64_t M, int64_t N, int64_t total_k,
+                                    const void* A, bst_layout a_layout, int64_t lda,
+                                    const void* B, bst_layout b_layout, int64_t ldb,
+                                    void* C, int64_t ldc, int64_t stride_c,
+                                    bst_dtype ab_type, bst_dtype c_type,
+                                    void* workspace, size_t workspace_bytes,
+                                    const bst_sched* sched, void* stream);
+
+/*
+ * bst_gemm_grouped_slice_k_quant_per_token -- the K slices of
+ * bst_gemm_grouped_slice_k on int8 operands, each group dequantised with its
+ * own scales ("Block Dispatch Policies",
+ * 11_grouped_matmul_slice_k_per_token_dequant):
+ *
+ *   acc_g[i,j] = sum over k in slice g of A[i,k] * B[k,j]     exactly, int32
+ *   C_g[i,j]   = bf16( acc_g[i,j] * scale_a[g*stride_sa + i] * scale_b[g*stride_sb + j] )
+ *
+ * scale_a fp32 [G, M] (row stride stride_sa; 0 shares one row of scales),
+ * scale_b fp32 [G, N] (stride_sb).  A, B, group_k and the layouts as for
+ * bst_gemm_grouped_slice_k (int8 elements).  C bf16, acc_out optional int32,
+ * both G x [M, N] with ldc and stride_c.  workspace: DEVICE scratch of
+ * bst_gemm_grouped_slice_k_quant_per_token_workspace_size(G, M, N, total_k)
+ * bytes, 256-byte aligned: the per-group maps plus A and B widened to bf16,
+ * multiplied exactly as bst_gemm_quant_per_token does on 256 x 256 pairs.
+ */
+size_t bst_gemm_grouped_slice_k_quant_per_token_workspace_size(int32_t G, int64_t M, int64_t N, int64_t total_k);
+
+bst_status bst_gemm_grouped_slice_k_quant_per_token(int32_t G, const int32_t* group_k, int64_t M, int64_t N,
+                                                    int64_t total_k,
+                                                    const int8_t* A, bst_layout a_layout, int64_t lda,
+                                                    const int8_t* B, bst_layout b_layout, int64_t ldb,
+                                                    const float* scale_a, int64_t stride_sa,
+                                                    const float* scale_b, int64_t stride_sb,
+                                                    void* C, int64_t ldc, int64_t stride_c, int32_t* acc_out,
+                                                    void* workspace, size_t workspace_bytes,
+                                                    const bst_sched* sched, void* stream);
+
+/*
  * bst_gemm_quant_per_token_noalloc -- the same int8 GEMM with per-token
  * dequant as bst_gemm_quant_per_token (same arguments, results and errors),
  * for callers that cannot allocate device memory at the point of the call:

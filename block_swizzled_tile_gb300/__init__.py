@@ -40,12 +40,14 @@ class Sched(ctypes.Structure):
     _fields_ = [("swizzle_offset", ctypes.c_uint32), ("swizzle_direction", ctypes.c_uint32),
                 ("tile_n", ctypes.c_uint32), ("tile_m", ctypes.c_uint32), ("num_ctas", ctypes.c_uint32),
                 ("split_k", ctypes.c_uint32),
-                ("trace", ctypes.c_void_p), ("timeline", ctypes.c_void_p)]
+                ("trace", ctypes.c_void_p), ("timeline", ctypes.c_void_p),
+                ("shuffle_k", ctypes.c_uint32), ("dynamic", ctypes.c_uint32)]
 
 
 def sched(swizzle_offset=1, swizzle_direction=0, tile_n=0, num_ctas=0, trace=None, timeline=None, tile_m=0,
-          split_k=0):
-    return Sched(swizzle_offset, swizzle_direction, tile_n, tile_m, num_ctas, split_k, _ptr(trace), _ptr(timeline))
+          split_k=0, shuffle_k=0, dynamic=0):
+    return Sched(swizzle_offset, swizzle_direction, tile_n, tile_m, num_ctas, split_k, _ptr(trace), _ptr(timeline),
+                 shuffle_k, dynamic)
 
 
 _lib = None

@@ -94,7 +94,7 @@ bool out_code(bst_dtype t, uint32_t& code) {
 uint64_t timeout_ns() { return t_timeout_ns ? t_timeout_ns : kDefaultTimeoutNs; }
 
 struct Sched {
-    uint32_t offset = 1, dir = 0, tile_n = 0, tile_m = 0, num_ctas = 0, split_k = 0;
+    uint32_t offset = 1, dir = 0, tile_n = 0, tile_m = 0, num_ctas = 0, split_k = 0, shuffle_k = 0, dynamic = 0;
     uint32_t* trace = nullptr;
     uint64_t* timeline = nullptr;
 };
@@ -105,15 +105,29 @@ bst_status read_sched(const bst_sched* s, Sched& out) {
     if (s->tile_n != 0 && s->tile_n != 64 && s->tile_n != 128 && s->tile_n != 256) return BST_ERR_INVALID_ARG;
     if (s->tile_m != 0 && s->tile_m != 128 && s->tile_m != 256) return BST_ERR_INVALID_ARG;
     if (s->split_k > 4 || s->split_k == 3) return BST_ERR_INVALID_ARG;
+    if (s->shuffle_k > 1 || s->dynamic > 1) return BST_ERR_INVALID_ARG;
+    if (s->dynamic && s->num_ctas) return BST_ERR_INVALID_ARG;            // the grid is one cluster per task
+    if ((s->dynamic || s->shuffle_k) && s->split_k >= 2) return BST_ERR_UNSUPPORTED;
+    if (s->dynamic && s->tile_m == 128) return BST_ERR_UNSUPPORTED;        // CTA-pair tiles only
+    out.shuffle_k = s->shuffle_k;
+    out.dynamic = s->dynamic;
     out.offset = s->swizzle_offset;
     out.dir = s->swizzle_direction;
     out.tile_n = s->tile_n;
-    out.tile_m = s->tile_m;
+    out.tile_m = s->dynamic ? 256u : s->tile_m;
     out.split_k = s->split_k;
     out.num_ctas = s->num_ctas;
     out.trace = s->trace;
     out.timeline = s->timeline;
     return BST_OK;
+}
+
+// CTA pairs to launch: a persistent grid of at most one pair per two SMs (or
+// num_ctas / 2), or -- with dynamic tasks -- one cluster per task.
+uint32_t pair_grid(const Sched& sch, uint64_t tiles, uint32_t sms) {
+    if (sch.dynamic) return static_cast<uint32_t>(std::max<uint64_t>(1, tiles));
+    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : sms;
+    return static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles));
 }
 
 // Operand of a GEMM as the kernel sees it: which index is contiguous, and
@@ -278,7 +292,7 @@ struct SplitChoice {
 
 SplitChoice choose_splits(const Sched& sch, bool eligible, uint64_t M, uint64_t N, uint32_t num_kb, uint32_t sms) {
     SplitChoice none;
-    if (sch.split_k == 1) return none;
+    if (sch.split_k == 1 || sch.dynamic || sch.shuffle_k) return none;
     const bool forced = sch.split_k >= 2;
     const bool bn_ok = sch.tile_n == 0 || sch.tile_n == 128 || sch.tile_n == 256;
     if (!eligible || (sch.tile_m && sch.tile_m != 256) || !bn_ok) {
@@ -407,11 +421,13 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.trace_cap = static_cast<uint32_t>(tiles);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    p.g.dynamic = sch.dynamic;
+    p.g.shuffle_k = sch.shuffle_k;
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (splits > 1) return cuda_status(launch_pair_splitk(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     if (pair)
-        return cuda_status(launch_pair(p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
+        return cuda_status(launch_pair(p, bn, pair_grid(sch, tiles, dev.sms),
                                        stream));
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_dense(p, bn, grid, stream));
@@ -468,6 +484,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     if (!out_code(ct, c_code)) return BST_ERR_UNSUPPORTED;
     Sched sch;
     if (bst_status s = read_sched(sched_in, sch)) return s;
+    if (sch.dynamic || sch.shuffle_k) return BST_ERR_UNSUPPORTED;   // one-CTA MXFP8 tiles, fixed K order
     if (la != BST_ROW_MAJOR || lb != BST_COL_MAJOR) return BST_ERR_UNSUPPORTED;
     if (K % 128) return BST_ERR_UNSUPPORTED;
     if (sch.tile_n == 64 || sch.tile_m == 256) return BST_ERR_UNSUPPORTED;
@@ -538,6 +555,8 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.trace_cap = static_cast<uint32_t>(tiles);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    p.g.dynamic = sch.dynamic;
+    p.g.shuffle_k = sch.shuffle_k;
     set_prefetch(p.g, a, b, sfa, static_cast<uint64_t>(M) * (K / 32), sfb, static_cast<uint64_t>(N) * (K / 32));
     if (splits > 1) return cuda_status(launch_mxf8_split(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
@@ -546,6 +565,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
 }
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
 
 }  // namespace
 }  // namespace bst
@@ -631,8 +651,9 @@ bst_status run_slice_k(const SliceKRun& r, int32_t G, const int32_t* group_k, in
     p.g.trace_cap = static_cast<uint32_t>(tiles);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
-    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
-    const uint32_t pairs = static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles));
+    p.g.dynamic = sch.dynamic;
+    p.g.shuffle_k = sch.shuffle_k;
+    const uint32_t pairs = pair_grid(sch, tiles, dev.sms);
     return cuda_status(r.dequant ? launch_pair_dequant(p, pairs, stream) : launch_pair(p, bn, pairs, stream));
 }
 
@@ -725,11 +746,13 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
     p.g.trace_cap = static_cast<uint32_t>(tiles_bound);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    p.g.dynamic = sch.dynamic;
+    p.g.shuffle_k = sch.shuffle_k;
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (pair)
         return cuda_status(launch_pair(
-            p, bn, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles_bound)), stream));
+            p, bn, pair_grid(sch, tiles_bound, dev.sms), stream));
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles_bound));
     return cuda_status(launch_dense(p, bn, grid, stream));
 }
@@ -824,9 +847,11 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     p.g.trace_cap = static_cast<uint32_t>(tiles);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
+    p.g.dynamic = sch.dynamic;
+    p.g.shuffle_k = sch.shuffle_k;
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (pair)
-        return cuda_status(launch_pair_dequant(p, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles)),
+        return cuda_status(launch_pair_dequant(p, pair_grid(sch, tiles, dev.sms),
                                                stream));
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_dequant(p, grid, stream));
@@ -923,9 +948,9 @@ bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, i
     p.g.trace_cap = static_cast<uint32_t>(tiles_bound);
     p.g.err = dev.err;
     p.g.timeout_ns = timeout_ns();
-    const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
-    return cuda_status(
-        launch_pair_dequant(p, static_cast<uint32_t>(std::min<uint64_t>(std::max(1u, ctas / 2), tiles_bound)), stream));
+    p.g.dynamic = sch.dynamic;
+    p.g.shuffle_k = sch.shuffle_k;
+    return cuda_status(launch_pair_dequant(p, pair_grid(sch, tiles_bound, dev.sms), stream));
 }
 
 size_t bst_gemm_grouped_slice_k_workspace_size(int32_t G) {

@@ -97,6 +97,8 @@ struct GemmArgs {
     int64_t sa_group_stride;   // slice-K dequant: elements between the groups' scale_a rows
     const uint8_t* kmaps;      // slice-K: per group 256 bytes, the A then the B tensor map
     const uint32_t* group_kb;  // slice-K: k-blocks of each group, then a status word (non-zero: bad sizes)
+    uint32_t dynamic;          // CTA-pair kernels: tasks claimed through cluster launch control
+    uint32_t shuffle_k;        // each tile starts its K loop at k-block (task % k-blocks)
     int32_t* acc_out;
     const uint8_t* sfa;
     const uint8_t* sfb;
@@ -605,6 +607,15 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         kb_hi = min(num_kb, ((split + 1) * units / SPLIT) * gran);
     }
     const bool has_k = kb_hi > kb_lo;
+    // ShuffleK (fp16/bf16): task t's K loop starts at k-block kb_lo + t % (kb_hi - kb_lo)
+    const uint32_t nk_span = kb_hi - kb_lo;
+    auto shuffle_rot = [&](uint32_t t) -> uint32_t {
+        return (KIND == kKindF16 && prm.g.shuffle_k && nk_span) ? t % nk_span : 0u;
+    };
+    auto shuffled = [&](uint32_t kb, uint32_t rot) -> uint32_t {
+        const uint32_t kx = kb + rot;
+        return kx < kb_hi ? kx : kx - nk_span;
+    };
     bool acc_ok = true;                                  // split-K: this CTA's partial is complete
 
     constexpr uint32_t kBWarp = b_warp_for<KIND>();
@@ -651,10 +662,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     const CUtensorMap* map = is_a ? &prm.tmap_a : &prm.tmap_b;
                     const uint32_t dst_off = is_a ? 0u : Lay::kABytes;
                     const int32_t row = is_a ? static_cast<int32_t>(ti.row0) : static_cast<int32_t>(n0);
+                    const uint32_t rot = shuffle_rot(t);
                     for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                         uint8_t* st = smem + stage * Lay::kStageBytes;
-                        const int32_t k0 = static_cast<int32_t>(kb * bk_elems);
+                        const int32_t k0 = static_cast<int32_t>(shuffled(kb, rot) * bk_elems);
                         if (is_a) mbar_arrive_expect_tx(&full[stage], tx);
                         tma_load_2d(st + dst_off, map, &full[stage], k0, row);
                         if (tl && is_a && issued < 15) tl[1 + issued] = globaltimer_ns();
@@ -663,10 +675,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     }
                     continue;
                 }
+                const uint32_t rot = shuffle_rot(t);
                 for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
-                    const uint32_t k0 = kb * bk_elems;
+                    const uint32_t k0 = shuffled(kb, rot) * bk_elems;
                     if (is_a) {
                         mbar_arrive_expect_tx(&full[stage], tx);
                         tma_tile(&prm.tmap_a, sa_s, &full[stage], a_mn, a_rank3, ti.row0, kBM, k0, zc, bk_elems);
@@ -757,11 +770,12 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 const TileInfo ti = tile_info(sa, t, kBM, BN, gt);
                 const uint32_t n0 = ti.n * BN;
                 const int32_t zc = static_cast<int32_t>(ti.tag);
+                const uint32_t rot = shuffle_rot(t);
                 for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     uint8_t* sb_s = sa_s + Lay::kABytes;
-                    const uint32_t k0 = kb * bk_elems;
+                    const uint32_t k0 = shuffled(kb, rot) * bk_elems;
                     if (KIND == kKindMXF8) {
                         // scale factors for this k-block, written straight into the
                         // order tcgen05.cp 32x128b.warpx4 expects: 16-byte line r%32

@@ -35,7 +35,11 @@ static cudaError_t launch_pair_one(const GemmParams& p, uint32_t max_pairs, cuda
         if (n <= 0) return cudaErrorInvalidConfiguration;
         resident[dev & 63].store(n);
     }
-    const uint32_t pairs = std::max(1u, std::min(max_pairs, static_cast<uint32_t>(n)));
+    // dynamic tasks: one cluster per task (those that do not fit wait, and the
+    // running ones cancel them to take their tasks); else a persistent grid
+    if (p.g.dynamic && max_pairs > (1u << 30)) return cudaErrorInvalidValue;
+    const uint32_t pairs = p.g.dynamic ? std::max(1u, max_pairs)
+                                       : std::max(1u, std::min(max_pairs, static_cast<uint32_t>(n)));
     cfg.gridDim = dim3(2 * pairs);
     add_pdl(cfg, attr);
     return cudaLaunchKernelEx(&cfg, kern, p);

@@ -44,6 +44,61 @@ constexpr uint32_t pair_threads() { return EPI == kEpiDequant ? 352u : kPairThre
 template <uint32_t EPI>
 constexpr uint32_t pair_epi_warps() { return EPI == kEpiDequant ? 8u : 4u; }
 
+// Depth of the ring of cluster-launch-control responses (dynamic tasks).
+constexpr uint32_t kClcDepth = 4;
+
+// The task sequence of one role of a CTA pair.
+//   Static: t = cid, cid + nclusters, ... (a persistent grid).
+//   Dynamic (the "dynamic task allocation" that "Block Scheduler Code
+//   Explained" lists among the scheduler's policies): the grid holds one
+//   cluster per task.  A cluster starts with its own task and then takes the
+//   tasks of clusters that have not started yet, which the leader's A-load
+//   thread cancels one at a time through cluster launch control.  Each
+//   response lands in a ring of kClcDepth slots in both CTAs; every other
+//   role reads it and frees the slot on the leader, so the claims run at most
+//   kClcDepth tasks ahead of the slowest role.  A response that cancelled
+//   nothing (or a task past the end) ends every role's sequence at the same
+//   point, and no request follows it.
+struct PairTasks {
+    uint32_t total, step;       // step: nclusters (static) or 0 (dynamic)
+    uint4* resp;                // [kClcDepth] responses, this CTA
+    uint64_t* full;             // [kClcDepth] response barriers, this CTA
+    uint64_t* empty;            // [kClcDepth] slot-free barriers (the leader's are used)
+    uint32_t empty_leader;      // cluster address of the leader's empty[0]
+    uint32_t peer_full;         // cluster address of the peer's full[0]
+    uint32_t i;                 // responses read
+    bool pending;               // issuer: a request whose response is unread
+
+    // issuer only: claim the next not-yet-started cluster into slot i
+    __device__ __forceinline__ bool request(const WaitCtl& ctl) {
+        const uint32_t s = i % kClcDepth, ph = (i / kClcDepth) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, ctl, 9)) return false;
+        mbar_arrive_expect_tx(&full[s], 16);
+        mbar_arrive_expect_tx_cluster_relaxed(peer_full + s * 8, 16);
+        clc_try_cancel_multicast(&resp[s], &full[s]);
+        pending = true;
+        return true;
+    }
+    // the task after t (total: none).  role 0: the issuer; 1: a consumer
+    // thread; 2: a consumer warp (all lanes call it)
+    __device__ __forceinline__ uint32_t next(uint32_t t, bool& ok, uint32_t role, const WaitCtl& ctl) {
+        if (step) return t + step;
+        const uint32_t s = i % kClcDepth, ph = (i / kClcDepth) & 1u;
+        const bool got = role == 2 ? warp_wait(&full[s], ph, ctl, 10) : mbar_wait(&full[s], ph, ctl, 10);
+        if (!got) { ok = false; return total; }
+        const uint32_t x = clc_cancelled_ctaid_x(&resp[s]);
+        const uint32_t nt = x == 0xFFFFFFFFu ? total : min(x >> 1, total);
+        ++i;
+        if (role == 0) {
+            pending = false;
+            if (nt < total && !request(ctl)) { ok = false; return total; }
+        } else if (role == 1 || (threadIdx.x & 31u) == 0) {
+            mbar_arrive_cluster_relaxed(empty_leader + s * 8);
+        }
+        return nt;
+    }
+};
+
 // Dequant: one fp32 accumulator (the current K-chunk) in TMEM columns
 // [0, BN) and the exact int32 running sums in [BN, 2*BN); otherwise two fp32
 // accumulators, so the epilogue of one tile overlaps the MMAs of the next.
@@ -56,9 +111,11 @@ struct PairLayout {
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kEpiOff = STAGES * kStageBytes;             // epilogue warps x 4 KB staging
     static constexpr uint32_t kBarOff = kEpiOff + EPI_WARPS * kEpiWarpBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * kACC + 1;
+    // full, empty, tfull, tempty, drain, then the task ring's full and empty
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * kACC + 1 + 2 * kClcDepth;
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
+    static constexpr uint32_t kClcOff = (kMiscOff + 16 + 15) & ~15u;      // kClcDepth x 16-byte responses
+    static constexpr uint32_t kTableOff = kClcOff + 16 * kClcDepth;
     static constexpr uint32_t kTmemCols = EPI == kEpiDequant ? 512 : (kACC * BN <= 256 ? 256 : 512);
     static_assert(kACC * BN <= 512 && (EPI == kEpiStore || BN == 256), "TMEM budget");
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -90,6 +147,8 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = bars + 2 * STAGES + ACC;
     uint64_t* drain = bars + 2 * STAGES + 2 * ACC;
+    uint64_t* clc_full = drain + 1;
+    uint64_t* clc_empty = clc_full + kClcDepth;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     uint32_t* tmem_holder = misc;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -119,6 +178,12 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
             mbar_init(&tempty[a], 2 * pair_epi_warps<EPI>());   // one arrival per epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
+        for (uint32_t j = 0; j < kClcDepth; ++j) {
+            mbar_init(&clc_full[j], 1);
+            // every role but the issuer, in both CTAs: A (peer), B (both),
+            // MMA, epilogue warps (both)
+            mbar_init(&clc_empty[j], 4 + 2 * pair_epi_warps<EPI>());
+        }
         *abort_flag = 0;
         *tiles_smem = prm.g.total_tiles;
         fence_barrier_init();
@@ -150,6 +215,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
     const uint32_t total_tiles = *tiles_smem;
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     if (tl && threadIdx.x == 0) tl[0] = globaltimer_ns();
+    const bool dyn = prm.g.dynamic != 0;
+    PairTasks tasks{total_tiles, dyn ? 0u : nclusters, reinterpret_cast<uint4*>(smem + Lay::kClcOff), clc_full,
+                    clc_empty, map_to_cta(smem_u32(clc_empty), 0), map_to_cta(smem_u32(clc_full), 1), 0, false};
 
     if (warp == 0 || warp == kPairBWarp) {
         // ------------------------------------------------------ producer --
@@ -164,7 +232,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
         const CUtensorMap* map_b = &prm.tmap_b;
         // single threads issue the loads (cheaper per k-block than a
         // warp-wide loop with one active lane)
-        for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t += nclusters) {
+        const uint32_t role = (rank == 0 && is_a) ? 0u : 1u;
+        if (lane == 0 && dyn && role == 0 && cid < total_tiles) ok = tasks.request(ctl);
+        for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t = tasks.next(t, ok, role, ctl)) {
             const TileInfo ti = tile_info(sa, t, TM, BN, gt);
             const uint32_t a_row = ti.row0 + rank * kBM;
             const uint32_t b_col = ti.n * BN + rank * BH;
@@ -179,13 +249,16 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                 tmap_acquire(is_a ? gm : gm + 128);
                 map_group = ti.tag;
             }
+            // ShuffleK: the K loop of task t starts at k-block t % tkb
+            const uint32_t rot = (prm.g.shuffle_k && tkb) ? t % tkb : 0u;
             for (uint32_t kb = 0; kb < tkb; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                 {
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     uint8_t* sb_s = sa_s + Lay::kABytes;
                     const uint32_t bar = full_leader + stage * 8;
-                    const int32_t k0 = kb * bk_elems;
+                    const uint32_t kx = kb + rot;
+                    const int32_t k0 = (kx < tkb ? kx : kx - tkb) * bk_elems;
                     if (is_a) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                         if (!a_mn) {
@@ -212,6 +285,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
+        if (lane == 0 && tasks.pending) {
+            // the issuer gave up with a request in flight: let its response land
+            mbar_wait_drain(&clc_full[tasks.i % kClcDepth], (tasks.i / kClcDepth) & 1u, ctl.timeout_ns);
+        }
         if (lane == 0 && !ok && rank == 0 && is_a) {
             // let the copies of both CTAs already counted here land
             uint32_t s = stage, ph = phase;
@@ -233,7 +310,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
             bool ok = true, any_mma = false;
             const uint32_t chunk_kb = prm.g.chunk_kb;
-            for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t += nclusters) {
+            for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t = tasks.next(t, ok, 1, ctl)) {
               // an empty slice-K group has no MMAs: its epilogue stores zeros
               const uint32_t tkb = mode == kModeSliceK ? tile_kb(tile_info(sa, t, TM, BN, gt).tag) : num_kb;
               const uint32_t nchunks = (tkb + chunk_kb - 1) / chunk_kb;
@@ -295,7 +372,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
         const uint32_t chunk_kb = prm.g.chunk_kb;
         uint32_t acc = 0, acc_phase = 0, ep_tile = 0;
         bool ok = true;
-        for (uint32_t t = cid; ok && t < total_tiles; t += nclusters) {
+        for (uint32_t t = cid; ok && t < total_tiles; t = tasks.next(t, ok, 2, ctl)) {
             const TileInfo ti = tile_info(sa, t, TM, BN, gt);
             if (trace && rank == 0 && warp == 2 && lane == 0) {
                 if (t < trace_cap) {

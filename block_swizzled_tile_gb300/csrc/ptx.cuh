@@ -401,6 +401,47 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_a
                  : "memory");
 }
 
+// Remote arrivals that publish no data (the arriving thread has only read
+// shared memory the barrier guards): relaxed, so the arrival does not wait
+// for the thread's earlier memory operations to become visible cluster-wide.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster_relaxed(uint32_t cluster_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Cluster launch control: asks the hardware to cancel a cluster of this grid
+// that has not started yet.  The 16-byte response is written to `resp` in
+// every CTA of the cluster and counted (16 bytes) on the barrier at the same
+// offset in each.  No request may follow one whose response said "none".
+__device__ __forceinline__ void clc_try_cancel_multicast(void* resp, uint64_t* bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+        "[%0], [%1];" ::"r"(smem_u32(resp)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The x index of the first CTA of the cluster a response cancelled, or
+// 0xFFFFFFFF when it cancelled none.
+__device__ __forceinline__ uint32_t clc_cancelled_ctaid_x(const void* resp) {
+    uint32_t ok, x = 0xFFFFFFFFu;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "+r"(x)
+        : "r"(smem_u32(resp))
+        : "memory");
+    return ok ? x : 0xFFFFFFFFu;
+}
+
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // an mbarrier of either CTA of the pair (cluster address)
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int32_t x,

@@ -100,6 +100,26 @@ typedef struct {
                                    [32..39] epilogue tile starts, [40..47] epilogue tile
                                    ends, [48..50] producer/MMA/epilogue exit.  Profiling
                                    only.                                               */
+    uint32_t shuffle_k;         /* 1: ShuffleK ("Block Dispatch Policies",
+                                   ENABLE_SHUFFLE_K): the K loop of task t starts at
+                                   k-block t % (k-blocks of the tile) and wraps, so
+                                   tiles running at the same time read different
+                                   k-blocks of a shared operand panel.  Changes only
+                                   the fp32 summation order.  fp16/bf16 and int8
+                                   paths; MXFP8 returns BST_ERR_UNSUPPORTED, and
+                                   split-K is not used with it (split_k >= 2 is
+                                   BST_ERR_UNSUPPORTED).                             */
+    uint32_t dynamic;           /* 1: dynamic task allocation ("Block Scheduler Code
+                                   Explained" section 1): the grid holds one CTA-pair
+                                   cluster per task; a cluster computes its own task,
+                                   then claims the tasks of clusters that have not
+                                   started, by hardware cluster launch control, until
+                                   none is left.  Tasks keep their numbering (the
+                                   trace is unchanged); which CTA runs which task is
+                                   decided at run time.  CTA-pair tiles only
+                                   (tile_m 256 is implied; 128 is
+                                   BST_ERR_UNSUPPORTED); num_ctas must be 0; MXFP8 and
+                                   split_k >= 2 return BST_ERR_UNSUPPORTED.          */
 } bst_sched;
 
 /*

@@ -472,6 +472,9 @@ def main():
     ap.add_argument("--tile-m", type=int, default=0, help="force 128 (one CTA) or 256 (CTA pair); 0 = automatic")
     ap.add_argument("--split-k", type=int, default=0, help="0 automatic, 1 off, 2 or 4 split-K CTA pairs")
     ap.add_argument("--swizzle", default="", help="force the schedule, e.g. Zn3 or Nz1; default: sweep")
+    ap.add_argument("--dynamic", type=int, default=0, choices=[0, 1],
+                    help="1: tasks claimed at run time through cluster launch control (CTA-pair tiles)")
+    ap.add_argument("--shuffle-k", type=int, default=0, choices=[0, 1], help="1: ShuffleK (rotated K start per task)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -501,22 +504,21 @@ def main():
     # swizzle sweep (untimed choice of SwizzleOffset/direction for the line)
     sweep = {}
     tn, tm, sk = args.tile_n, args.tile_m, args.split_k
-    work.sched = work.bst.sched(1, 0, tile_n=tn, tile_m=tm, split_k=sk)
+    opts = dict(tile_n=tn, tile_m=tm, split_k=sk, dynamic=args.dynamic, shuffle_k=args.shuffle_k)
+    work.sched = work.bst.sched(1, 0, **opts)
     if args.swizzle:
-        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, tile_n=tn,
-                                    tile_m=tm, split_k=sk)
+        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, **opts)
     elif not args.lite:
         n = max(8, min(200, args.steps))
         for S in (1, 2, 4, 8):
             for d in (0, 1):
-                work.sched = work.bst.sched(S, d, tile_n=tn, tile_m=tm, split_k=sk)
+                work.sched = work.bst.sched(S, d, **opts)
                 for i in range(3):
                     work.step(i)
                 ms = timed_steps(work, n, stream)
                 sweep["%s%d" % ("Zn" if d == 0 else "Nz", S)] = round(work.flops * n / (ms * 1e-3) / 1e12, 2)
         best = max(sweep, key=sweep.get)
-        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, tile_n=tn, tile_m=tm,
-                                    split_k=sk)
+        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, **opts)
 
     for i in range(args.warmup):
         work.step(i)
@@ -609,6 +611,8 @@ def main():
                             ">" if work.copies * (work.in_bytes + work.out_bytes) > L2_BYTES else "<="),
                    "tile_n": work.sched.tile_n or "auto", "tile_m": work.sched.tile_m or "auto",
                    "split_k": work.sched.split_k or "auto",
+                   "tasks": "dynamic (cluster launch control)" if work.sched.dynamic else "static stride",
+                   "shuffle_k": bool(work.sched.shuffle_k),
                    "launch": "CUDA graphs, one stream", "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": stored_traffic(work.kernel_key),

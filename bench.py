@@ -157,14 +157,25 @@ class Workload:
             self.desc = ("grouped bf16 GEMM slice-K (C_g = X_g^T dY_g), G=%d K sizes %s, M=%d N=%d, A and B "
                          "MN-major, bf16 out" % (len(gk), gk, M, N))
             self.kernel_key = "gemm_slice_k_bf16_%dx%dx%dx%d" % (len(gk), M, N, sum(gk))
+        elif name == "grouped_slice_k_int8":
+            w = wl.grouped_slice_k_int8(seed=seed)
+            self.w = w
+            gk, M, N = w["group_k"], w["M"], w["N"]
+            self.flops = 2.0 * M * N * sum(gk)
+            self.in_bytes = w["a"].nbytes + w["b"].nbytes + w["sa"].nbytes + w["sb"].nbytes
+            self.out_bytes = len(gk) * M * N * 2
+            self.dtype = "s8"
+            self.desc = ("grouped int8 GEMM slice-K with per-token dequant, G=%d K sizes %s, M=%d N=%d, A^T [K,M] "
+                         "and B [K,N] (MN-contiguous), int32 accumulate, bf16 out" % (len(gk), gk, M, N))
+            self.kernel_key = "gemm_slice_k_int8_%dx%dx%dx%d" % (len(gk), M, N, sum(gk))
         else:
             raise SystemExit("unknown workload " + name)
         per_set = self.in_bytes + self.out_bytes
         # enough copies that the bytes between two uses of one copy exceed L2
         self.copies = copies or max(1, min(4096, math.ceil(2 * L2_BYTES / per_set)))
         self.sched = bst.sched(1, 0)
-        self.launches_per_step = (3 if name in ("int8_per_token", "grouped_int8_per_token") else
-                                  2 if name == "grouped_slice_k_bf16" else 1)
+        self.launches_per_step = {"int8_per_token": 3, "grouped_int8_per_token": 3, "grouped_slice_k_bf16": 2,
+                                  "grouped_slice_k_int8": 4}.get(name, 1)
         self._alloc()
 
     def _alloc(self):
@@ -203,6 +214,16 @@ class Workload:
                 nb = self.bst.gemm_grouped_slice_k_workspace_size(len(gk))
                 s["WS"] = torch.empty(nb, dtype=torch.uint8, device="cuda")
                 s["WSB"] = nb
+            elif self.name == "grouped_slice_k_int8":
+                gk = w["group_k"]
+                # the weight-gradient layout: A^T [sum K, M] and B [sum K, N] (any group sizes)
+                s["A"], s["B"] = to_dev(np.ascontiguousarray(w["a"].T)), to_dev(w["b"])
+                s["SA"], s["SB"] = to_dev(w["sa"]), to_dev(w["sb"])
+                s["G"] = torch.tensor(gk, dtype=torch.int32, device="cuda")
+                s["C"] = torch.empty(len(gk) * w["M"] * w["N"], dtype=torch.int16, device="cuda")
+                nb = self.bst.gemm_grouped_slice_k_quant_per_token_workspace_size(len(gk), w["M"], w["N"], sum(gk))
+                s["WS"] = torch.empty(nb, dtype=torch.uint8, device="cuda")
+                s["WSB"] = nb
             else:
                 s["A"], s["B"] = to_dev(w["a"]), to_dev(w["b"])
                 s["SA"], s["SB"] = to_dev(w["sa"]), to_dev(w["sb"])
@@ -235,6 +256,12 @@ class Workload:
             gk, M, N = w["group_k"], w["M"], w["N"]
             bst.gemm_grouped_slice_k(len(gk), s["G"], M, N, sum(gk), s["X"], bst.COL_MAJOR, M, s["DY"], bst.ROW_MAJOR,
                                      N, s["C"], N, M * N, bst.BF16, bst.BF16, s["WS"], s["WSB"], sched=sched)
+        elif self.name == "grouped_slice_k_int8":
+            gk, M, N = w["group_k"], w["M"], w["N"]
+            K = sum(gk)
+            bst.gemm_grouped_slice_k_quant_per_token(len(gk), s["G"], M, N, K, s["A"], bst.COL_MAJOR, M, s["B"],
+                                                     bst.ROW_MAJOR, N, s["SA"], M, s["SB"], N, s["C"], N, M * N,
+                                                     None, s["WS"], s["WSB"], sched=sched)
         else:
             bst.gemm_quant_per_token(w["M"], w["N"], w["K"], s["A"], w["K"], s["B"], bst.COL_MAJOR, w["K"],
                                      s["SA"], s["SB"], s["C"], w["N"], None, s["WS"], s["WSB"], sched=sched)
@@ -380,6 +407,10 @@ def oracle_rows(work, rows):
         a = og.decode(np.ascontiguousarray(w["x"][:, :take].T), "bf16")
         og.gemm_grouped_slice_k(a, og.decode(w["dy"], "bf16"), w["group_k"], "bf16")
         return 2.0 * take * w["N"] * sum(w["group_k"])
+    if work.name == "grouped_slice_k_int8":
+        take = min(rows, w["M"])
+        og.gemm_grouped_slice_k_quant_per_token(w["a"][:take], w["b"], w["group_k"], w["sa"][:, :take], w["sb"])
+        return 2.0 * take * w["N"] * sum(w["group_k"])
     if work.name == "grouped_int8_per_token":
         gm = w["group_m"]
         g = next(i for i, m in enumerate(gm) if m)
@@ -426,7 +457,8 @@ def reference_arm(args, work_name):
     work.w = {"fp16_square": wl.fp16_square, "fp16_tail": wl.fp16_tail, "mxfp8": wl.mxfp8,
               "grouped_bf16": wl.grouped_bf16, "int8_per_token": wl.int8_per_token,
               "grouped_int8_per_token": wl.grouped_int8_per_token,
-              "grouped_slice_k_bf16": wl.grouped_slice_k_bf16}[work_name]()
+              "grouped_slice_k_bf16": wl.grouped_slice_k_bf16,
+              "grouped_slice_k_int8": wl.grouped_slice_k_int8}[work_name]()
     desc = {"fp16_square": "fp16 GEMM M=1024 N=1024 K=2048, A row-major, B col-major, fp32 accumulate, fp16 out"}
     # size the per-step sample so that warmup + steps take about two minutes
     budget = min(20.0, 120.0 / max(1, args.steps + args.warmup))
@@ -465,7 +497,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="fp16_square",
                     choices=["fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token",
-                             "grouped_int8_per_token", "grouped_slice_k_bf16"])
+                             "grouped_int8_per_token", "grouped_slice_k_bf16", "grouped_slice_k_int8"])
     ap.add_argument("--lite", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.0)
     ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (64/128/256); 0 = automatic")
@@ -581,9 +613,9 @@ def main():
     if rank != 0:
         return
     peaks, src = measured_peaks()
-    # int8 steps are three launches (two widenings and the GEMM) and slice-K
-    # steps two (the per-group map set-up and the GEMM) inside one C-ABI
-    # call: their roofline covers the whole step, not the GEMM alone
+    # int8 steps are three launches (two widenings and the GEMM), slice-K
+    # steps two (the per-group map set-up and the GEMM) and int8 slice-K four,
+    # inside one C-ABI call: their roofline covers the whole step
     per_launch_ms = ms / args.steps
     value = whole_job_tflops(world, work.flops, args.steps, ms)
     # the sustained cuBLAS figure was taken under the power cap: use it when

@@ -620,12 +620,16 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
         const uint32_t b_col = ti.n * BN + half * BH;
         uint32_t stage = 0, phase = 0, issued = 0;
         bool ok = true;
+        // ShuffleK: this split's range starts at (task + split) % its k-blocks
+        const uint32_t nk = kb_end - kb_begin;
+        const uint32_t rot = (prm.g.shuffle_k && nk) ? (t + split) % nk : 0u;
         for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
             uint8_t* sa_s = smem + stage * SL::kStageBytes;
             uint8_t* sb_s = sa_s + SL::kABytes;
             const uint32_t bar = full_leader + stage * 8;
-            const int32_t k0 = kb * bk_elems;
+            const uint32_t kx = kb + rot;
+            const int32_t k0 = (kx < kb_end ? kx : kx - nk) * bk_elems;
             if (is_a) {
                 if (half == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                 if (!a_mn) tma_load_2d_pair(sa_s, &prm.tmap_a, bar, k0, a_row);

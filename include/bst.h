@@ -106,9 +106,9 @@ typedef struct {
                                    tiles running at the same time read different
                                    k-blocks of a shared operand panel.  Changes only
                                    the fp32 summation order.  fp16/bf16 and int8
-                                   paths; MXFP8 returns BST_ERR_UNSUPPORTED, and
-                                   split-K is not used with it (split_k >= 2 is
-                                   BST_ERR_UNSUPPORTED).                             */
+                                   paths (a split-K tile rotates within its split's
+                                   K range, starting at (task + split) % its
+                                   k-blocks); MXFP8 returns BST_ERR_UNSUPPORTED.     */
     uint32_t dynamic;           /* 1: dynamic task allocation ("Block Scheduler Code
                                    Explained" section 1): the grid holds one CTA-pair
                                    cluster per task; a cluster computes its own task,

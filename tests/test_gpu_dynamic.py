@@ -40,6 +40,17 @@ def test_dense_pair(mnk, tn, dyn, shuffle):
     assert np.array_equal(_rows(trace), np.array(osw.swizzle_map(M, N, 256, tn, 2, 1), dtype=np.uint32))
 
 
+@pytest.mark.parametrize("tn,splits", [(256, 2), (128, 2), (256, 4), (128, 4)])
+@pytest.mark.parametrize("mnk", [(1024, 1024, 2048), (300, 500, 1000), (256, 256, 200)])
+def test_shuffle_k_split_k(tn, splits, mnk):
+    """Split-K tiles rotate within each split's K range (K = 200 leaves
+    splits of 0 or 1 k-blocks)."""
+    M, N, K = mnk
+    w = wl.dense16(M, N, K, "f16", b_col_major=True, seed=M + K + tn)
+    got = run_dense(w, "f16", bst.sched(1, 0, tile_n=tn, tile_m=256, split_k=splits, shuffle_k=1))
+    assert_close_f16(got, oracle_dense(w, "f16"))
+
+
 @pytest.mark.parametrize("mnk,lda_pad", [((300, 260, 1000), 0), ((129, 500, 300), 3), ((640, 128, 4096), 0)])
 @pytest.mark.parametrize("tn", [64, 128, 256])
 def test_shuffle_k_one_cta(mnk, lda_pad, tn):
@@ -163,7 +174,6 @@ def test_flags_rejected():
     for kw, status in (({"dynamic": 1, "num_ctas": 8}, bst.ERR_INVALID_ARG),
                        ({"dynamic": 1, "tile_m": 128}, bst.ERR_UNSUPPORTED),
                        ({"dynamic": 1, "split_k": 2}, bst.ERR_UNSUPPORTED),
-                       ({"shuffle_k": 1, "split_k": 2}, bst.ERR_UNSUPPORTED),
                        ({"dynamic": 2}, bst.ERR_INVALID_ARG)):
         with pytest.raises(bst.BstError) as e:
             run_dense(d, "f16", bst.sched(1, 0, **kw))

@@ -362,23 +362,63 @@ __device__ __noinline__ static void load_tile_regs(uint8_t* dst, const uint8_t* 
     }
 }
 
-__device__ __forceinline__ void load_tile_plain(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t mn_major,
+// The same shared-memory image by cp.async (V = 4, 8 or 16): every vector of
+// the tile is in flight at once, straight from L2 into shared memory, with
+// out-of-range bytes zero-filled by the copy itself.  The caller follows
+// with cp.async.mbarrier.arrive, so the stage's barrier completes when this
+// lane's copies have landed (the MMA thread fences for the async proxy).
+template <uint32_t V, bool MN>
+__device__ __noinline__ static void load_tile_async(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t lines,
+                                                    uint32_t mn0, uint32_t mn_lim, uint32_t k0, uint32_t k_lim,
+                                                    uint32_t lane) {
+    constexpr uint32_t kEsize = 2;
+    constexpr uint32_t kLineElems = kLine / kEsize;   // 64
+    constexpr uint32_t vpl = kLine / V;               // vectors per 128-byte line: 8, 16 or 32
+    static_assert(32 % vpl == 0, "lane pattern");
+    constexpr uint32_t kLinesPerPass = 32 / vpl;
+    const uint32_t bil = (lane % vpl) * V;            // byte of this lane's vectors within their lines
+    const uint32_t eil = bil / kEsize;
+#pragma unroll 4
+    for (uint32_t L = lane / vpl; L < lines; L += kLinesPerPass) {
+        uint32_t outer, outer_lim, e, inner_lim;
+        if (!MN) {                    // line = one MN row, a k-block of K
+            outer = mn0 + L;
+            outer_lim = mn_lim;
+            e = k0 + eil;
+            inner_lim = k_lim;
+        } else {                      // line = one k of a 64-element MN atom
+            outer = k0 + (L % kLineElems);
+            outer_lim = k_lim;
+            e = mn0 + (L / kLineElems) * kLineElems + eil;
+            inner_lim = mn_lim;
+        }
+        const uint32_t in_elems = (outer < outer_lim && e < inner_lim) ? inner_lim - e : 0u;
+        const uint32_t in_bytes = min(V, in_elems * kEsize);
+        const uint8_t* src = in_bytes ? base + (static_cast<int64_t>(outer) * ld + e) * kEsize : base;
+        cp_async_v<V>(dst + L * kLine + ((((bil >> 4) ^ (L & 7u)) << 4) | (bil & 15u)), src, in_bytes);
+    }
+}
+
+// Returns true when the copies went out asynchronously (the caller then
+// arrives with cp.async.mbarrier.arrive), false when they were register
+// loads and stores (2-byte vectors, which cp.async cannot copy).
+__device__ __forceinline__ bool load_tile_plain(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t mn_major,
                                                 uint32_t V, uint32_t esize, uint32_t lines, uint32_t mn0,
                                                 uint32_t mn_lim, uint32_t k0, uint32_t k_lim, uint32_t lane) {
     (void)esize;   // always 2 here
     if (mn_major) {
         switch (V) {
-            case 16: load_tile_regs<16, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
-            case 8: load_tile_regs<8, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
-            case 4: load_tile_regs<4, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
-            default: load_tile_regs<2, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            case 16: load_tile_async<16, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
+            case 8: load_tile_async<8, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
+            case 4: load_tile_async<4, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
+            default: load_tile_regs<2, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return false;
         }
     } else {
         switch (V) {
-            case 16: load_tile_regs<16, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
-            case 8: load_tile_regs<8, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
-            case 4: load_tile_regs<4, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
-            default: load_tile_regs<2, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); break;
+            case 16: load_tile_async<16, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
+            case 8: load_tile_async<8, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
+            case 4: load_tile_async<4, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
+            default: load_tile_regs<2, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return false;
         }
     }
 }
@@ -802,6 +842,9 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         }
                         cp_async_arrive_noinc(&full[stage]);
                     } else {
+                        // operands TMA cannot fetch: cp.async where the vectors
+                        // allow it (the lane's arrival fires when its copies
+                        // land), else register copies, fenced before the arrival
                         if (!a_tma)
                             load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec,
                                             esize, kBM, ti.row0, ti.m_lim, k0, K, lane);
@@ -809,8 +852,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                             load_tile_plain(sb_s,
                                             b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
                                             b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane);
-                        fence_proxy_async_smem();        // generic-proxy writes -> the MMA's reads
-                        mbar_arrive(&full[stage]);
+                        fence_proxy_async_smem();        // register-copied bytes -> the MMA's reads
+                        cp_async_arrive_noinc(&full[stage]);
                         if (tma_thread) {                // the TMA half of a mixed stage
                             mbar_arrive_expect_tx(&full[stage], tx);
                             if (a_tma)
@@ -856,9 +899,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
-                    // scale factors written by cp.async need a proxy fence before
-                    // tcgen05 reads them (every other writer fences before it arrives)
-                    if (KIND == kKindMXF8 && !sf_tma) fence_proxy_async_smem();
+                    // bytes written by cp.async (MXFP8 scale factors, operands
+                    // TMA cannot fetch) need a proxy fence before tcgen05 reads
+                    // them (every other writer fences before it arrives)
+                    if ((KIND == kKindMXF8 && !sf_tma) || lanes_copy_ops) fence_proxy_async_smem();
                     {
                         if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
                         const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;

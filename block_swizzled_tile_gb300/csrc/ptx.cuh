@@ -213,6 +213,15 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t 
                  );
 }
 
+// V-byte (4, 8 or 16) asynchronous copy into shared memory; bytes past
+// src_bytes (<= V) are zero-filled, and with src_bytes = 0 nothing is read
+template <uint32_t V>
+__device__ __forceinline__ void cp_async_v(void* dst, const void* src, uint32_t src_bytes) {
+    static_assert(V == 4 || V == 8 || V == 16, "cp.async size");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(smem_u32(dst)), "l"(src), "n"(V),
+                 "r"(src_bytes));
+}
+
 // waits until every cp.async issued by this thread has landed
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 

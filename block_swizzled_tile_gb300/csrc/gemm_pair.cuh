@@ -22,7 +22,9 @@
 //             outstanding copies every time.
 //   empty[s]  in both CTAs; the leader's MMA commit multicasts to both.
 //   tfull[a]  in both CTAs; the leader's MMA commit multicasts to both.
-//   tempty[a] leader only; one arrival per epilogue warp of both CTAs (8).
+//   tempty[a] leader only; one arrival per epilogue warp of both CTAs (8),
+//             relaxed: a warp arrives once its reads of the accumulator have
+//             completed (tcgen05.wait::ld), and publishes no data with it.
 // A cluster barrier after set-up (barriers initialised before any remote
 // arrive) and before exit (no CTA leaves while the other may still touch its
 // shared memory) brackets the work.
@@ -424,22 +426,40 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                                                   rows_valid, min(32u, n_act - cc * 32), v, lane);
                     }
                 } else {
-                    // fold the chunk (an exact integer in fp32) into the running sums
-#pragma unroll 1
+                    // fold the chunk (an exact integer in fp32) into the running
+                    // sums.  The accumulator is released as soon as the chunk is
+                    // in registers, so the next chunk's MMAs overlap the update
+                    // of the running sums (other TMEM columns).
+                    int32_t ci[EPI == kEpiDequant ? kCols : 1];
+#pragma unroll
                     for (uint32_t cc = 0; cc < kCols / 32; ++cc) {
-                        uint32_t v[32], r[32];
+                        uint32_t v[32];
                         tmem_ld_32x32b_x32(taddr + cc * 32, v);
+#pragma unroll
+                        for (uint32_t j = 0; j < 32; ++j)
+                            ci[(EPI == kEpiDequant ? cc * 32 + j : 0)] = __float2int_rn(__uint_as_float(v[j]));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
+#pragma unroll
+                    for (uint32_t cc = 0; cc < kCols / 32; ++cc) {
+                        uint32_t r[32];
                         if (c > 0) tmem_ld_32x32b_x32(run_t + cc * 32, r);
 #pragma unroll
                         for (uint32_t j = 0; j < 32; ++j)
                             r[j] = static_cast<uint32_t>((c > 0 ? static_cast<int32_t>(r[j]) : 0) +
-                                                         __float2int_rn(__uint_as_float(v[j])));
+                                                         ci[(EPI == kEpiDequant ? cc * 32 + j : 0)]);
                         tmem_st_32x32b_x32(run_t + cc * 32, r);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+                if (EPI == kEpiStore) {
+                    // the accumulator's reads are complete (tcgen05.wait::ld):
+                    // a relaxed arrival releases it, with no data to publish
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader + acc * 8);
+                }
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
             }
             if (!ok) break;

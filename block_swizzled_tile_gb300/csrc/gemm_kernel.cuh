@@ -188,6 +188,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitCt
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
+// Every lane of the warp polls the barrier itself (the issuing warps of the
+// MMA loops, which must stay converged); the result is made warp-uniform.
+__device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
+    const bool ok = mbar_wait(bar, parity, ctl, where);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // What the scheduler needs, in registers.
 struct SchedArgs {
     uint32_t M, N, swz_offset, swz_dir, mode, total_m;
@@ -626,6 +633,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     griddep_launch_dependents();
     if (mode == kModeGrouped && warp == 2)
         build_group_table(gt, prm.g.group_m, G, N, kBM, BN, sa.total_m, err, tiles_smem, lane);
+    __syncwarp();                                    // reconverge lane-0 set-up branches first
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -888,22 +896,23 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
         bool ok = true, any_mma = false;
         const uint32_t nchunks = SPLIT > 1 ? (has_k ? 1u : 0u) : (num_kb + chunk_kb - 1) / chunk_kb;
-        // one thread issues every MMA (a single-lane loop, see the producer)
-        for (uint32_t t = t_first; lane == 0 && ok && t < total_tiles; t += t_step) {
+        // the whole warp runs the loop (waits are warp-wide); the elected lane
+        // (lane 0) issues every MMA, scale copy and commit
+        for (uint32_t t = t_first; ok && t < total_tiles; t += t_step) {
             for (uint32_t c = 0; ok && c < nchunks; ++c) {
                 const uint32_t kb_begin = SPLIT > 1 ? kb_lo : c * chunk_kb;
                 const uint32_t kb_end = SPLIT > 1 ? kb_hi : min(num_kb, kb_begin + chunk_kb);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
+                if (!warp_poll(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
+                    if (!warp_poll(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
                     // bytes written by cp.async (MXFP8 scale factors, operands
                     // TMA cannot fetch) need a proxy fence before tcgen05 reads
                     // them (every other writer fences before it arrives)
                     if ((KIND == kKindMXF8 && !sf_tma) || lanes_copy_ops) fence_proxy_async_smem();
-                    {
+                    if (elect_one()) {
                         if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
                         const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
                         const uint32_t sb_addr = sa_addr + Lay::kABytes;
@@ -930,12 +939,14 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         }
                         umma_commit(&empty[stage]);
                     }
+                    __syncwarp();
                     ++mma_kb;
                     any_mma = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[acc]);
+                if (elect_one()) umma_commit(&tfull[acc]);
+                __syncwarp();
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
             }
         }
@@ -1058,6 +1069,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // receive slot of CTA g, completing on that CTA's receive barrier of
         // the same warp; it then adds the SPLIT-1 partials it received to its
         // own rows of its own columns, rounds once and stores.
+        __syncwarp();
         tc_fence_before();
         __syncthreads();
         cluster_sync();
@@ -1142,11 +1154,15 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
             }
         }
+        __syncwarp();
         tc_fence_before();
         __syncthreads();
         cluster_sync();                                  // no CTA leaves while a peer may still touch it
     }
     if (tl && lane == 0 && warp <= 2) tl[48 + warp] = globaltimer_ns();
+    // single-lane roles leave their warps diverged: reconverge every warp
+    // first, so that the block barrier counts each warp once
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
         for (uint32_t g = lane; g < G; g += 32) gt.tile_off[g] = bad ? 0u : prm.g.group_kb[g];
         if (lane == 0 && bad) *tiles_smem = 0;
     }
+    __syncwarp();                                    // reconverge lane-0 set-up branches first
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -312,7 +313,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, mma_kb = 0;
             bool ok = true, any_mma = false;
             const uint32_t chunk_kb = prm.g.chunk_kb;
-            for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t = tasks.next(t, ok, 1, ctl)) {
+            // the whole warp runs the loop (waits are warp-wide); the elected
+            // lane (lane 0) issues every MMA and commit
+            for (uint32_t t = cid; ok && t < total_tiles; t = tasks.next(t, ok, 2, ctl)) {
               // an empty slice-K group has no MMAs: its epilogue stores zeros
               const uint32_t tkb = mode == kModeSliceK ? tile_kb(tile_info(sa, t, TM, BN, gt).tag) : num_kb;
               const uint32_t nchunks = (tkb + chunk_kb - 1) / chunk_kb;
@@ -320,13 +323,13 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
               for (uint32_t c = 0; ok && c < nchunks; ++c) {
                 const uint32_t kb_begin = c * chunk_kb;
                 const uint32_t kb_end = min(tkb, kb_begin + chunk_kb);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
+                if (!warp_poll(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
+                    if (!warp_poll(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
-                    {
+                    if (elect_one()) {
                         if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
                         const uint32_t sa_addr = smem_base + stage * Lay::kStageBytes;
                         const uint64_t adesc = smem_desc(sa_addr, a_lbo, 1024, kSwizzle128B);
@@ -337,12 +340,14 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
                                           (kb > kb_begin || kk > 0) ? 1u : 0u);
                         umma_commit_pair_mc(&empty[stage], 0x3);
                     }
+                    __syncwarp();
                     ++mma_kb;
                     any_mma = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit_pair_mc(&tfull[acc], 0x3);
+                if (elect_one()) umma_commit_pair_mc(&tfull[acc], 0x3);
+                __syncwarp();
                 if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
               }
             }
@@ -498,6 +503,9 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
     }
 
     if (tl && lane == 0 && warp <= 2) tl[48 + warp] = globaltimer_ns();
+    // single-lane roles leave their warps diverged: reconverge every warp
+    // first, so that the block barrier counts each warp once
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -616,6 +624,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
         tmem_alloc_pair(tmem_holder, SL::kTmemCols);
         tmem_relinquish_pair();
     }
+    __syncwarp();                                    // reconverge lane-0 set-up branches first
     tc_fence_before();
     __syncthreads();
     cluster_sync();                                  // barriers of every CTA initialised
@@ -674,8 +683,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
                 mbar_wait_drain(&full[s], ph, ctl.timeout_ns);
             }
         }
-    } else if (warp == 1 && lane == 0 && has_tile && has_k && half == 0) {
+    } else if (warp == 1 && has_tile && has_k && half == 0) {
         // ------------------------------------- MMA issuer (pair leaders) --
+        // the whole warp runs the loop; the elected lane (lane 0) issues
         const uint32_t a_lbo = a_mn ? bk_elems * kLine : 16u;
         const uint32_t b_lbo = b_mn ? bk_elems * kLine : 16u;
         const uint32_t a_step = a_mn ? 16u * kLine : 32u;
@@ -685,24 +695,29 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
         uint32_t stage = 0, phase = 0;
         bool ok = true, any_mma = false;
         for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-            if (!mbar_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
+            if (!warp_poll(&full[stage], phase, ctl, 3)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa_addr = smem_base + stage * SL::kStageBytes;
-            const uint64_t adesc = smem_desc(sa_addr, a_lbo, 1024, kSwizzle128B);
-            const uint64_t bdesc = smem_desc(sa_addr + SL::kABytes, b_lbo, 1024, kSwizzle128B);
+            if (elect_one()) {
+                const uint32_t sa_addr = smem_base + stage * SL::kStageBytes;
+                const uint64_t adesc = smem_desc(sa_addr, a_lbo, 1024, kSwizzle128B);
+                const uint64_t bdesc = smem_desc(sa_addr + SL::kABytes, b_lbo, 1024, kSwizzle128B);
 #pragma unroll
-            for (uint32_t kk = 0; kk < 4; ++kk)
-                umma_f16_pair(tmem_base, adesc + ((kk * a_step) >> 4), bdesc + ((kk * b_step) >> 4), idesc,
-                              (kb > kb_begin || kk > 0) ? 1u : 0u);
-            umma_commit_pair_mc(&empty[stage], pair_mask);
-            if (tl && kb - kb_begin < 16) tl[16 + kb - kb_begin] = globaltimer_ns();
+                for (uint32_t kk = 0; kk < 4; ++kk)
+                    umma_f16_pair(tmem_base, adesc + ((kk * a_step) >> 4), bdesc + ((kk * b_step) >> 4), idesc,
+                                  (kb > kb_begin || kk > 0) ? 1u : 0u);
+                umma_commit_pair_mc(&empty[stage], pair_mask);
+                if (tl && kb - kb_begin < 16) tl[16 + kb - kb_begin] = globaltimer_ns();
+            }
+            __syncwarp();
             any_mma = true;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (ok) umma_commit_pair_mc(tfull, pair_mask);
-        else if (any_mma) {
-            umma_commit_pair_mc(drain, static_cast<uint16_t>(1u << crank));
-            mbar_wait_drain(drain, 0, ctl.timeout_ns);
+        if (lane == 0) {                                 // the lane that issued the MMAs
+            if (ok) umma_commit_pair_mc(tfull, pair_mask);
+            else if (any_mma) {
+                umma_commit_pair_mc(drain, static_cast<uint16_t>(1u << crank));
+                mbar_wait_drain(drain, 0, ctl.timeout_ns);
+            }
         }
     } else if (warp >= 2 && warp < 6 && has_tile) {
         // ----------------------------------------------------- epilogue --
@@ -753,6 +768,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
         // finish: own rows of own columns plus the S-1 received partials
         const bool got = warp_wait(&recv[q], 0, ctl, 5);
         if (tl && warp == 2 && lane == 0) tl[33] = globaltimer_ns();
+        if (tl && lane == 0) tl[48 + q] = globaltimer_ns();
         const uint8_t* slots = smem + SL::kRecvOff + q * (S - 1) * SL::kSlotBytes + lane * (W * 4);
         const uint32_t wrow = half * kBM + q * 32;       // first row of this warp in the tile
         const uint32_t rows_valid = ti.m_act > wrow ? min(32u, ti.m_act - wrow) : 0u;
@@ -788,6 +804,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
                 store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(ti.n * BN + col) * csize,
                                       ldc * csize, rows_valid, min(32u, ti.n_act - col), v, lane);
         }
+        if (tl && lane == 0) tl[40 + q] = globaltimer_ns();
         if (lane == 0) bulk_wait_read_all();             // the ring may not be left while being read
         if (prm.g.trace && split == 0 && half == 0 && q == 0 && lane == 0 && t < prm.g.trace_cap) {
             uint32_t* tr = prm.g.trace + static_cast<uint64_t>(t) * 5;
@@ -796,9 +813,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
     }
 
     if (tl && threadIdx.x == 64) tl[36] = globaltimer_ns();
+    // single-lane roles leave their warps diverged: reconverge every warp
+    // first, so that the block barrier counts each warp once
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (tl && threadIdx.x == 0) tl[38] = globaltimer_ns();
     cluster_sync();                                  // no CTA leaves while a peer may still touch it
+    if (tl && threadIdx.x == 0) tl[39] = globaltimer_ns();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, SL::kTmemCols);

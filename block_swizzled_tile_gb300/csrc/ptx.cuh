@@ -26,6 +26,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// 1 in exactly one lane of the (converged) warp -- the lowest active one, so
+// lane 0 of a full warp -- 0 elsewhere.  The MMA loops run on the whole warp
+// and issue from the elected lane: a tcgen05.mma group issued by a lone lane
+// of a diverged warp and followed by an mbarrier wait costs about 320 ns per
+// k-block on sm_103a whatever its size, against about 200 ns (128 x 128
+// pieces) to 260 ns (128 x 256, the tensor time) from a converged warp.
+__device__ __forceinline__ uint32_t elect_one() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok));
+    return ok;
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
     uint32_t l;
     asm volatile("mov.u32 %0, %laneid;" : "=r"(l));

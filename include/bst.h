@@ -98,8 +98,11 @@ typedef struct {
                                    (ns) of their pipeline events: [0] start, [1..15]
                                    producer k-block issues, [16..31] MMA k-block starts,
                                    [32..39] epilogue tile starts, [40..47] epilogue tile
-                                   ends, [48..50] producer/MMA/epilogue exit.  Profiling
-                                   only.                                               */
+                                   ends, [48..50] producer/MMA/epilogue exit.  Split-K
+                                   kernels instead use [32] accumulator ready, [34] / [33]
+                                   partials sent / received, [36..39] exit steps, and per
+                                   epilogue warp [48..51] partials received, [40..43]
+                                   stores done.  Profiling only.                       */
     uint32_t shuffle_k;         /* 1: ShuffleK ("Block Dispatch Policies",
                                    ENABLE_SHUFFLE_K): the K loop of task t starts at
                                    k-block t % (k-blocks of the tile) and wraps, so

@@ -1071,8 +1071,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // own rows of its own columns, rounds once and stores.
         __syncwarp();
         tc_fence_before();
-        __syncthreads();
-        cluster_sync();
+        cluster_sync();                                  // also orders this CTA's own warps
         tc_fence_after();
         if (warp >= 2 && warp < 6 && t_first < total_tiles) {
             constexpr uint32_t W = Lay::kSplitW;
@@ -1156,15 +1155,15 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         }
         __syncwarp();
         tc_fence_before();
-        __syncthreads();
         cluster_sync();                                  // no CTA leaves while a peer may still touch it
     }
     if (tl && lane == 0 && warp <= 2) tl[48 + warp] = globaltimer_ns();
     // single-lane roles leave their warps diverged: reconverge every warp
-    // first, so that the block barrier counts each warp once
+    // first, so that the block barrier counts each warp once (split tiles
+    // have just passed the cluster barrier, which orders every warp already)
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if (SPLIT == 1) __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, Lay::kTmemCols);

@@ -71,7 +71,7 @@ struct SplitLaunch {
     static cudaLaunchConfig_t config(uint32_t tiles, cudaStream_t stream, cudaLaunchAttribute* attr) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * S * tiles);
-        cfg.blockDim = dim3(kPairThreads);
+        cfg.blockDim = dim3(Lay::kThreads);
         cfg.dynamicSmemBytes = Lay::smem_bytes();
         cfg.stream = stream;
         attr[0].id = cudaLaunchAttributeClusterDimension;

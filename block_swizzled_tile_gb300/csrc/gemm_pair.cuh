@@ -504,10 +504,10 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
 
     if (tl && lane == 0 && warp <= 2) tl[48 + warp] = globaltimer_ns();
     // single-lane roles leave their warps diverged: reconverge every warp
-    // first, so that the block barrier counts each warp once
+    // first, so that the barrier counts each warp once; the cluster barrier
+    // also orders this CTA's own warps before TMEM is freed
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
     cluster_sync();
     if (warp == 1) {
         tc_fence_after();
@@ -547,25 +547,36 @@ struct SplitLayout {
     static constexpr uint32_t kBBytes = (BN / 2) * kLine;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kW = BN / S;                         // columns each split finishes
-    static constexpr uint32_t kSlotBytes = 32 * kW * 4;            // one warp's rows of W columns
+    static constexpr uint32_t kSlotBytes = 32 * kW * 4;            // 32 rows of W columns
     static constexpr uint32_t kSlots = 4 * (S - 1);                // per CTA, sent and received
     static constexpr uint32_t kRecvOff = STAGES * kStageBytes;
     static constexpr uint32_t kRecvBytes = kSlots * kSlotBytes;
+    // Epilogue groups: warps 2-5, and (kEH = 2) warps 0, 1, 6, 7 once their
+    // loads and MMAs are issued; the group of warp w finishes columns
+    // [h*kWH, (h+1)*kWH) of each split's W in TMEM lane quarter w % 4.  The
+    // second group stages its stores in the idle ring, after the send staging.
+    static constexpr uint32_t kEH =
+        (kW >= 64 && kSlots * kSlotBytes + 4 * kEpiWarpBytes <= STAGES * kStageBytes) ? 2u : 1u;
+    static constexpr uint32_t kWH = kW / kEH;
+    static constexpr uint32_t kSubBytes = 32 * kWH * 4;            // one warp's rows of its kWH columns
+    static constexpr uint32_t kEpi1Off = kSlots * kSlotBytes;      // second group's store staging (ring)
+    static constexpr uint32_t kThreads = kEH == 2 ? 256u : 224u;
     static constexpr uint32_t kEpiOff = kRecvOff + kRecvBytes;
     static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 4;       // full, empty, tfull, drain, recv[4]
+    // full, empty, tfull, drain, recv[4 * kEH]
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 + 4 * kEH;
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTmemCols = BN;
     static constexpr uint32_t smem_bytes() { return 1024 + kMiscOff + 16; }
     static_assert(S == 2 || S == 4, "splits");
-    static_assert(kW % 32 == 0, "whole 32-column chunks per split");
+    static_assert(kW % 32 == 0 && kWH % 32 == 0, "whole 32-column chunks per split and group");
     static_assert(kSlots * kSlotBytes <= STAGES * kStageBytes, "sender staging reuses the ring");
     static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(smem_bytes() <= 232448, "shared memory per CTA");
 };
 
 template <uint32_t BN, uint32_t STAGES, uint32_t S>
-__global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const __grid_constant__ GemmParams prm) {
+__global__ void __launch_bounds__(256, 1) gemm_pair_splitk_kernel(const __grid_constant__ GemmParams prm) {
     using SL = SplitLayout<BN, STAGES, S>;
     constexpr uint32_t TM = 2 * kBM;
     constexpr uint32_t BH = BN / 2;
@@ -610,11 +621,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
         }
         mbar_init(tfull, 1);
         mbar_init(drain, 1);
-        for (uint32_t o = 0; o < 4; ++o) mbar_init(&recv[o], 1);
+        for (uint32_t o = 0; o < 4 * SL::kEH; ++o) mbar_init(&recv[o], 1);
         *abort_flag = 0;
         fence_barrier_init();
         // the receive barrier of each epilogue warp expects the S-1 partials of its rows
-        for (uint32_t o = 0; o < 4; ++o) mbar_arrive_expect_tx(&recv[o], (S - 1) * SL::kSlotBytes);
+        for (uint32_t o = 0; o < 4 * SL::kEH; ++o) mbar_arrive_expect_tx(&recv[o], (S - 1) * SL::kSubBytes);
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&prm.tmap_a);
@@ -719,28 +730,33 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
                 mbar_wait_drain(drain, 0, ctl.timeout_ns);
             }
         }
-    } else if (warp >= 2 && warp < 6 && has_tile) {
+    }
+    __syncwarp();                                        // reconverge the single-lane load warps
+    const bool epi_main = warp >= 2 && warp < 6;
+    if ((epi_main || (SL::kEH == 2 && (warp < 2 || warp >= 6))) && has_tile) {
         // ----------------------------------------------------- epilogue --
         const uint32_t q = warp & 3u;                    // TMEM lane quarter of this warp
+        const uint32_t h = epi_main ? 0u : 1u;           // column group of this warp
         const uint32_t taddr = tmem_base + ((q * 32) << 16);
-        constexpr uint32_t W = SL::kW;
+        constexpr uint32_t W = SL::kW, WH = SL::kWH;
+        const uint32_t qh = q * SL::kEH + h;             // receive barrier and slot group
         // this warp's rows are final once its pair's MMAs are done
         bool acc_ok = true;
         if (has_k) acc_ok = warp_wait(tfull, 0, ctl, 4);
         tc_fence_after();
         if (tl && warp == 2 && lane == 0) tl[32] = globaltimer_ns();
         const bool own_valid = acc_ok && has_k;          // else this split's partial counts as zero
-        // send: for every other split g, this warp's rows of g's columns
+        // send: for every other split g, this warp's rows of its group of g's columns
         uint32_t gi = 0;
 #pragma unroll 1
         for (uint32_t g = 0; g < S; ++g) {
             if (g == split) continue;
-            uint8_t* stage_rows = smem + (q * (S - 1) + gi) * SL::kSlotBytes;
-            uint8_t* my_row = stage_rows + lane * (W * 4);
+            uint8_t* stage_rows = smem + (qh * (S - 1) + gi) * SL::kSubBytes;
+            uint8_t* my_row = stage_rows + lane * (WH * 4);
 #pragma unroll 1
-            for (uint32_t cc = 0; cc < W / 32; ++cc) {
+            for (uint32_t cc = 0; cc < WH / 32; ++cc) {
                 uint32_t v[32];
-                if (own_valid) tmem_ld_32x32b_x32(taddr + g * W + cc * 32, v);
+                if (own_valid) tmem_ld_32x32b_x32(taddr + g * W + h * WH + cc * 32, v);
                 else {
 #pragma unroll
                     for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
@@ -756,31 +772,31 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
             __syncwarp();
             if (lane == 0) {
                 const uint32_t dest = 2 * g + half;      // split g, same half
-                const uint32_t slot = q * (S - 1) + (split < g ? split : split - 1);
-                const uint32_t dst = map_to_cta(smem_u32(smem + SL::kRecvOff + slot * SL::kSlotBytes), dest);
-                const uint32_t bar = map_to_cta(smem_u32(&recv[q]), dest);
-                bulk_copy_to_cluster(dst, stage_rows, SL::kSlotBytes, bar);
+                const uint32_t slot = qh * (S - 1) + (split < g ? split : split - 1);
+                const uint32_t dst = map_to_cta(smem_u32(smem + SL::kRecvOff + slot * SL::kSubBytes), dest);
+                const uint32_t bar = map_to_cta(smem_u32(&recv[qh]), dest);
+                bulk_copy_to_cluster(dst, stage_rows, SL::kSubBytes, bar);
                 bulk_commit_group();
             }
             ++gi;
         }
         if (tl && warp == 2 && lane == 0) tl[34] = globaltimer_ns();
         // finish: own rows of own columns plus the S-1 received partials
-        const bool got = warp_wait(&recv[q], 0, ctl, 5);
+        const bool got = warp_wait(&recv[qh], 0, ctl, 5);
         if (tl && warp == 2 && lane == 0) tl[33] = globaltimer_ns();
-        if (tl && lane == 0) tl[48 + q] = globaltimer_ns();
-        const uint8_t* slots = smem + SL::kRecvOff + q * (S - 1) * SL::kSlotBytes + lane * (W * 4);
+        if (tl && lane == 0 && h == 0) tl[48 + q] = globaltimer_ns();
+        const uint8_t* slots = smem + SL::kRecvOff + qh * (S - 1) * SL::kSubBytes + lane * (WH * 4);
         const uint32_t wrow = half * kBM + q * 32;       // first row of this warp in the tile
         const uint32_t rows_valid = ti.m_act > wrow ? min(32u, ti.m_act - wrow) : 0u;
         const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
         const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
         const int64_t ldc = prm.g.ldc;
         uint8_t* const cwarp = prm.g.C + static_cast<int64_t>(ti.row0 + wrow) * ldc * csize;
-        uint8_t* const epi_stage = smem + SL::kEpiOff + q * kEpiWarpBytes;
+        uint8_t* const epi_stage = smem + (h ? SL::kEpi1Off : SL::kEpiOff) + q * kEpiWarpBytes;
 #pragma unroll 1
-        for (uint32_t cc = 0; cc < W / 32; ++cc) {
+        for (uint32_t cc = 0; cc < WH / 32; ++cc) {
             uint32_t v[32];
-            if (own_valid) tmem_ld_32x32b_x32(taddr + split * W + cc * 32, v);
+            if (own_valid) tmem_ld_32x32b_x32(taddr + split * W + h * WH + cc * 32, v);
             else {
 #pragma unroll
                 for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
@@ -791,7 +807,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
 #pragma unroll
                     for (uint32_t gg = 0; gg < 8; ++gg) {
                         const uint32_t granule = (cc * 8 + gg) ^ (lane & 7u);
-                        const uint4 x = *reinterpret_cast<const uint4*>(slots + si * SL::kSlotBytes + granule * 16);
+                        const uint4 x = *reinterpret_cast<const uint4*>(slots + si * SL::kSubBytes + granule * 16);
                         v[4 * gg] = __float_as_uint(__uint_as_float(v[4 * gg]) + __uint_as_float(x.x));
                         v[4 * gg + 1] = __float_as_uint(__uint_as_float(v[4 * gg + 1]) + __uint_as_float(x.y));
                         v[4 * gg + 2] = __float_as_uint(__uint_as_float(v[4 * gg + 2]) + __uint_as_float(x.z));
@@ -799,14 +815,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
                     }
                 }
             }
-            const uint32_t col = split * W + cc * 32;    // column within the tile
+            const uint32_t col = split * W + h * WH + cc * 32;   // column within the tile
             if (rows_valid && col < ti.n_act)
                 store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(ti.n * BN + col) * csize,
                                       ldc * csize, rows_valid, min(32u, ti.n_act - col), v, lane);
         }
-        if (tl && lane == 0) tl[40 + q] = globaltimer_ns();
+        if (tl && lane == 0 && h == 0) tl[40 + q] = globaltimer_ns();
         if (lane == 0) bulk_wait_read_all();             // the ring may not be left while being read
-        if (prm.g.trace && split == 0 && half == 0 && q == 0 && lane == 0 && t < prm.g.trace_cap) {
+        if (prm.g.trace && split == 0 && half == 0 && q == 0 && h == 0 && lane == 0 && t < prm.g.trace_cap) {
             uint32_t* tr = prm.g.trace + static_cast<uint64_t>(t) * 5;
             tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
         }
@@ -814,12 +830,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_splitk_kernel(const
 
     if (tl && threadIdx.x == 64) tl[36] = globaltimer_ns();
     // single-lane roles leave their warps diverged: reconverge every warp
-    // first, so that the block barrier counts each warp once
+    // first, so that the barrier counts each warp once.  The cluster barrier
+    // also orders this CTA's own warps (a block barrier before it only adds
+    // latency): no CTA leaves, and no TMEM is freed, while any thread of the
+    // cluster may still touch it.
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
-    if (tl && threadIdx.x == 0) tl[38] = globaltimer_ns();
-    cluster_sync();                                  // no CTA leaves while a peer may still touch it
+    cluster_sync();
     if (tl && threadIdx.x == 0) tl[39] = globaltimer_ns();
     if (warp == 1) {
         tc_fence_after();

@@ -177,20 +177,11 @@ struct GemmLayout {
     static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
 };
 
-// One lane of the warp waits on the barrier (the others would only add
-// shared-memory traffic); the warp then re-converges, with the memory
-// ordering of __syncwarp, and every lane gets the same verdict, so a timeout
-// never splits the warp.
+// Warp-wide wait: every lane polls the barrier itself and the result is made
+// warp-uniform.  Measured on sm_103a, this is much cheaper for the warp's
+// following work than one lane polling while the others wait at a warp
+// barrier (an MMA loop waiting that way ran at a third of the tensor rate).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
-    uint32_t ok = 1;
-    if ((threadIdx.x & 31u) == 0) ok = mbar_wait(bar, parity, ctl, where) ? 1u : 0u;
-    __syncwarp();
-    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-}
-
-// Every lane of the warp polls the barrier itself (the issuing warps of the
-// MMA loops, which must stay converged); the result is made warp-uniform.
-__device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
     const bool ok = mbar_wait(bar, parity, ctl, where);
     return __all_sync(0xFFFFFFFFu, ok);
 }
@@ -902,11 +893,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             for (uint32_t c = 0; ok && c < nchunks; ++c) {
                 const uint32_t kb_begin = SPLIT > 1 ? kb_lo : c * chunk_kb;
                 const uint32_t kb_end = SPLIT > 1 ? kb_hi : min(num_kb, kb_begin + chunk_kb);
-                if (!warp_poll(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
+                if (!warp_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!warp_poll(&full[stage], phase, ctl, 3)) { ok = false; break; }
+                    if (!warp_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
                     // bytes written by cp.async (MXFP8 scale factors, operands
                     // TMA cannot fetch) need a proxy fence before tcgen05 reads

@@ -323,11 +323,11 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
               for (uint32_t c = 0; ok && c < nchunks; ++c) {
                 const uint32_t kb_begin = c * chunk_kb;
                 const uint32_t kb_end = min(tkb, kb_begin + chunk_kb);
-                if (!warp_poll(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
+                if (!warp_wait(&tempty[acc], acc_phase ^ 1u, ctl, 2)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!warp_poll(&full[stage], phase, ctl, 3)) { ok = false; break; }
+                    if (!warp_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
                     tc_fence_after();
                     if (elect_one()) {
                         if (tl && mma_kb < 16) tl[16 + mma_kb] = globaltimer_ns();
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(256, 1) gemm_pair_splitk_kernel(const __grid_c
         uint32_t stage = 0, phase = 0;
         bool ok = true, any_mma = false;
         for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-            if (!warp_poll(&full[stage], phase, ctl, 3)) { ok = false; break; }
+            if (!warp_wait(&full[stage], phase, ctl, 3)) { ok = false; break; }
             tc_fence_after();
             if (elect_one()) {
                 const uint32_t sa_addr = smem_base + stage * SL::kStageBytes;

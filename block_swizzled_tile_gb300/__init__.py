@@ -24,7 +24,8 @@ EXPORTED = ["bst_gemm", "bst_gemm_batched", "bst_gemm_grouped", "bst_gemm_groupe
             "bst_gemm_grouped_slice_k_workspace_size", "bst_gemm_grouped_slice_k_quant_per_token",
             "bst_gemm_grouped_slice_k_quant_per_token_workspace_size", "bst_gemm_quant_per_token",
             "bst_gemm_quant_per_token_noalloc", "bst_gemm_quant_per_token_workspace_size", "bst_swizzle_map",
-            "bst_swizzle_map_grouped", "bst_check_async", "bst_status_string", "bst_set_wait_timeout_ns"]
+            "bst_swizzle_map_grouped", "bst_check_async", "bst_status_string", "bst_set_wait_timeout_ns",
+            "bst_wait_check"]
 # BST_NOALLOC_SCRATCH_BYTES: the scratch limit of gemm_quant_per_token_noalloc
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -80,6 +81,7 @@ _SIGS = {
     "bst_check_async": [_vp],
     "bst_status_string": [_i32],
     "bst_set_wait_timeout_ns": [ctypes.c_uint64],
+    "bst_wait_check": [ctypes.c_uint64, _i32, _vp],
 }
 
 
@@ -239,3 +241,9 @@ def check_async(stream=None):
 
 def set_wait_timeout_ns(ns):
     lib().bst_set_wait_timeout_ns(ns)
+
+
+def wait_check(timeout_ns, arrive, stream=None):
+    """Launches the bounded-wait self-check (bst_wait_check); the result is
+    reported by the next check_async."""
+    _check(lib().bst_wait_check(timeout_ns, 1 if arrive else 0, _stream(stream)), "bst_wait_check")

@@ -1144,4 +1144,11 @@ const char* bst_status_string(bst_status s) {
 
 void bst_set_wait_timeout_ns(uint64_t ns) { t_timeout_ns = ns; }
 
+bst_status bst_wait_check(uint64_t timeout_ns, int32_t arrive, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull) return BST_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (bst_status s = device_info(dev)) return s;
+    return cuda_status(launch_wait_check(timeout_ns, arrive ? 1u : 0u, dev.err, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -110,6 +110,7 @@ cudaError_t launch_zero_fill(uint8_t* C, int64_t ldc, int64_t batch_stride, int6
                              int64_t batch, uint32_t esize, uint32_t sms, cudaStream_t stream);
 
 cudaError_t launch_swizzle_map(const PlainSched& s, uint32_t total, uint32_t* out, cudaStream_t stream);
+cudaError_t launch_wait_check(uint64_t timeout_ns, uint32_t arrive, uint32_t* err, cudaStream_t stream);
 cudaError_t launch_swizzle_map_grouped(const int32_t* group_m, uint32_t G, uint32_t N, uint32_t tile_m,
                                        uint32_t tile_n, uint32_t offset, uint32_t dir, uint32_t* out,
                                        uint32_t max_tasks, uint32_t* err, cudaStream_t stream);

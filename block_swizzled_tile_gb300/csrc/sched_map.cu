@@ -1,7 +1,7 @@
 // Debug map kernels that run the device scheduler of sched.cuh over every
 // task index ("Block Scheduler Code Explained", section 7 execution flow:
-// batch index, block coordinate, actual block shape per task), and the
-// zero-fill used when K == 0.
+// batch index, block coordinate, actual block shape per task), the
+// zero-fill used when K == 0, and the self-check of the bounded waits.
 #include "internal.h"
 
 namespace bst {
@@ -99,6 +99,32 @@ cudaError_t launch_zero_fill(uint8_t* C, int64_t ldc, int64_t batch_stride, int6
                              int64_t batch, uint32_t esize, uint32_t sms, cudaStream_t stream) {
     if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
     zero_fill_kernel<<<sms * 4, 256, 0, stream>>>(C, ldc, batch_stride, rows, cols, batch, esize);
+    return cudaGetLastError();
+}
+
+// Self-check of the device-side failure detection: thread 0 waits on a
+// shared-memory barrier with the same bounded wait the GEMM kernels use.  With
+// arrive != 0 thread 32 arrives on it (the wait succeeds); otherwise nothing
+// arrives, the wait gives up after timeout_ns and records a timeout in the
+// error word.  Nothing asynchronous is in flight, so giving up is harmless.
+__global__ void wait_check_kernel(uint64_t timeout_ns, uint32_t arrive, uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 32 && arrive) mbar_arrive(&bar);
+    if (threadIdx.x == 0) {
+        const WaitCtl ctl{&abort_flag, timeout_ns, err};
+        mbar_wait(&bar, 0, ctl, 99);
+    }
+}
+
+cudaError_t launch_wait_check(uint64_t timeout_ns, uint32_t arrive, uint32_t* err, cudaStream_t stream) {
+    wait_check_kernel<<<1, 64, 0, stream>>>(timeout_ns, arrive, err);
     return cudaGetLastError();
 }
 

@@ -397,6 +397,20 @@ const char* bst_status_string(bst_status s);
  */
 void bst_set_wait_timeout_ns(uint64_t ns);
 
+/*
+ * bst_wait_check -- self-check of the device-side failure detection (the
+ * pages have no counterpart; it exercises the bounded waits every GEMM kernel
+ * uses between its producer, MMA and epilogue roles).  Launches one small
+ * kernel on `stream` whose thread waits on a shared-memory barrier with that
+ * bounded wait.  arrive != 0: another thread arrives on the barrier first, so
+ * the wait succeeds and the next bst_check_async returns BST_OK.  arrive == 0:
+ * nothing arrives, the wait gives up after timeout_ns (1 ns .. 10 s, else
+ * BST_ERR_INVALID_ARG before anything is launched) and the next
+ * bst_check_async returns BST_ERR_TIMEOUT.  Nothing else is in flight while
+ * it waits, so the device stays usable.  Asynchronous; allocates nothing.
+ */
+bst_status bst_wait_check(uint64_t timeout_ns, int32_t arrive, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

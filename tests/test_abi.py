@@ -84,6 +84,9 @@ def test_argument_errors_need_no_device(lib):
                                 None, None) == bst.ERR_INVALID_ARG
     assert lib.bst_swizzle_map(10, 10, 0, 4, 1, None, 1, None) == bst.ERR_INVALID_ARG
     assert lib.bst_swizzle_map(1 << 31, 1 << 31, 1, 1, 1, None, 1, None) == bst.ERR_INVALID_ARG
+    # the bounded-wait self-check: its limit is checked before any device work
+    assert lib.bst_wait_check(0, 0, None) == bst.ERR_INVALID_ARG
+    assert lib.bst_wait_check(10_000_000_001, 1, None) == bst.ERR_INVALID_ARG
 
 
 def test_noalloc_rejects_oversize_without_a_device(lib):

@@ -433,14 +433,15 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     return cuda_status(launch_dense(p, bn, grid, stream));
 }
 
-// MXFP8 tile width and split-K.  One thread issues every MMA of a CTA, and
-// the issue cost per k-block (about 0.42 us at 128 columns, 0.45 us at 256)
-// barely depends on the width, so wide tiles win whenever they can fill the
-// GPU; split-K over clusters of S CTAs (one tile per cluster) lets 128 x 256
-// tiles do so.  Cost = waves x k-blocks per CTA x per-k-block time, plus about
-// 7 us for a split (the exchange and finish of the partials through
-// distributed shared memory, and the cluster launch, measured on a 128 x 256
-// tile).  splits = 0 on return: a forced split this problem cannot take.
+// MXFP8 tile width and split-K.  The per-k-block cost of the MMA loop (about
+// 0.41 us at 128 columns, 0.44 us at 256, with the operands arriving from
+// DRAM) barely depends on the width, so wide tiles win whenever they can fill
+// the GPU; split-K over clusters of S CTAs (one tile per cluster) lets
+// 128 x 256 tiles do so.  Cost = waves x k-blocks per CTA x per-k-block time,
+// plus about 4 us for a split (the cluster launch, and the exchange and finish
+// of the partials through distributed shared memory by two warp groups,
+// measured on 128 x 256 tiles of 1024 x 2048 x 4096).  splits = 0 on return:
+// a forced split this problem cannot take.
 bst_status choose_mx(const Sched& sch, uint64_t loops_m, uint64_t N, uint32_t num_kb, uint32_t sms, uint32_t& bn,
                      uint32_t& splits) {
     auto tiles_of = [&](uint32_t w) { return loops_m * ((N + w - 1) / w); };
@@ -466,10 +467,7 @@ bst_status choose_mx(const Sched& sch, uint64_t loops_m, uint64_t N, uint32_t nu
             if (s > 1 && (sch.split_k == 1 || num_kb < 4 * s || !split_ok(w, s))) continue;
             const uint64_t ctas = s > 1 ? tiles_of(w) * s : tiles_of(w);
             const double waves = static_cast<double>((ctas + sms - 1) / sms);
-            // measured with the operands arriving from DRAM (1024 x 2048 x
-            // 4096): 0.45 / 0.42 us per k-block, and about 7 us more for the
-            // cluster launch and exchange of a split
-            const double cost = waves * ((num_kb + s - 1) / s) * (w == 256 ? 0.45 : 0.42) + (s > 1 ? 7.0 : 0.0);
+            const double cost = waves * ((num_kb + s - 1) / s) * (w == 256 ? 0.44 : 0.41) + (s > 1 ? 4.0 : 0.0);
             if (cost < best * 0.999) { best = cost; bn = w; splits = s; }
         }
     }

@@ -153,7 +153,7 @@ struct GemmLayout {
     static constexpr uint32_t kRawOff = (kSfOff + STAGES * kSfStageBytes + 1023) & ~1023u;
     static constexpr uint32_t kEpiOff = kRawOff + 2 * kRawSlotBytes;       // 4 epilogue warps x 4 KB staging
     static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
-    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2 + 4; // ..., drain, raw_full[2], recv[4]
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2 + 8; // ..., drain, raw_full[2], recv[8]
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
     // TMEM: ACC accumulators of BN fp32 columns, then (MXFP8) per stage 4
@@ -174,6 +174,18 @@ struct GemmLayout {
     static_assert(SPLIT == 1 || (ACC == 1 && kSplitW % 32 == 0 &&
                                  2 * kSplitSlots * kSplitSlotBytes <= STAGES * kStageBytes),
                   "split-K slots reuse the ring");
+    // Split-K epilogue groups: warps 2-5, and (kSplitEH = 2) warps 0, 1, 6, 7,
+    // idle once the main loop is done; the group of warp w sums and stores
+    // columns [h*kSplitWH, (h+1)*kSplitWH) of each split's W in TMEM lane
+    // quarter w % 4.  The second group stages its stores in the ring, after
+    // the send staging.
+    static constexpr uint32_t kSplitEH =
+        (SPLIT > 1 && kSplitW >= 64 && 2 * kSplitSlots * kSplitSlotBytes + 4 * kEpiWarpBytes <= STAGES * kStageBytes)
+            ? 2u : 1u;
+    static constexpr uint32_t kSplitWH = kSplitW / kSplitEH;
+    static constexpr uint32_t kSplitSubBytes = 32 * kSplitWH * 4;    // one warp's rows of its kSplitWH columns
+    static constexpr uint32_t kSplitEpi1Off = 2 * kSplitSlots * kSplitSlotBytes;
+    static_assert(kSplitWH % 32 == 0, "whole 32-column chunks per split and group");
     static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
 };
 
@@ -603,13 +615,14 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         mbar_init(drain, 1);
         mbar_init(&raw_full[0], 1);
         mbar_init(&raw_full[1], 1);
-        for (uint32_t o = 0; o < 4; ++o) mbar_init(&recv[o], 1);
+        for (uint32_t o = 0; o < 8; ++o) mbar_init(&recv[o], 1);
         *abort_flag = 0;
         *tiles_smem = prm.g.total_tiles;
         fence_barrier_init();
         // split-K: each epilogue warp's receive barrier expects SPLIT-1 partials
         if (SPLIT > 1)
-            for (uint32_t o = 0; o < 4; ++o) mbar_arrive_expect_tx(&recv[o], (SPLIT - 1) * Lay::kSplitSlotBytes);
+            for (uint32_t o = 0; o < 4 * Lay::kSplitEH; ++o)
+                mbar_arrive_expect_tx(&recv[o], (SPLIT - 1) * Lay::kSplitSubBytes);
     }
     if (warp == 0 && lane == 0) {
         if (a_tma) prefetch_tmap(&prm.tmap_a);
@@ -1055,31 +1068,37 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // Every CTA of the cluster is past its main loop (its ring is idle)
         // once this barrier completes.  Split g finishes columns [g*W,
         // (g+1)*W) of the tile.  Every epilogue warp stages, for each other
-        // split g, its 32 rows of g's columns in its own ring (row per lane,
-        // 16-byte granules XOR-swizzled by row) and bulk-copies them into a
-        // receive slot of CTA g, completing on that CTA's receive barrier of
-        // the same warp; it then adds the SPLIT-1 partials it received to its
-        // own rows of its own columns, rounds once and stores.
+        // split g, its 32 rows of its group's half (or all) of g's columns in
+        // the ring (row per lane, 16-byte granules XOR-swizzled by row) and
+        // bulk-copies them into a receive slot of CTA g, completing on that
+        // CTA's receive barrier of the same warp; it then adds the SPLIT-1
+        // partials it received to its own rows of its own columns, rounds once
+        // and stores.
         __syncwarp();
         tc_fence_before();
         cluster_sync();                                  // also orders this CTA's own warps
         tc_fence_after();
-        if (warp >= 2 && warp < 6 && t_first < total_tiles) {
-            constexpr uint32_t W = Lay::kSplitW;
-            constexpr uint32_t kSlot = Lay::kSplitSlotBytes;
+        const bool epi_main = warp >= 2 && warp < 6;
+        if ((epi_main || (Lay::kSplitEH == 2 && (warp < 2 || warp >= 6))) && t_first < total_tiles) {
+            constexpr uint32_t W = Lay::kSplitW, WH = Lay::kSplitWH, EH = Lay::kSplitEH;
+            constexpr uint32_t kSlot = Lay::kSplitSubBytes;
             const uint32_t q = warp & 3u;
+            const uint32_t h = epi_main ? 0u : 1u;       // column group of this warp
+            const uint32_t qh = q * EH + h;              // receive barrier and slot group
             const uint32_t taddr = tmem_base + ((q * 32) << 16);
-            const bool own_valid = acc_ok && has_k;      // else this split's partial counts as zero
+            // warps 2-5 waited for the accumulator before the barrier; the
+            // second group relies on that wait (no abort recorded since)
+            const bool own_valid = (epi_main ? acc_ok : *abort_flag == 0) && has_k;   // else zeros
             uint32_t gi = 0;
 #pragma unroll 1
             for (uint32_t g = 0; g < SPLIT; ++g) {
                 if (g == split) continue;
-                uint8_t* stage_rows = smem + Lay::kSplitSendOff + (q * (SPLIT - 1) + gi) * kSlot;
-                uint8_t* my_row = stage_rows + lane * (W * 4);
+                uint8_t* stage_rows = smem + Lay::kSplitSendOff + (qh * (SPLIT - 1) + gi) * kSlot;
+                uint8_t* my_row = stage_rows + lane * (WH * 4);
 #pragma unroll 1
-                for (uint32_t cc = 0; cc < W / 32; ++cc) {
+                for (uint32_t cc = 0; cc < WH / 32; ++cc) {
                     uint32_t v[32];
-                    if (own_valid) tmem_ld_32x32b_x32(taddr + g * W + cc * 32, v);
+                    if (own_valid) tmem_ld_32x32b_x32(taddr + g * W + h * WH + cc * 32, v);
                     else {
 #pragma unroll
                         for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
@@ -1094,27 +1113,27 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 fence_proxy_async_smem();                // generic writes -> the bulk copy's reads
                 __syncwarp();
                 if (lane == 0) {
-                    const uint32_t slot = q * (SPLIT - 1) + (split < g ? split : split - 1);
+                    const uint32_t slot = qh * (SPLIT - 1) + (split < g ? split : split - 1);
                     const uint32_t dst = map_to_cta(smem_u32(smem + slot * kSlot), g);
-                    const uint32_t bar = map_to_cta(smem_u32(&recv[q]), g);
+                    const uint32_t bar = map_to_cta(smem_u32(&recv[qh]), g);
                     bulk_copy_to_cluster(dst, stage_rows, kSlot, bar);
                     bulk_commit_group();
                 }
                 ++gi;
             }
-            const bool got = warp_wait(&recv[q], 0, ctl, 5);
+            const bool got = warp_wait(&recv[qh], 0, ctl, 5);
             const TileInfo ti = tile_info(sa, t_first, kBM, BN, gt);
-            const uint8_t* slots = smem + q * (SPLIT - 1) * kSlot + lane * (W * 4);
+            const uint8_t* slots = smem + qh * (SPLIT - 1) * kSlot + lane * (WH * 4);
             const uint32_t rows_valid = ti.m_act > q * 32 ? min(32u, ti.m_act - q * 32) : 0u;
             const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec;
             const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
             const int64_t ldc = prm.g.ldc;
             uint8_t* const cwarp = prm.g.C + static_cast<int64_t>(ti.row0 + q * 32) * ldc * csize;
-            uint8_t* const epi_stage = smem + Lay::kEpiOff + q * kEpiWarpBytes;
+            uint8_t* const epi_stage = smem + (h ? Lay::kSplitEpi1Off : Lay::kEpiOff) + q * kEpiWarpBytes;
 #pragma unroll 1
-            for (uint32_t cc = 0; cc < W / 32; ++cc) {
+            for (uint32_t cc = 0; cc < WH / 32; ++cc) {
                 uint32_t v[32];
-                if (own_valid) tmem_ld_32x32b_x32(taddr + split * W + cc * 32, v);
+                if (own_valid) tmem_ld_32x32b_x32(taddr + split * W + h * WH + cc * 32, v);
                 else {
 #pragma unroll
                     for (uint32_t j = 0; j < 32; ++j) v[j] = 0u;
@@ -1133,13 +1152,13 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         }
                     }
                 }
-                const uint32_t col = split * W + cc * 32;    // column within the tile
+                const uint32_t col = split * W + h * WH + cc * 32;   // column within the tile
                 if (rows_valid && col < ti.n_act)
                     store_chunk_coalesced(epi_stage, c_type, c_vec, cwarp + static_cast<int64_t>(ti.n * BN + col) * csize,
                                           ldc * csize, rows_valid, min(32u, ti.n_act - col), v, lane);
             }
             if (lane == 0) bulk_wait_read_all();         // the ring may not be left while being read
-            if (prm.g.trace && split == 0 && q == 0 && lane == 0 && t_first < prm.g.trace_cap) {
+            if (prm.g.trace && split == 0 && q == 0 && h == 0 && lane == 0 && t_first < prm.g.trace_cap) {
                 uint32_t* tr = prm.g.trace + static_cast<uint64_t>(t_first) * 5;
                 tr[0] = ti.tag; tr[1] = ti.m; tr[2] = ti.n; tr[3] = ti.m_act; tr[4] = ti.n_act;
             }

@@ -3,15 +3,18 @@
 // One CTA per SM walks the task indices t = blockIdx.x, blockIdx.x + grid,
 // ... ; each task index is turned into an output tile by the block-swizzle
 // scheduler (sched.cuh, "Block Scheduler Code Explained" sections 4-7).
-// Roles inside the CTA (192 threads):
+// Roles inside the CTA (224 threads, 256 for MXFP8):
 //   warp 0     producer: per k-block waits for a free shared-memory stage and
-//              fills it (TMA, or cp.async for operands TMA cannot take; MXFP8
-//              scale factors by cp.async) -- the counterpart of the GM->L1
-//              copies of "Block Dispatch Policies" (MmadAtlasA2Preload /
-//              PreloadAsync: the producer runs ahead across tile and group
+//              fills it (lane 0 issues the A loads by TMA; the warp copies
+//              operands TMA cannot take by cp.async) -- the counterpart of the
+//              GM->L1 copies of "Block Dispatch Policies" (MmadAtlasA2Preload
+//              / PreloadAsync: the producer runs ahead across tile and group
 //              boundaries, i.e. inter-block and inter-group preloading).
-//   warp 1     MMA issuer: one thread issues tcgen05.mma into a TMEM
-//              accumulator, releasing each stage with tcgen05.commit.
+//              Lane 0 of warp 6 (7 for MXFP8) issues the B loads; for MXFP8,
+//              warp 6 lays out the scale factors.
+//   warp 1     MMA issuer: the whole warp waits on each stage, lane 0 issues
+//              tcgen05.mma into a TMEM accumulator and releases the stage with
+//              tcgen05.commit.
 //   warps 2-5  epilogue: TMEM -> registers -> global, with the tail tile cut
 //              by GetActualBlockShape (section 4.6); the accumulator is
 //              double-buffered so the epilogue of tile i overlaps the MMAs of

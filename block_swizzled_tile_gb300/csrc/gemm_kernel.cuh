@@ -154,8 +154,10 @@ struct GemmLayout {
     static constexpr uint32_t kRawRowsA = 128;
     static constexpr uint32_t kRawSlotBytes = KIND == kKindMXF8 ? (kRawRowsA + BN) * 16u : 0u;
     static constexpr uint32_t kRawOff = (kSfOff + STAGES * kSfStageBytes + 1023) & ~1023u;
-    static constexpr uint32_t kEpiOff = kRawOff + 2 * kRawSlotBytes;       // 4 epilogue warps x 4 KB staging
-    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiWarpBytes;
+    // 4 epilogue warps x 4 KB staging; split-K stages its stores in the idle
+    // ring instead (after the main loop), which leaves room for a deeper ring
+    static constexpr uint32_t kEpiOff = kRawOff + 2 * kRawSlotBytes;
+    static constexpr uint32_t kBarOff = kEpiOff + (SPLIT > 1 ? 0u : 4 * kEpiWarpBytes);
     static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2 + 8; // ..., drain, raw_full[2], recv[8]
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
@@ -180,15 +182,18 @@ struct GemmLayout {
     // Split-K epilogue groups: warps 2-5, and (kSplitEH = 2) warps 0, 1, 6, 7,
     // idle once the main loop is done; the group of warp w sums and stores
     // columns [h*kSplitWH, (h+1)*kSplitWH) of each split's W in TMEM lane
-    // quarter w % 4.  The second group stages its stores in the ring, after
-    // the send staging.
+    // quarter w % 4.  Both groups stage their stores in the ring, after the
+    // receive slots and the send staging.
     static constexpr uint32_t kSplitEH =
-        (SPLIT > 1 && kSplitW >= 64 && 2 * kSplitSlots * kSplitSlotBytes + 4 * kEpiWarpBytes <= STAGES * kStageBytes)
+        (SPLIT > 1 && kSplitW >= 64 && 2 * kSplitSlots * kSplitSlotBytes + 8 * kEpiWarpBytes <= STAGES * kStageBytes)
             ? 2u : 1u;
     static constexpr uint32_t kSplitWH = kSplitW / kSplitEH;
     static constexpr uint32_t kSplitSubBytes = 32 * kSplitWH * 4;    // one warp's rows of its kSplitWH columns
-    static constexpr uint32_t kSplitEpi1Off = 2 * kSplitSlots * kSplitSlotBytes;
+    static constexpr uint32_t kSplitEpi0Off = 2 * kSplitSlots * kSplitSlotBytes;
+    static constexpr uint32_t kSplitEpi1Off = kSplitEpi0Off + 4 * kEpiWarpBytes;
     static_assert(kSplitWH % 32 == 0, "whole 32-column chunks per split and group");
+    static_assert(SPLIT == 1 || kSplitEpi0Off + kSplitEH * 4 * kEpiWarpBytes <= STAGES * kStageBytes,
+                  "split-K store staging in the ring");
     static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
 };
 
@@ -1132,7 +1137,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             const uint32_t csize = c_type == kOutF32 ? 4u : 2u;
             const int64_t ldc = prm.g.ldc;
             uint8_t* const cwarp = prm.g.C + static_cast<int64_t>(ti.row0 + q * 32) * ldc * csize;
-            uint8_t* const epi_stage = smem + (h ? Lay::kSplitEpi1Off : Lay::kEpiOff) + q * kEpiWarpBytes;
+            uint8_t* const epi_stage = smem + (h ? Lay::kSplitEpi1Off : Lay::kSplitEpi0Off) + q * kEpiWarpBytes;
 #pragma unroll 1
             for (uint32_t cc = 0; cc < WH / 32; ++cc) {
                 uint32_t v[32];

@@ -80,7 +80,7 @@ struct MxSplit {
 };
 
 cudaError_t launch_mxf8_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream) {
-    if (bn == 256 && splits == 2) return MxSplit<256, kMxStages256, 2>::launch(p, tiles, stream);
+    if (bn == 256 && splits == 2) return MxSplit<256, kMxSplitStages256, 2>::launch(p, tiles, stream);
     if (bn == 128 && splits == 2) return MxSplit<128, kMxStages128, 2>::launch(p, tiles, stream);
     if (bn == 128 && splits == 4) return MxSplit<128, kMxStages128, 4>::launch(p, tiles, stream);
     return cudaErrorInvalidValue;
@@ -89,7 +89,7 @@ cudaError_t launch_mxf8_split(const GemmParams& p, uint32_t bn, uint32_t splits,
 // 0 when there is no such instantiation
 cudaError_t mxf8_split_resident(uint32_t bn, uint32_t splits, uint32_t* out) {
     *out = 0;
-    if (bn == 256 && splits == 2) return MxSplit<256, kMxStages256, 2>::resident(out);
+    if (bn == 256 && splits == 2) return MxSplit<256, kMxSplitStages256, 2>::resident(out);
     if (bn == 128 && splits == 2) return MxSplit<128, kMxStages128, 2>::resident(out);
     if (bn == 128 && splits == 4) return MxSplit<128, kMxStages128, 4>::resident(out);
     return cudaSuccess;

@@ -118,6 +118,9 @@ cudaError_t launch_swizzle_map_grouped(const int32_t* group_m, uint32_t G, uint3
 // Configurations instantiated for each kernel family.
 constexpr uint32_t kDenseStages64 = 8, kDenseStages128 = 6, kDenseStages256 = 4;
 constexpr uint32_t kMxStages128 = 6, kMxStages256 = 3;
+// split-K tiles stage their epilogue stores in the idle ring, so 128 x 256
+// split tiles fit a fourth stage (more bytes in flight per SM)
+constexpr uint32_t kMxSplitStages256 = 4;
 constexpr uint32_t kDequantStages = 6;
 constexpr uint32_t kPairStages128 = 8, kPairStages256 = 6;
 constexpr uint32_t kPairDequantStages = 5;

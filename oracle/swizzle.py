@@ -13,7 +13,7 @@ scheduling, snake scanning, tail blocks) and section 6
 All arithmetic is on exact Python integers, so no wrap-around of the page's
 uint32 products can occur here.
 
-Readings where the page is silent (each one is listed in the design doc):
+Readings taken where the page is silent:
 * CeilDiv is never printed: it is the integer ceiling ceil(a / b).
 * The Nz body of GetBlockCoord is elided ("similar Nz direction processing
   logic").  Section 4.5's prose says Nz windows are SwizzleOffset *columns*

@@ -51,7 +51,7 @@ constexpr uint32_t kClcDepth = 4;
 
 // The task sequence of one role of a CTA pair.
 //   Static: t = cid, cid + nclusters, ... (a persistent grid).
-//   Dynamic (the "dynamic task allocation" that "Block Scheduler Code
+//   Dynamic (dynamic task allocation, which "Block Scheduler Code
 //   Explained" lists among the scheduler's policies): the grid holds one
 //   cluster per task.  A cluster starts with its own task and then takes the
 //   tasks of clusters that have not started yet, which the leader's A-load

@@ -11,8 +11,8 @@
 //    32 bits for any offset the caller passes.
 //  * the Nz branch, elided on the page, is the transpose of Zn: windows of
 //    SwizzleOffset tile-columns, n fastest inside a window, m reversed on odd
-//    windows (the page's prose: "divided by column", "reverses the N-dimension
-//    or M-dimension index").
+//    windows (the page's prose divides the grid by columns for Nz and has the
+//    snake reverse the index along the window).
 #pragma once
 #include <cstdint>
 

@@ -15,12 +15,12 @@ uint32 products can occur here.
 
 Readings taken where the page is silent:
 * CeilDiv is never printed: it is the integer ceiling ceil(a / b).
-* The Nz body of GetBlockCoord is elided ("similar Nz direction processing
-  logic").  Section 4.5's prose says Nz windows are SwizzleOffset *columns*
-  wide and that the snake reverses "the N-dimension or M-dimension index";
-  the reading taken is the exact transpose of the Zn branch: windows of
-  SwizzleOffset tile-columns, n fastest inside a window, the last window
-  narrower, m reversed on odd windows.  Parity of this branch is pinned only
+* The Nz body of GetBlockCoord is elided: the page only says it mirrors the
+  Zn logic.  Section 4.5's prose gives Nz windows a width of SwizzleOffset
+  tile-columns and has the snake reverse the index of whichever dimension the
+  window runs along; the reading taken is the exact transpose of the Zn
+  branch: windows of SwizzleOffset tile-columns, n fastest inside a window,
+  the last window narrower, m reversed on odd windows.  Parity of this branch is pinned only
   by invariants and closed forms (bijection, exact cover, window shape,
   snake, row-major order when SwizzleOffset >= loopsN).
 * GemmCoord{mIdx, nIdx, 0} are tile indices; the tile's first element is

@@ -50,13 +50,18 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
 def csrc_hash():
-    """Hash of the CUDA sources, so stored profiler counters are only used
-    for the kernel they were taken from."""
+    """Hash of the CUDA sources' code (comments and whitespace removed), so
+    stored profiler counters are only used for the kernels they were taken
+    from, and an edit of a comment does not discard them."""
+    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_swizzled_tile_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(f.encode() + " ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

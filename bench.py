@@ -49,19 +49,23 @@ METRIC = "GEMM TFLOP/s at 1 GB300 and % of dtype dense tensor peak"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
+def code_text(src):
+    """C/C++ source with its comments removed and its whitespace collapsed."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def csrc_hash():
     """Hash of the CUDA sources' code (comments and whitespace removed), so
     stored profiler counters are only used for the kernels they were taken
     from, and an edit of a comment does not discard them."""
-    import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_swizzled_tile_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         with open(os.path.join(d, f), encoding="utf-8") as fh:
-            src = fh.read()
-        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-        src = re.sub(r"//[^\n]*", " ", src)
-        h.update(f.encode() + " ".join(src.split()).encode())
+            h.update(f.encode() + code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -38,9 +38,18 @@ thread_local uint64_t t_timeout_ns = 0;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+// The device whose primary context this host thread has made current (-1:
+// none yet).  cudaGetDevice binds no context, and a thread that has made no
+// other runtime call would reach the driver's tensor-map encoder without one.
+thread_local int t_bound_dev = -1;
+
 bst_status device_info(DeviceInfo& out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BST_ERR_CUDA;
+    if (t_bound_dev != dev) {
+        if (cudaSetDevice(dev) != cudaSuccess) return BST_ERR_CUDA;   // makes its primary context current
+        t_bound_dev = dev;
+    }
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     DeviceInfo& d = g_dev[dev];
     if (!d.ready) {

@@ -529,14 +529,17 @@ namespace bst {
 // The S fp32 partial tiles are summed on chip.  Split g finishes columns
 // [g*W, (g+1)*W) (W = BN/S) of each CTA's 128 rows.  Once its pair's MMAs are
 // done (the stage ring is then idle), every epilogue warp copies, for each
-// other split g, its 32 rows of g's columns into its own ring, and one bulk
-// copy moves them into a receive slot of the CTA of split g (same half),
-// completing on that CTA's receive barrier of the same warp.  The receive
-// slots sit outside the ring, so a sender never waits for the receiver.  The
-// warp then adds the S-1 slots it received to its own rows of its own
-// columns, rounds once and stores them through the coalesced epilogue.  All
-// four warps send and finish in parallel; nothing goes through global memory
-// and no second kernel runs.
+// other split g, its 32 rows of its share of g's columns into the ring, and
+// one bulk copy moves them into a receive slot of the CTA of split g (same
+// half), completing on that CTA's receive barrier of the same warp.  The
+// receive slots sit outside the ring, so a sender never waits for the
+// receiver.  The warp then adds the S-1 slots it received to its own rows of
+// its share of its own columns, rounds once and stores them through the
+// coalesced epilogue.  The epilogue warps are 2-5 and, when the ring has room
+// (W >= 64), also 0, 1, 6 and 7 once their loads and MMAs are issued: two
+// warps per TMEM lane quarter, each with half of the columns.  All send and
+// finish in parallel; nothing goes through global memory and no second
+// kernel runs.
 //
 // Shared-memory rows of a partial (W fp32) keep their 16-byte granules
 // XOR-swizzled by row (granule c at c ^ (row % 8)), so both the row-per-lane

@@ -144,3 +144,91 @@ def test_e8m0():
     v = formats.decode_e8m0(np.array([127, 128, 126, 0, 254, 255], np.uint8))
     assert v[0] == 1.0 and v[1] == 2.0 and v[2] == 0.5
     assert v[3] == 2.0 ** -127 and v[4] == 2.0 ** 127 and np.isnan(v[5])
+
+
+def _decode_binary32_by_fields(bits):
+    """IEEE binary32 from its fields: 1 sign, 8 exponent (bias 127), 23
+    mantissa; float64 holds every binary32 value exactly."""
+    b = np.asarray(bits, dtype=np.uint64)
+    s = np.where(b >> 31, -1.0, 1.0)
+    e = ((b >> 23) & 0xFF).astype(np.int64)
+    m = (b & 0x7FFFFF).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -149, (1.0 + m / 2.0 ** 23) * np.ldexp(1.0, (e - 127).clip(-126, 127)))
+    val = np.where(e == 0xFF, np.where(m == 0, np.inf, np.nan), val)
+    return s * val
+
+
+def _f32_nearest_even_check(x, got_bits):
+    """The defining property of round-to-nearest-even into binary32, checked
+    on each x against the two binary32 codes next to the result (bit pattern
+    +-1 of the same sign; zero's neighbours are the smallest subnormals):
+    the result is no farther from x than either neighbour, a tie goes to the
+    even code, and a result of +-inf means |x| reached the overflow bound
+    2**128 - 2**103 (halfway between the largest finite value and 2**128)."""
+    bad = []
+    for xi, gb in zip(x.tolist(), got_bits.tolist()):
+        y = float(_decode_binary32_by_fields(np.array([gb]))[0])
+        if np.isinf(y):
+            if not (abs(xi) >= 2.0 ** 128 - 2.0 ** 103 and np.sign(y) == np.sign(xi)):
+                bad.append(xi)
+            continue
+        mag = gb & 0x7FFFFFFF
+        sign = gb & 0x80000000
+        neigh = []
+        for dm in (-1, 1):
+            nm = mag + dm
+            if nm < 0:
+                neigh.append((0x80000000 ^ sign) | 1)       # across zero: the other sign's smallest subnormal
+            elif nm <= 0x7F7FFFFF:
+                neigh.append(sign | nm)
+        d = abs(y - xi)
+        for nb in neigh:
+            v = float(_decode_binary32_by_fields(np.array([nb]))[0])
+            dn = abs(v - xi)
+            if dn < d or (dn == d and v != y and (gb & 1) and not (nb & 1)):
+                bad.append(xi)
+                break
+    return bad
+
+
+def test_f64_to_f32_matches_nearest_even_neighbour_search():
+    rng = np.random.default_rng(4)
+    # random doubles over many binades (their low 29 bits are what rounding drops)
+    rnd = rng.standard_normal(4000) * 10.0 ** rng.integers(-40, 38, 4000)
+    # exact ties: the midpoint of two adjacent binary32 values, both parities
+    lo_bits = rng.integers(0x00800000, 0x7F7FFFFF, 3000).astype(np.uint64)
+    lo = _decode_binary32_by_fields(lo_bits)
+    hi = _decode_binary32_by_fields(lo_bits + 1)
+    mids = (lo + hi) / 2                                   # exact in float64
+    near = mids * (1 + rng.uniform(-1e-12, 1e-12, 3000))
+    edges = [2.0 ** -149, 2.0 ** -150, 3 * 2.0 ** -150, 5 * 2.0 ** -151, 2.0 ** -126, 2.0 ** -126 - 2.0 ** -150,
+             float(np.finfo(np.float32).max), 2.0 ** 128 - 2.0 ** 104, 2.0 ** 128 - 2.0 ** 103,
+             2.0 ** 128 - 2.0 ** 103 - 2.0 ** 70, 1e39, 0.0, 1.0, -1.0 - 2.0 ** -24, 1.0 + 2.0 ** -24,
+             1.0 + 3 * 2.0 ** -24]
+    x = np.concatenate([rnd, mids, -mids[:500], near, edges, [-e for e in edges]])
+    with np.errstate(over="ignore"):
+        got = formats.f64_to_f32(x)
+    assert got.dtype == np.float32
+    assert _f32_nearest_even_check(x, got.view(np.uint32)) == []
+
+
+def test_f32_neighbour_check_catches_a_planted_truncation():
+    """Truncation toward zero (a plausible mistake in an f32 encoder) must
+    fail the nearest-even check above."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(2000) * 10.0 ** rng.integers(-20, 20, 2000)
+    trunc = x.astype(np.float32)
+    up = np.abs(trunc.astype(np.float64)) > np.abs(x)
+    trunc[up] = np.nextafter(trunc[up], np.float32(0))
+    assert len(_f32_nearest_even_check(x, trunc.view(np.uint32))) > 100
+
+
+def test_binary32_field_decoder_known_values():
+    known = {0x3F800000: 1.0, 0xC0000000: -2.0, 0x00000001: 2.0 ** -149, 0x00800000: 2.0 ** -126,
+             0x7F7FFFFF: (2 - 2.0 ** -23) * 2.0 ** 127, 0x7F800000: np.inf, 0x00000000: 0.0, 0x3EAAAAAB: None}
+    for b, v in known.items():
+        got = float(_decode_binary32_by_fields(np.array([b]))[0])
+        if v is None:
+            assert abs(got - 1 / 3) < 2.0 ** -25
+        else:
+            assert got == v

@@ -63,13 +63,66 @@ def test_as_logical_layouts():
     assert np.array_equal(cm, flat.reshape(3, 7)[:, :5].T)
 
 
-def test_batched_is_per_batch():
-    w = wl.dense16(20, 30, 40, "bf16", seed=1, batch=3)
-    a = og.decode(w["a"], "bf16")
-    b = og.decode(w["b"], "bf16")
-    got = og.gemm_batched(a, b, "bf16")
-    for i in range(3):
-        assert np.array_equal(got[i], og.gemm(a[i], b[i], "bf16"))
+def test_batched_closed_form():
+    """Batch i multiplies its own A_i by B_i = (i+1) * I, so output batch i is
+    (i+1) * A_i rounded once; a mixed-up batch index or a shared operand
+    fails it."""
+    batch, M, K = 4, 9, 12
+    g = wl._gen(31)
+    a = np.stack([og.decode(wl.uniform16((M, K), -1, 1, "bf16", g), "bf16") for _ in range(batch)])
+    b = np.stack([(i + 1) * np.eye(K) for i in range(batch)])
+    got = formats.bf16_bits_to_f64(og.gemm_batched(a, b, "bf16"))
+    for i in range(batch):
+        want = formats.bf16_bits_to_f64(formats.f64_to_bf16_bits((i + 1) * a[i]))
+        assert np.array_equal(got[i], want)
+    assert not np.array_equal(got[0], got[1])
+
+
+def _triple_loop_f64(a, b):
+    """sum_k a[i,k]*b[k,j] by an explicit loop over i, j, k in float64."""
+    M, K = a.shape
+    N = b.shape[1]
+    out = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(a[i, k]) * float(b[k, j])
+            out[i, j] = s
+    return out
+
+
+def _triple_loop_int(a, b):
+    M, K = a.shape
+    N = b.shape[1]
+    return [[sum(int(a[i, k]) * int(b[k, j]) for k in range(K)) for j in range(N)] for i in range(M)]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_matmul_primitive_agrees_with_triple_loop(dtype):
+    """The oracle's float64 product uses numpy's matmul as a library
+    primitive; an explicit triple loop (the plain definition) must give the
+    same sums.  The two differ only in summation order, so they agree to
+    float64 rounding, and after the one rounding to the output type they
+    are identical on these shapes."""
+    g = wl._gen(32)
+    for M, N, K in [(1, 1, 1), (3, 4, 5), (7, 5, 33), (16, 9, 70), (2, 3, 0)]:
+        a = og.decode(wl.uniform16((M, K), -1, 1, dtype, g), dtype)
+        b = og.decode(wl.uniform16((K, N), -1, 1, dtype, g), dtype)
+        loop = _triple_loop_f64(a, b)
+        prim = og.gemm_f64(a, b)
+        assert np.allclose(prim, loop, rtol=1e-14, atol=1e-300)
+        assert np.array_equal(og.round_out(loop, dtype), og.gemm(a, b, dtype))
+
+
+def test_int_primitive_agrees_with_triple_loop():
+    g = wl._gen(33)
+    for M, N, K in [(4, 3, 1), (6, 5, 17), (3, 7, 129)]:
+        a = wl.uniform_int8((M, K), g)
+        b = wl.uniform_int8((K, N), g)
+        assert og.int_gemm_exact(a, b).tolist() == _triple_loop_int(a, b)
+        acc, _ = og.gemm_quant_per_token(a, b, np.ones(M, np.float32), np.ones(N, np.float32))
+        assert acc.tolist() == _triple_loop_int(a, b)
 
 
 def test_grouped_closed_form():

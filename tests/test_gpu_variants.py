@@ -1,6 +1,8 @@
 """GPU parity of the grouped slice-M, MXFP8 and int8 per-token-dequant paths
 against the CPU oracle, at small ragged sizes and at the full workload sizes
-(full sizes compare a seeded sample of whole output rows)."""
+(full sizes compare every output element)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -38,22 +40,6 @@ def run_grouped(w, sched=None, b_col_major=False, out="bf16"):
     return decode_out(raw.copy(), out)
 
 
-def oracle_grouped_rows(w, rows, out="bf16"):
-    """Oracle output for the given global rows: row i of group g is
-    round(x[i] . w[g])."""
-    gm = w["group_m"]
-    off = np.concatenate([[0], np.cumsum(gm)])
-    x = og.decode(w["x"], "bf16")
-    res = np.zeros((len(rows), w["N"]))
-    rows = np.asarray(rows)
-    for g in range(len(gm)):
-        sel = np.nonzero((rows >= off[g]) & (rows < off[g + 1]))[0]
-        if len(sel):
-            wg = og.decode(w["w"][g], "bf16")
-            res[sel] = decode_out(og.gemm(x[rows[sel]], wg, out), out)
-    return res
-
-
 @pytest.mark.parametrize("gm", [[3, 0, 130, 1, 0, 257], [0, 0, 64], [200], [1] * 17, [300, 0, 513]])
 @pytest.mark.parametrize("bcol", [False, True])
 def test_grouped_small(gm, bcol):
@@ -83,15 +69,24 @@ def test_grouped_inconsistent_sizes_reported():
     bst.check_async()      # the error word was cleared
 
 
-@pytest.mark.parametrize("forced", [None, [0, 2048, 0, 1024, 3072, 0, 2048, 0]])
+@functools.lru_cache(maxsize=1)
+def _grouped_full_oracle(forced):
+    w = wl.grouped_bf16(group_m=None if forced is None else list(forced))
+    ref = decode_out(og.gemm_grouped(og.decode(w["x"], "bf16"), og.decode(w["w"], "bf16"), w["group_m"], "bf16"),
+                     "bf16")
+    return w, ref
+
+
+@pytest.mark.parametrize("forced", [None, (0, 2048, 0, 1024, 3072, 0, 2048, 0)])
 @pytest.mark.parametrize("tm", [0, 128, 256])
 def test_grouped_full_workload(forced, tm):
-    """G=8 groups summing to 8192 rows, K=N=4096, bf16; sampled rows."""
-    w = wl.grouped_bf16(group_m=forced)
-    got = run_grouped(w, bst.sched(1, 0, tile_m=tm))
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(sum(w["group_m"]), 384, replace=False))
-    assert_close_f16(got[rows], oracle_grouped_rows(w, rows))
+    """G=8 groups summing to 8192 rows, K=N=4096, bf16: every element of the
+    output against the oracle (tm 0 is the automatic choice the bench
+    times)."""
+    w, ref = _grouped_full_oracle(forced)
+    for S, d in ([(1, 0), (8, 1)] if tm == 0 else [(1, 0)]):
+        got = run_grouped(w, bst.sched(S, d, tile_m=tm))
+        assert_close_f16(got, ref)
 
 
 # --------------------------------------------------------------- MXFP8 -----
@@ -192,21 +187,23 @@ def test_mxfp8_full_workload():
 
 # ---------------------------------------------------------------- int8 -----
 
-def run_int8(w, b_col_major=True, sched=None):
+def run_int8(w, b_col_major=True, sched=None, with_acc=True):
+    """One bst_gemm_quant_per_token call; with_acc=False passes acc_out =
+    NULL (the call the bench times) and returns acc None."""
     M, N, K = w["M"], w["N"], w["K"]
     Bst = w["b"] if b_col_major else np.ascontiguousarray(w["b"].T)
     A, B = dev(w["a"]), dev(Bst)
     SA, SB = dev(w["sa"]), dev(w["sb"])
     cbuf, C = empty_bytes(M * N * 2, CANARY)
-    abuf, ACC = empty_bytes(M * N * 4, CANARY)
+    abuf, ACC = empty_bytes(M * N * 4, CANARY) if with_acc else (None, None)
     ws_bytes = bst.gemm_quant_per_token_workspace_size(M, N, K)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     bst.gemm_quant_per_token(M, N, K, A, K, B, bst.COL_MAJOR if b_col_major else bst.ROW_MAJOR,
                              K if b_col_major else N, SA, SB, C, N, ACC, ws, ws_bytes, sched=sched)
     bst.check_async()
-    assert canary_intact(cbuf, CANARY) and canary_intact(abuf, CANARY)
+    assert canary_intact(cbuf, CANARY) and (abuf is None or canary_intact(abuf, CANARY))
     out = decode_out(host(C, np.uint16).reshape(M, N).copy(), "bf16")
-    acc = host(ACC, np.int32).reshape(M, N).copy()
+    acc = host(ACC, np.int32).reshape(M, N).copy() if with_acc else None
     return out, acc
 
 
@@ -247,20 +244,41 @@ def test_int8_extreme_sums_exact():
         assert_close_fro(out, rout, FRO_MX)
 
 
-def test_int8_full_workload():
-    """int8 8192x8192x8192 with per-row / per-column fp32 scales; exact
-    int32 accumulators and dequantised bf16 on a seeded sample of rows."""
+@functools.lru_cache(maxsize=1)
+def _int8_full_oracle():
     w = wl.int8_per_token()
+    racc, rout = oracle_int8_rows(w, np.arange(w["M"]))
+    return w, racc, rout
+
+
+def test_int8_full_workload():
+    """int8 8192x8192x8192 with per-row / per-column fp32 scales: every int32
+    accumulator bit-exact and every dequantised bf16 output within the
+    tolerance."""
+    w, racc, rout = _int8_full_oracle()
     out, acc = run_int8(w, True)
-    rows = np.sort(np.random.default_rng(1).choice(w["M"], 256, replace=False))
-    racc, rout = oracle_int8_rows(w, rows)
-    assert np.array_equal(acc[rows], racc)
-    assert_close_fro(out[rows], rout, FRO_MX)
+    assert np.array_equal(acc, racc)
+    assert_close_fro(out, rout, FRO_MX)
+
+
+@pytest.mark.parametrize("S,d", [(1, 0), (8, 1)])
+def test_int8_full_workload_without_acc_out(S, d):
+    """The call exactly as the bench times it (acc_out = NULL, automatic
+    tiles): every bf16 output within the tolerance of the oracle, and
+    bit-identical to the same call that also writes the accumulators."""
+    w, racc, rout = _int8_full_oracle()
+    out, _ = run_int8(w, True, bst.sched(S, d), with_acc=False)
+    assert_close_fro(out, rout, FRO_MX)
+    out_acc, acc = run_int8(w, True, bst.sched(S, d))
+    assert np.array_equal(out.view(np.uint64), out_acc.view(np.uint64))
+    assert np.array_equal(acc, racc)
 
 
 # ------------------------------------------- grouped int8, per-token dequant -
 
-def run_grouped_int8(w, b_col_major=True, sched=None, gdev=None):
+def run_grouped_int8(w, b_col_major=True, sched=None, gdev=None, with_acc=True):
+    """One bst_gemm_grouped_quant_per_token call; with_acc=False passes
+    acc_out = NULL (the call the bench times) and returns acc None."""
     gm, N, K = w["group_m"], w["N"], w["K"]
     G = len(gm)
     total = sum(gm)
@@ -269,15 +287,15 @@ def run_grouped_int8(w, b_col_major=True, sched=None, gdev=None):
     Wd, SA, SB = dev(W), dev(w["sa"]), dev(w["sb"])
     gdev = torch.tensor(gm, dtype=torch.int32, device="cuda") if gdev is None else gdev
     cbuf, C = empty_bytes(max(total, 1) * N * 2, CANARY)
-    abuf, ACC = empty_bytes(max(total, 1) * N * 4, CANARY)
+    abuf, ACC = empty_bytes(max(total, 1) * N * 4, CANARY) if with_acc else (None, None)
     ws_bytes = bst.gemm_grouped_quant_per_token_workspace_size(G, total, N, K)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     bst.gemm_grouped_quant_per_token(G, gdev, total, N, K, X, K, Wd, bst.COL_MAJOR if b_col_major else bst.ROW_MAJOR,
                                      K if b_col_major else N, N * K, SA, SB, N, C, N, ACC, ws, ws_bytes, sched=sched)
     bst.check_async()
-    assert canary_intact(cbuf, CANARY) and canary_intact(abuf, CANARY)
+    assert canary_intact(cbuf, CANARY) and (abuf is None or canary_intact(abuf, CANARY))
     out = decode_out(host(C, np.uint16).reshape(-1, N)[:total].copy(), "bf16")
-    acc = host(ACC, np.int32).reshape(-1, N)[:total].copy()
+    acc = host(ACC, np.int32).reshape(-1, N)[:total].copy() if with_acc else None
     return out, acc
 
 
@@ -317,24 +335,22 @@ def test_grouped_int8_inconsistent_sizes_reported():
     bst.check_async()      # the error word was cleared
 
 
-@pytest.mark.parametrize("forced", [None, [0, 2048, 0, 1024, 3072, 0, 2048, 0]])
-def test_grouped_int8_full_workload(forced):
-    """G = 8 groups summing to 8192 rows, K = N = 4096; exact int32
-    accumulators and bf16 outputs on a seeded sample of whole rows."""
-    w = wl.grouped_int8_per_token(group_m=forced)
-    out, acc = run_grouped_int8(w, True)
-    rows = np.sort(np.random.default_rng(2).choice(sum(w["group_m"]), 256, replace=False))
-    gm = w["group_m"]
-    off = np.concatenate([[0], np.cumsum(gm)])
-    racc = np.zeros((len(rows), w["N"]), np.int64)
-    rout = np.zeros((len(rows), w["N"]))
-    for g in range(len(gm)):
-        sel = np.nonzero((rows >= off[g]) & (rows < off[g + 1]))[0]
-        if len(sel):
-            a, ro = og.gemm_quant_per_token(w["x"][rows[sel]], np.ascontiguousarray(w["w"][g].T),
-                                            w["sa"][rows[sel]], w["sb"][g])
-            racc[sel] = a
-            rout[sel] = decode_out(ro, "bf16")
-    assert np.array_equal(acc[rows], racc)
-    assert_close_fro(out[rows], rout, FRO_MX)
+@functools.lru_cache(maxsize=1)
+def _grouped_int8_full_oracle(forced):
+    w = wl.grouped_int8_per_token(group_m=None if forced is None else list(forced))
+    racc, rout = oracle_grouped_int8(w)
+    return w, racc, rout
 
+
+@pytest.mark.parametrize("forced", [None, (0, 2048, 0, 1024, 3072, 0, 2048, 0)])
+def test_grouped_int8_full_workload(forced):
+    """G = 8 groups summing to 8192 rows, K = N = 4096: every int32
+    accumulator bit-exact and every bf16 output within the tolerance; then
+    the call as the bench times it (acc_out = NULL), whose outputs must be
+    bit-identical to the first call's."""
+    w, racc, rout = _grouped_int8_full_oracle(forced)
+    out, acc = run_grouped_int8(w, True)
+    assert np.array_equal(acc, racc)
+    assert_close_fro(out, rout, FRO_MX)
+    out_noacc, _ = run_grouped_int8(w, True, bst.sched(1, 0), with_acc=False)
+    assert np.array_equal(out_noacc.view(np.uint64), out.view(np.uint64))

@@ -16,9 +16,11 @@
 
 #include "bst.h"
 
-namespace {
+// File-scope scratch array with internal linkage; host code never uses its
+// name as an address, only the device address looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BST_NOALLOC_SCRATCH_BYTES];
 
-__device__ __align__(256) unsigned char g_noalloc_scratch[BST_NOALLOC_SCRATCH_BYTES];
+namespace {
 
 constexpr int kMaxDevices = 64;
 std::atomic<uintptr_t> g_scratch_addr[kMaxDevices];

@@ -1,8 +1,10 @@
 """GPU check of bst_gemm_quant_per_token_noalloc, the int8 per-token GEMM
 entry point that takes its scratch from the library's fixed array instead of
 a caller workspace.  Its results must equal those of
-bst_gemm_quant_per_token on the same inputs (exact int32 accumulators, bf16
-outputs within the dequant tolerance), on two calls issued back to back."""
+bst_gemm_quant_per_token on the same inputs bit for bit (the same kernels run
+on the same bytes: exact int32 accumulators and identical bf16 outputs, which
+are also within the dequant tolerance of each other), on two calls issued
+back to back, and a call must leave the device's free memory unchanged."""
 import numpy as np
 import pytest
 import torch
@@ -61,7 +63,27 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
         assert canary_intact(cbuf, CANARY) and canary_intact(abuf, CANARY)
         out, acc = _results(M, N, C, ACC)
         assert np.array_equal(acc, wacc)
+        assert np.array_equal(out.view(np.uint64), wout.view(np.uint64))
         assert_close_fro(out, wout, FRO_MX)
+
+
+def test_noalloc_call_leaves_free_device_memory_unchanged():
+    """After one warm-up call (which only looks up the scratch array's
+    address), a further call allocates no device memory: the free memory the
+    driver reports is the same before and after it."""
+    w = wl.int8_per_token(512, 384, 1024, seed=13)
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B, SA, SB = dev(w["a"]), dev(w["b"]), dev(w["sa"]), dev(w["sb"])
+    _, C, _, ACC = _buffers(M, N)
+    bst.gemm_quant_per_token_noalloc(M, N, K, A, K, B, bst.COL_MAJOR, K, SA, SB, C, N, ACC)
+    bst.check_async()
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    bst.gemm_quant_per_token_noalloc(M, N, K, A, K, B, bst.COL_MAJOR, K, SA, SB, C, N, ACC)
+    bst.check_async()
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
 
 
 def test_noalloc_rejects_problems_past_the_scratch_limit():

@@ -1,27 +1,34 @@
 """Benchmark of the block-swizzled tile GEMM on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--lite]
+                    [--workload NAME] [--configs 0|1] [--lite]
 
 A step is one call of the GEMM entry point on one batch of synthetic input.
 The default workload is the fp16 GEMM M=N=1024, K=2048 (A row-major, B
 column-major, entries N(0,1)/sqrt(K), fp32 accumulate, fp16 out) -- the one
 the metric "GEMM TFLOP/s at 1 GB300 and % of the dtype's dense tensor peak"
-is quoted on.  Other workloads (--workload fp16_tail | mxfp8 | grouped_bf16 |
-int8_per_token) print the same line for their own shape.
+is quoted on.  The default run also measures the other four configurations
+the metric is quoted on (the fp16 500x380x256 tail, MXFP8 1024x2048x4096,
+grouped bf16 slice-M and int8 8192^3 with per-token dequant) and reports each
+under "configs" with its own timing, roofline, clocks, end-to-end figure and
+oracle baseline.  Other workloads (--workload fp16_tail | mxfp8 | ...) print
+the line for their own shape alone.
 
 Timing: W untimed steps, then exactly K steps replayed from CUDA graphs on one
 stream, bracketed by a barrier and a device synchronise, timed with CUDA
-events; inputs rotate over enough independent copies that the bytes touched
-between two uses of one copy exceed the 129 MB L2.  With N > 1 (torchrun)
-every rank runs an independent replica on its own GPU (the path shards by
-whole problems, no collective on the data path) and rank 0 prints the total
-over ranks divided by the slowest rank's time.
+events; the graphs are queued behind an untimed device-side wait so that the
+host's submission latency is not in the timed region; inputs rotate over
+enough independent copies that the bytes touched between two uses of one copy
+exceed the 129 MB L2.  The extra configurations time min(K, about one second
+of steps).  With N > 1 (torchrun) every rank runs an independent replica on
+its own GPU (the path shards by whole problems, no collective on the data
+path) and rank 0 prints the total over ranks divided by the slowest rank's
+time.
 
 --impl reference times the CPU oracle (the plain fp64 definition in oracle/)
 on the host cores on a bounded sample of rows of the same workload.
---lite skips the CPU baseline, the clock sampler and the end-to-end leg (for
-profiler runs).
+--lite skips the CPU baseline, the clock sampler, the end-to-end leg and the
+extra configurations (for profiler runs).
 """
 import argparse
 import hashlib
@@ -304,6 +311,10 @@ def timed_steps(work, K, stream):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # an untimed device wait ahead of the first event keeps the GPU busy while
+    # the host submits the graphs, so the timed region holds the K steps'
+    # device time and not the host's submission latency
+    device_wait(stream)
     t0.record(stream)
     for _ in range(reps):
         full.replay()
@@ -314,6 +325,13 @@ def timed_steps(work, K, stream):
     barrier()
     torch.cuda.synchronize()
     return t0.elapsed_time(t1)
+
+
+def device_wait(stream, us=50.0):
+    """Queues a device-side spin of about ``us`` microseconds on ``stream``
+    (untimed; it precedes the first timing event)."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2100))
 
 
 def e2e_pipelined(work, hin, steps, warm):
@@ -386,6 +404,7 @@ def e2e_pipelined(work, hin, steps, warm):
     reps = -(-steps // per)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    device_wait(cap)
     e0.record(cap)
     for _ in range(reps):
         with torch.cuda.stream(cap):
@@ -577,6 +596,158 @@ def reference_arm(args, work_name):
 
 # ------------------------------------------------------------------ main --
 
+# the configurations the metric is quoted on; the first is the headline line
+CONFIGS = [("c2", "fp16_square"), ("c1", "fp16_tail"), ("c3", "mxfp8"), ("c4", "grouped_bf16"),
+           ("c5", "int8_per_token")]
+
+
+def sched_opts(args):
+    return dict(tile_n=args.tile_n, tile_m=args.tile_m, split_k=args.split_k, dynamic=args.dynamic,
+                shuffle_k=args.shuffle_k)
+
+
+def choose_swizzle(work, args, stream, opts):
+    """Untimed sweep of SwizzleOffset {1,2,4,8} x {Zn,Nz}: two passes in
+    opposite orders, averaged, after a warm-up of the same work, so a GPU
+    that heats up (or cools down) during the sweep favours no setting by its
+    position in the order.  Returns ({setting: TFLOP/s}, ms per step of the
+    warm-up)."""
+    n = max(8, min(200, args.steps))
+    order = [(S, d) for S in (1, 2, 4, 8) for d in (0, 1)]
+    times = {}
+    work.sched = work.bst.sched(1, 0, **opts)
+    warm_ms = timed_steps(work, n, stream) / n
+    for seq in (order, order[::-1]):
+        for S, d in seq:
+            work.sched = work.bst.sched(S, d, **opts)
+            for i in range(3):
+                work.step(i)
+            times.setdefault((S, d), []).append(timed_steps(work, n, stream))
+    sweep = {}
+    for (S, d), ts in times.items():
+        ms = sum(ts) / len(ts)
+        sweep["%s%d" % ("Zn" if d == 0 else "Nz", S)] = round(work.flops * n / (ms * 1e-3) / 1e12, 2)
+    best = max(sweep, key=sweep.get)
+    work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, **opts)
+    return sweep, warm_ms
+
+
+def roofline_of(work, per_step_ms, clocks, peaks, src):
+    """The dominant kernel's roofline entry: tensor-bound GEMMs against the
+    dtype's dense peak; a GEMM whose arithmetic intensity is below the ridge
+    of the measured peaks (the fp16 tail) against the measured HBM copy rate,
+    with its tensor fraction alongside."""
+    capped = bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
+    kind = "bf16_tflops_sustained" if capped and "bf16_tflops_sustained" in peaks else "bf16_tflops"
+    how = "sustained, power cap active" if kind.endswith("sustained") else "burst"
+    if work.dtype == "e4m3":
+        peak = peaks[kind] * 2.0
+        peak_note = "%s bf16 %s x 2 (nominal fp8/bf16 ratio)" % (src, how)
+    else:
+        peak = peaks[kind]
+        peak_note = "%s bf16 %s (%s)" % (src, how, "fp16 runs at the bf16 rate" if work.dtype == "f16" else
+                                         "int8 is multiplied on the bf16 pipe" if work.dtype == "s8" else "bf16")
+    sec = per_step_ms * 1e-3
+    tflops = work.flops / sec / 1e12
+    alg_bytes = work.in_bytes + work.out_bytes
+    ai = work.flops / alg_bytes
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    entry = {"achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak, "bound": "tensor",
+             "traffic": stored_traffic(work.kernel_key), "peak_source": peak_note, "kernel": work.kernel_key,
+             "launches_covered": work.launches_per_step, "per_launch_us": per_step_ms * 1e3,
+             "algorithmic_bytes": alg_bytes, "arithmetic_intensity": round(ai, 1), "ridge": round(ridge, 1)}
+    if ai < ridge:
+        gbs = alg_bytes / sec / 1e9
+        entry.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": gbs / peaks["hbm_gbs"], "peak_source": "%s HBM copy rate" % src,
+                      "tensor_tflops": tflops, "tensor_frac": tflops / peak})
+    return entry
+
+
+def measure(name, args, world, rank, stream, sampler, cpu_budget, steps):
+    """One workload: swizzle choice, warm-up, clock-sampled soak and exactly
+    `steps` timed steps, the end-to-end leg and the oracle on the host.
+    Returns the fields of its JSON line and frees its device memory."""
+    work = Workload(name)
+    opts = sched_opts(args)
+    sweep = {}
+    work.sched = work.bst.sched(1, 0, **opts)
+    est_ms = None
+    if args.swizzle:
+        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, **opts)
+    elif not args.lite:
+        sweep, est_ms = choose_swizzle(work, args, stream, opts)
+    for i in range(args.warmup):
+        work.step(i)
+    torch.cuda.synchronize()
+    if est_ms is None:
+        est_ms = timed_steps(work, 8, stream) / 8
+
+    clocks = None
+    t_soak = time.time()
+    if sampler:
+        # untimed soak of the same work so the clock samples see the load
+        per_soak = max(1, int(args.soak_seconds / max(1e-6, est_ms * 1e-3)))
+        timed_steps(work, min(per_soak, 400000), stream)
+    ms = timed_steps(work, steps, stream)
+    t_end = time.time()
+    if sampler:
+        time.sleep(0.2)
+        clocks = sampler.summary(t_soak, t_end)
+        clocks["window"] = "soak+timed"
+    ms = max_over_ranks(ms)
+
+    e2e = None
+    if not args.lite:
+        # end to end: pinned host inputs -> device, GEMM, result -> host, every step
+        hin = work.host_inputs()
+        ems, ke = e2e_pipelined(work, hin, max(10, min(steps, 500)), 3)
+        ems = max_over_ranks(ems)
+        e2e = {"value": whole_job_tflops(world, work.flops, ke, ems), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hin.values())),
+               "d2h_bytes_per_step": int(work.sets[0]["C"].numel() * work.sets[0]["C"].element_size()),
+               "steps": ke, "pipeline": "inputs of step i+1 copied in while step i computes and copies out; one "
+                                         "copy stream per input tensor; steps replayed from CUDA graphs"}
+        del hin
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.lite and cpu_budget > 0:
+        rate, sample, dt = cpu_rate(work, cpu_budget)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": int(os.environ["OPENBLAS_NUM_THREADS"]), "kind": "oracle",
+               "sample": sample + ", fp64 BLAS matmul + one rounding"}
+
+    peaks, src = measured_peaks()
+    per_step_ms = ms / steps
+    out = {
+        "value": whole_job_tflops(world, work.flops, steps, ms), "unit": "TFLOP/s", "steps": steps,
+        "ms_per_step": per_step_ms, "dtype": work.dtype,
+        "config": {"workload": work.desc,
+                   "swizzle": {"offset": work.sched.swizzle_offset,
+                               "direction": "Zn" if work.sched.swizzle_direction == 0 else "Nz"},
+                   "l2": "inputs rotate over %d copies (%.0f MB %s 129 MB L2)"
+                         % (work.copies, work.copies * (work.in_bytes + work.out_bytes) / 1e6,
+                            ">" if work.copies * (work.in_bytes + work.out_bytes) > L2_BYTES else "<="),
+                   "tile_n": work.sched.tile_n or "auto", "tile_m": work.sched.tile_m or "auto",
+                   "split_k": work.sched.split_k or "auto",
+                   "tasks": "dynamic (cluster launch control)" if work.sched.dynamic else "static stride",
+                   "shuffle_k": bool(work.sched.shuffle_k),
+                   "launch": "CUDA graphs, one stream, queued behind an untimed device wait so that the host's "
+                             "graph submission is outside the timed region",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline_of(work, per_step_ms, clocks, peaks, src),
+        "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": steps * work.launches_per_step,
+    }
+    if sweep:
+        out["swizzle_sweep_tflops"] = sweep
+    for s in work.sets:
+        s.clear()
+    del work
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -586,6 +757,8 @@ def main():
     ap.add_argument("--workload", default="fp16_square",
                     choices=["fp16_square", "fp16_tail", "mxfp8", "grouped_bf16", "int8_per_token",
                              "grouped_int8_per_token", "grouped_slice_k_bf16", "grouped_slice_k_int8"])
+    ap.add_argument("--configs", type=int, default=1, choices=[0, 1],
+                    help="1 (default, headline workload only): also measure the other four configurations")
     ap.add_argument("--lite", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.0)
     ap.add_argument("--tile-n", type=int, default=0, help="force the tile width (64/128/256); 0 = automatic")
@@ -618,124 +791,46 @@ def main():
             _build.build()
         barrier()
 
-    work = Workload(args.workload)
     stream = torch.cuda.current_stream()
-
-    # swizzle sweep (untimed choice of SwizzleOffset/direction for the line)
-    sweep = {}
-    tn, tm, sk = args.tile_n, args.tile_m, args.split_k
-    opts = dict(tile_n=tn, tile_m=tm, split_k=sk, dynamic=args.dynamic, shuffle_k=args.shuffle_k)
-    work.sched = work.bst.sched(1, 0, **opts)
-    if args.swizzle:
-        work.sched = work.bst.sched(int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1, **opts)
-    elif not args.lite:
-        # two passes in opposite orders, averaged, after an untimed warm-up of
-        # the same work: a GPU that heats up (or down) during the sweep then
-        # favours no setting by its position in the order
-        n = max(8, min(200, args.steps))
-        order = [(S, d) for S in (1, 2, 4, 8) for d in (0, 1)]
-        times = {}
-        timed_steps(work, n, stream)
-        for seq in (order, order[::-1]):
-            for S, d in seq:
-                work.sched = work.bst.sched(S, d, **opts)
-                for i in range(3):
-                    work.step(i)
-                times.setdefault((S, d), []).append(timed_steps(work, n, stream))
-        for (S, d), ts in times.items():
-            ms = sum(ts) / len(ts)
-            sweep["%s%d" % ("Zn" if d == 0 else "Nz", S)] = round(work.flops * n / (ms * 1e-3) / 1e12, 2)
-        best = max(sweep, key=sweep.get)
-        work.sched = work.bst.sched(int(best[2:]), 0 if best.startswith("Zn") else 1, **opts)
-
-    for i in range(args.warmup):
-        work.step(i)
-    torch.cuda.synchronize()
-
-    clocks = None
     sampler = ClockSampler(local) if not args.lite else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-        # untimed soak of the same work so the clock samples see the load
-        t_soak = time.time()
-        per_soak = max(1, int(args.soak_seconds / max(1e-6, 5e-6 * work.launches_per_step)))
-        timed_steps(work, min(per_soak, 400000), stream)
-    t_begin = time.time()
-    ms = timed_steps(work, args.steps, stream)
-    t_end = time.time()
-    if sampler:
-        time.sleep(0.2)
-        sampler.stop()
-        clocks = sampler.summary(t_soak, t_end)
-        clocks["window"] = "soak+timed"
-    ms = max_over_ranks(ms)
-
-    # end to end: pinned host inputs -> device, GEMM, result -> host, every step
-    e2e = None
-    if not args.lite:
-        hin = work.host_inputs()
-        ems, ke = e2e_pipelined(work, hin, max(10, min(args.steps, 500)), 3)
-        ems = max_over_ranks(ems)
-        e2e = {"value": whole_job_tflops(world, work.flops, ke, ems), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hin.values())),
-               "d2h_bytes_per_step": int(work.sets[0]["C"].numel() * work.sets[0]["C"].element_size()),
-               "steps": ke, "pipeline": "inputs of step i+1 copied in while step i computes and copies out; one "
-                                         "copy stream per input tensor; steps replayed from CUDA graphs"}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.lite:
-        rate, sample, dt = cpu_rate(work, 12.0)
-        cpu = {"value": rate, "unit": "TFLOP/s", "cores": int(os.environ["OPENBLAS_NUM_THREADS"]), "kind": "oracle",
-               "sample": sample + ", fp64 BLAS matmul + one rounding"}
+    try:
+        head = measure(args.workload, args, world, rank, stream, sampler, 12.0, args.steps)
+        extra = {}
+        forced = args.tile_n or args.tile_m or args.split_k or args.swizzle or args.dynamic or args.shuffle_k
+        if args.configs and args.workload == "fp16_square" and not args.lite and not forced:
+            for tag, name in CONFIGS[1:]:
+                # each timed window held to about a second of device time
+                probe = extra_steps(name, args.steps)
+                extra[tag] = dict(measure(name, args, world, rank, stream, sampler, 6.0, probe),
+                                  workload_name=name)
+    finally:
+        if sampler:
+            sampler.stop()
 
     if rank != 0:
         return
-    peaks, src = measured_peaks()
-    # int8 steps are three launches (two widenings and the GEMM), slice-K
-    # steps two (the per-group map set-up and the GEMM) and int8 slice-K four,
-    # inside one C-ABI call: their roofline covers the whole step
-    per_launch_ms = ms / args.steps
-    value = whole_job_tflops(world, work.flops, args.steps, ms)
-    # the sustained cuBLAS figure was taken under the power cap: use it when
-    # the cap was active during this run's timed region, else the burst one
-    capped = bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
-    kind = "bf16_tflops_sustained" if capped and "bf16_tflops_sustained" in peaks else "bf16_tflops"
-    how = "sustained, power cap active" if kind.endswith("sustained") else "burst"
-    if work.dtype == "e4m3":
-        peak = peaks[kind] * 2.0
-        peak_note = "%s bf16 %s x 2 (nominal fp8/bf16 ratio)" % (src, how)
-    else:
-        peak = peaks[kind]
-        peak_note = "%s bf16 %s (%s)" % (src, how, "fp16 runs at the bf16 rate" if work.dtype == "f16" else
-                                         "int8 is multiplied on the bf16 pipe" if work.dtype == "s8" else "bf16")
-    achieved = work.flops / (ms / args.steps * 1e-3) / 1e12
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": work.dtype, "data": "synthetic",
-        "config": {"workload": work.desc,
-                   "swizzle": {"offset": work.sched.swizzle_offset,
-                               "direction": "Zn" if work.sched.swizzle_direction == 0 else "Nz"},
-                   "l2": "inputs rotate over %d copies (%.0f MB %s 129 MB L2)"
-                         % (work.copies, work.copies * (work.in_bytes + work.out_bytes) / 1e6,
-                            ">" if work.copies * (work.in_bytes + work.out_bytes) > L2_BYTES else "<="),
-                   "tile_n": work.sched.tile_n or "auto", "tile_m": work.sched.tile_m or "auto",
-                   "split_k": work.sched.split_k or "auto",
-                   "tasks": "dynamic (cluster launch control)" if work.sched.dynamic else "static stride",
-                   "shuffle_k": bool(work.sched.shuffle_k),
-                   "launch": "CUDA graphs, one stream", "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": stored_traffic(work.kernel_key),
-                     "peak_source": peak_note, "kernel": work.kernel_key,
-                     "launches_covered": work.launches_per_step,
-                     "per_launch_us": per_launch_ms * 1e3},
-        "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
-        "gpu_launches": args.steps * work.launches_per_step,
-    }
-    if sweep:
-        line["swizzle_sweep_tflops"] = sweep
+    line = {"metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
+            "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"], "clocks": head["clocks"],
+            "e2e": head["e2e"], "gpu_launches": head["gpu_launches"]}
+    if "swizzle_sweep_tflops" in head:
+        line["swizzle_sweep_tflops"] = head["swizzle_sweep_tflops"]
+    if extra:
+        line["configs"] = extra
     print(json.dumps(line), flush=True)
+
+
+# device time of one step of each extra configuration, for sizing its timed
+# window (the K of the command line when that is shorter)
+STEP_US = {"fp16_tail": 10.0, "mxfp8": 15.0, "grouped_bf16": 220.0, "int8_per_token": 800.0}
+
+
+def extra_steps(name, k):
+    return max(3, min(k, int(1e6 / STEP_US[name])))
 
 
 if __name__ == "__main__":

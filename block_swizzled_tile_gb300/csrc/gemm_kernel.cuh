@@ -132,6 +132,32 @@ __device__ __forceinline__ void prefetch_operands(const GemmArgs& g, uint32_t ti
     }
 }
 
+// L2 prefetch of the first k-blocks of one operand tile: `rows` rows of the
+// tile starting at mn0 (below mn_lim), k-blocks [kb0, kb0 + nkb) (of 64
+// 16-bit elements, below K), one 128-byte line each, spread over `nthreads`
+// threads.  Every prefetched address is an element that exists.  A
+// prefetch reads nothing into the SM and L2 stays coherent with whatever an
+// earlier kernel still writes, so this may run before griddepcontrol.wait:
+// it only moves the DRAM latency of the first loads off the critical path.
+__device__ __forceinline__ void prefetch_tile_l2(const OperandDesc& od, uint32_t mn0, uint32_t rows, uint32_t mn_lim,
+                                                 uint32_t kb0, uint32_t nkb, uint32_t K, uint32_t tid,
+                                                 uint32_t nthreads) {
+    if (od.mn_major) {
+        // line = one k of a 64-element MN atom
+        const uint32_t atoms = rows / 64;
+        for (uint32_t L = tid; L < atoms * nkb * 64; L += nthreads) {
+            const uint32_t k = kb0 * 64 + L % (nkb * 64), mn = mn0 + (L / (nkb * 64)) * 64;
+            if (k < K && mn < mn_lim) prefetch_l2(od.ptr + (static_cast<int64_t>(k) * od.ld + mn) * 2);
+        }
+    } else {
+        // line = one MN row over one k-block
+        for (uint32_t L = tid; L < rows * nkb; L += nthreads) {
+            const uint32_t k = (kb0 + L % nkb) * 64, mn = mn0 + L / nkb;
+            if (k < K && mn < mn_lim) prefetch_l2(od.ptr + (static_cast<int64_t>(mn) * od.ld + k) * 2);
+        }
+    }
+}
+
 struct GemmParams {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;

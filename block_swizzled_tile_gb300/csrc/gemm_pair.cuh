@@ -644,14 +644,23 @@ __global__ void __launch_bounds__(256, 1) gemm_pair_splitk_kernel(const __grid_c
     cluster_sync();                                  // barriers of every CTA initialised
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // set-up above touches no global memory: it overlaps the previous kernel
-    griddep_wait();
-    griddep_launch_dependents();
-    if (tl && threadIdx.x == 0) { tl[0] = t_entry; tl[1] = globaltimer_ns(); }
     const WaitCtl ctl{abort_flag, prm.g.timeout_ns, err};
     GroupTable gt{nullptr, nullptr, 0};
     TileInfo ti{};
     if (has_tile) ti = tile_info(sa, t, TM, BN, gt);
+    if (has_tile && has_k && warp >= 2 && warp < 6) {
+        // the epilogue warps (idle until the accumulator is ready) pull this
+        // CTA's first k-blocks into L2 while the previous kernel finishes
+        const uint32_t nk = min(4u, kb_end - kb_begin);
+        prefetch_tile_l2(prm.g.a, ti.row0 + half * kBM, kBM, prm.g.M, kb_begin, nk, prm.g.K, threadIdx.x - 64, 128);
+        prefetch_tile_l2(prm.g.b, ti.n * BN + half * BH, BH, prm.g.N, kb_begin, nk, prm.g.K, threadIdx.x - 64, 128);
+    }
+    // set-up above (the tile's coordinates come from the arguments alone,
+    // and an L2 prefetch reads nothing into the SM) overlaps the previous
+    // kernel
+    griddep_wait();
+    griddep_launch_dependents();
+    if (tl && threadIdx.x == 0) { tl[0] = t_entry; tl[1] = globaltimer_ns(); }
 
     if ((warp == 0 || warp == kPairBWarp) && lane == 0 && has_tile) {
         // ------------------------------------------------------ producer --
@@ -667,7 +676,8 @@ __global__ void __launch_bounds__(256, 1) gemm_pair_splitk_kernel(const __grid_c
         const uint32_t nk = kb_end - kb_begin;
         const uint32_t rot = (prm.g.shuffle_k && nk) ? (t + split) % nk : 0u;
         for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+            // the ring starts empty: only a stage being reused is waited for
+            if (issued >= STAGES && !mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
             uint8_t* sa_s = smem + stage * SL::kStageBytes;
             uint8_t* sb_s = sa_s + SL::kABytes;
             const uint32_t bar = full_leader + stage * 8;
@@ -836,10 +846,15 @@ __global__ void __launch_bounds__(256, 1) gemm_pair_splitk_kernel(const __grid_c
     // first, so that the barrier counts each warp once.  The cluster barrier
     // also orders this CTA's own warps (a block barrier before it only adds
     // latency): no CTA leaves, and no TMEM is freed, while any thread of the
-    // cluster may still touch it.
+    // cluster may still touch it.  Its arrival is relaxed: every access a CTA
+    // makes to another's shared memory has completed before it gets here (the
+    // partials it sent were counted on the receivers' barriers, which they
+    // waited for, and its bulk copies have finished reading its own ring), so
+    // there is nothing to release, and a release arrival would first wait for
+    // this CTA's global stores of C to drain.
     __syncwarp();
     tc_fence_before();
-    cluster_sync();
+    cluster_sync_relaxed_arrive();
     if (tl && threadIdx.x == 0) tl[39] = globaltimer_ns();
     if (warp == 1) {
         tc_fence_after();

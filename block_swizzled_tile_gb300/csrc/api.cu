@@ -442,24 +442,29 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     return cuda_status(launch_dense(p, bn, grid, stream));
 }
 
-// MXFP8 tile width and split-K.  The per-k-block cost of the MMA loop (about
-// 0.41 us at 128 columns, 0.44 us at 256, with the operands arriving from
-// DRAM) barely depends on the width, so wide tiles win whenever they can fill
-// the GPU; split-K over clusters of S CTAs (one tile per cluster) lets
-// 128 x 256 tiles do so.  Cost = waves x k-blocks per CTA x per-k-block time,
-// plus about 4 us for a split (the cluster launch, and the exchange and finish
-// of the partials through distributed shared memory by two warp groups,
-// measured on 128 x 256 tiles of 1024 x 2048 x 4096).  splits = 0 on return:
-// a forced split this problem cannot take.
-bst_status choose_mx(const Sched& sch, uint64_t loops_m, uint64_t N, uint32_t num_kb, uint32_t sms, uint32_t& bn,
-                     uint32_t& splits) {
+// MXFP8 tile shape and split-K.  One-CTA 128 x {128, 256} tiles cost about
+// 0.41 / 0.44 us per k-block (the MMA loop with the operands arriving from
+// DRAM; it barely depends on the width), so wide tiles win whenever they can
+// fill the GPU; split-K over clusters of S CTAs (one tile per cluster) lets
+// 128 x 256 tiles do so, at about 4 us for the cluster launch and the
+// exchange and finish of the partials through distributed shared memory.
+// CTA-pair 256 x {128, 256} tiles (operands and scale-factor arrays that TMA
+// can address, K a multiple of 1024) need no exchange: about 0.27 / 0.31 us
+// per k-block per pair (measured on 1024 x 2048 x 4096), two SMs per tile.
+// Cost = waves x k-blocks per CTA x per-k-block time (+ the split cost).
+// splits = 0 on return: a forced split this problem cannot take.
+bst_status choose_mx(const Sched& sch, uint64_t M, uint64_t N, uint32_t num_kb, uint32_t sms, bool pair_ok,
+                     uint32_t& tm, uint32_t& bn, uint32_t& splits) {
+    const uint64_t loops_m = (M + kBM - 1) / kBM;
     auto tiles_of = [&](uint32_t w) { return loops_m * ((N + w - 1) / w); };
     auto split_ok = [&](uint32_t w, uint32_t s) {
         uint32_t resident = 0;
         if (mxf8_split_resident(w, s, &resident) != cudaSuccess) { cudaGetLastError(); return false; }
         return resident > 0 && tiles_of(w) <= resident && tiles_of(w) * s <= sms;
     };
+    if (sch.tile_m == 256 && (!pair_ok || sch.split_k >= 2)) return BST_ERR_UNSUPPORTED;
     if (sch.split_k >= 2) {
+        tm = kBM;
         bn = sch.tile_n ? sch.tile_n : (sch.split_k == 2 ? 256u : 128u);
         splits = sch.split_k;
         uint32_t resident = 0;
@@ -470,14 +475,27 @@ bst_status choose_mx(const Sched& sch, uint64_t loops_m, uint64_t N, uint32_t nu
         return BST_OK;
     }
     double best = 1e300;
-    for (uint32_t w : {128u, 256u}) {
-        if (sch.tile_n && sch.tile_n != w) continue;
-        for (uint32_t s : {1u, 2u, 4u}) {
-            if (s > 1 && (sch.split_k == 1 || num_kb < 4 * s || !split_ok(w, s))) continue;
-            const uint64_t ctas = s > 1 ? tiles_of(w) * s : tiles_of(w);
-            const double waves = static_cast<double>((ctas + sms - 1) / sms);
-            const double cost = waves * ((num_kb + s - 1) / s) * (w == 256 ? 0.44 : 0.41) + (s > 1 ? 4.0 : 0.0);
-            if (cost < best * 0.999) { best = cost; bn = w; splits = s; }
+    bn = 0;
+    if (sch.tile_m != 256) {
+        for (uint32_t w : {128u, 256u}) {
+            if (sch.tile_n && sch.tile_n != w) continue;
+            for (uint32_t s : {1u, 2u, 4u}) {
+                if (s > 1 && (sch.split_k == 1 || num_kb < 4 * s || !split_ok(w, s))) continue;
+                const uint64_t ctas = s > 1 ? tiles_of(w) * s : tiles_of(w);
+                const double waves = static_cast<double>((ctas + sms - 1) / sms);
+                const double cost = waves * ((num_kb + s - 1) / s) * (w == 256 ? 0.44 : 0.41) + (s > 1 ? 4.0 : 0.0);
+                if (cost < best * 0.999) { best = cost; tm = kBM; bn = w; splits = s; }
+            }
+        }
+    }
+    if (pair_ok && sch.tile_m != kBM) {
+        for (uint32_t w : {128u, 256u}) {
+            if (sch.tile_n && sch.tile_n != w) continue;
+            const uint64_t tiles = ((M + 255) / 256) * ((N + w - 1) / w);
+            const uint64_t units = std::max(1u, sms / 2);
+            const double waves = static_cast<double>((tiles + units - 1) / units);
+            const double cost = waves * num_kb * (w == 256 ? 0.31 : 0.27);
+            if (cost < best * 0.999) { best = cost; tm = 256; bn = w; splits = 1; }
         }
     }
     return bn ? BST_OK : BST_ERR_UNSUPPORTED;
@@ -497,7 +515,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     if (sch.dynamic || sch.shuffle_k) return BST_ERR_UNSUPPORTED;   // one-CTA MXFP8 tiles, fixed K order
     if (la != BST_ROW_MAJOR || lb != BST_COL_MAJOR) return BST_ERR_UNSUPPORTED;
     if (K % 128) return BST_ERR_UNSUPPORTED;
-    if (sch.tile_n == 64 || sch.tile_m == 256) return BST_ERR_UNSUPPORTED;
+    if (sch.tile_n == 64 || (sch.tile_m && sch.tile_m != kBM && sch.tile_m != 256)) return BST_ERR_UNSUPPORTED;
     if (ldc < N || ldc < 1) return BST_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return BST_OK;
     if (!C || (K > 0 && (!A || !B || !sfa || !sfb))) return BST_ERR_INVALID_ARG;
@@ -510,25 +528,34 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
     const uint32_t csize = dtype_bytes(ct);
     if (K == 0) return cuda_status(launch_zero_fill(static_cast<uint8_t*>(C), ldc, 0, M, N, 1, csize, dev.sms, stream));
-    const uint64_t loops_m = (M + kBM - 1) / kBM;
     const uint32_t num_kb = static_cast<uint32_t>(K / 128);
-    uint32_t bn = 0, splits = 1;
-    if (bst_status s = choose_mx(sch, loops_m, N, num_kb, dev.sms, bn, splits)) return s;
-    const uint64_t tiles = loops_m * ((N + bn - 1) / bn);
+    // scale factors by TMA when each row's codes are a whole number of 16-byte
+    // groups (K a multiple of 512) and both arrays start 16-byte aligned;
+    // otherwise the scale warp copies them row by row (one-CTA tiles only)
+    const bool sf_tma = K % 512 == 0 && reinterpret_cast<uintptr_t>(sfa) % 16 == 0 &&
+                        reinterpret_cast<uintptr_t>(sfb) % 16 == 0;
+    uint32_t tm = kBM, bn = 0, splits = 1;
+    // CTA pairs take the codes in groups of 8 k-blocks (K a multiple of 1024)
+    const bool pair_ok = sf_tma && K % 1024 == 0 && tma_ok(a) && tma_ok(b);
+    if (bst_status s = choose_mx(sch, M, N, num_kb, dev.sms, pair_ok, tm, bn, splits))
+        return s;
+    const bool pair = tm == 256;
+    const uint64_t tiles = ((M + tm - 1) / tm) * ((N + bn - 1) / bn);
     if (tiles >= (1ull << 31)) return BST_ERR_INVALID_ARG;
-    if (smem_mxf8(bn) > dev.max_smem) return BST_ERR_UNSUPPORTED;
+    if ((pair ? smem_mxf8_pair(bn) : smem_mxf8(bn)) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
-    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, bn, CU_TENSOR_MAP_DATA_TYPE_UINT8, true)) return s;
+    if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, pair ? bn / 2 : bn, CU_TENSOR_MAP_DATA_TYPE_UINT8, true))
+        return s;
     p.g.M = M; p.g.N = N; p.g.K = K;
     p.g.batch = 1;
     p.g.mode = kModePlain;
     p.g.esize = 1;
     p.g.swz_offset = sch.offset;
     p.g.swz_dir = sch.dir;
-    p.g.ps.init(static_cast<uint32_t>(M), static_cast<uint32_t>(N), kBM, bn, sch.offset, sch.dir);
+    p.g.ps.init(static_cast<uint32_t>(M), static_cast<uint32_t>(N), tm, bn, sch.offset, sch.dir);
     p.g.num_kb = K / 128;
     p.g.chunk_kb = p.g.num_kb;
     p.g.total_tiles = static_cast<uint32_t>(tiles);
@@ -539,18 +566,18 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.sfa = sfa;
     p.g.sfb = sfb;
     p.g.sf_ld = static_cast<uint32_t>(K / 32);
-    // scale factors by TMA when each row's codes are a whole number of 16-byte
-    // groups (K a multiple of 512) and both arrays start 16-byte aligned;
-    // otherwise the scale warp copies them row by row
-    if (K % 512 == 0 && reinterpret_cast<uintptr_t>(sfa) % 16 == 0 && reinterpret_cast<uintptr_t>(sfb) % 16 == 0) {
+    if (sf_tma) {
         if (!encoder()) return BST_ERR_CUDA;
         const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 32);
         cuuint32_t estr[2] = {1, 1};
         cuuint64_t dims_a[2] = {row_bytes, static_cast<cuuint64_t>(M)};
         cuuint64_t dims_b[2] = {row_bytes, static_cast<cuuint64_t>(N)};
         cuuint64_t strides[1] = {row_bytes};
-        cuuint32_t box_a[2] = {16, kBM};
-        cuuint32_t box_b[2] = {16, bn};
+        // one-CTA tiles take 16 bytes (4 k-blocks) of codes per row per load,
+        // CTA pairs 32 (8 k-blocks), all of a tile's B columns in each CTA
+        const cuuint32_t row_box = pair ? 32 : 16;
+        cuuint32_t box_a[2] = {row_box, kBM};
+        cuuint32_t box_b[2] = {row_box, bn};
         if (g_encode(&p.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(sfa), dims_a, strides, box_a,
                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
@@ -569,6 +596,7 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.shuffle_k = sch.shuffle_k;
     set_prefetch(p.g, a, b, sfa, static_cast<uint64_t>(M) * (K / 32), sfb, static_cast<uint64_t>(N) * (K / 32));
     if (splits > 1) return cuda_status(launch_mxf8_split(p, bn, splits, static_cast<uint32_t>(tiles), stream));
+    if (pair) return cuda_status(launch_mxf8_pair(p, bn, pair_grid(sch, tiles, dev.sms), stream));
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     const uint32_t grid = static_cast<uint32_t>(std::min<uint64_t>(ctas, tiles));
     return cuda_status(launch_mxf8(p, bn, grid, stream));

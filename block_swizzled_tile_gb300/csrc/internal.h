@@ -68,6 +68,9 @@ cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaSt
 cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
 // MXFP8 split-K over clusters of `splits` CTAs (tile 128 x bn), one tile per cluster
 cudaError_t launch_mxf8_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream);
+// MXFP8 on CTA-pair tiles 256 x bn (no split): clusters of 2, at most max_pairs
+cudaError_t launch_mxf8_pair(const GemmParams& p, uint32_t bn, uint32_t max_pairs, cudaStream_t stream);
+uint32_t smem_mxf8_pair(uint32_t bn);
 // clusters the MXFP8 split-K kernel keeps resident at once (0: no such shape)
 cudaError_t mxf8_split_resident(uint32_t bn, uint32_t splits, uint32_t* out);
 cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stream);
@@ -124,6 +127,7 @@ constexpr uint32_t kMxSplitStages256 = 4;
 constexpr uint32_t kDequantStages = 6;
 constexpr uint32_t kPairStages128 = 8, kPairStages256 = 6;
 constexpr uint32_t kPairDequantStages = 5;
+constexpr uint32_t kPairMxStages128 = 7, kPairMxStages256 = 4;
 constexpr uint32_t kDequantChunkK = 1024;  // K elements per exact fp32 chunk
 
 }  // namespace bst

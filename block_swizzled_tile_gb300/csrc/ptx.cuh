@@ -142,6 +142,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCt
     return mbar_wait_slow(bar, parity, ctl, where);
 }
 
+// The same wait with acquire semantics at cluster scope: used where the
+// phase is completed by a release arrival of another CTA of the cluster
+// whose shared-memory writes the waiting side then consumes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, WaitCtl ctl, uint32_t where) {
+    const uint32_t a = smem_u32(bar);
+#pragma unroll 1
+    for (uint32_t i = 0; i < 16; ++i)
+        if (mbar_try_wait_cluster(a, parity)) return true;
+    // the slow path observes the phase with cta-scope acquire; the fence
+    // extends it to the cluster
+    const bool ok = mbar_wait_slow(bar, parity, ctl, where);
+    fence_acq_rel_cluster();
+    return ok;
+}
+
 // Wait used only while shutting down after an abort: ignores the abort flag,
 // still gives up after the time limit.
 static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -422,6 +451,15 @@ __device__ __forceinline__ void cluster_sync_relaxed_arrive() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Release fence at cluster scope restricted to this CTA's shared-memory
+// accesses: orders them before a following relaxed arrival on another CTA's
+// barrier.  A release arrival orders every earlier memory access of the
+// thread, and on GB300 waits about a microsecond for the SM's outstanding
+// global traffic (operand loads in flight included); this one does not.
+__device__ __forceinline__ void fence_release_smem_cluster() {
+    asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+}
+
 // arrive on an mbarrier given by its shared::cluster address (own or peer CTA)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
@@ -514,6 +552,28 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, u
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// MXFP8 MMA of a CTA pair (M = 256): as umma_mxf8, with A rows 0-127 and
+// the first half of B in the leader's shared memory and the rest in the
+// peer's.  Each CTA's tensor memory holds the accumulator rows and the A
+// scale factors of its own 128 rows and the B scale factors of all N columns,
+// at the same addresses in both CTAs.
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
+// The pair's shared -> tensor memory copy (issued by the leader): the source
+// descriptor addresses the same offset in both CTAs' shared memory, and each
+// CTA's tensor memory receives the lines of its own shared memory.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
 }
 
 // arrive once on the barrier at the same shared offset in every CTA of

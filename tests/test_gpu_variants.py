@@ -176,12 +176,67 @@ def test_mxfp8_split_k_f32_out_unit_scales():
     assert_close_fro(got, ref, 1e-5)
 
 
+@pytest.mark.parametrize("tn", [128, 256])
+def test_mxfp8_pair_scale_placement(tn):
+    """CTA-pair MXFP8 tiles (256 x tn): each CTA's tensor memory must get the
+    scale codes of its own 128 rows of A and of all tn columns of B.  Single
+    bumped codes in both CTAs' row halves and in both halves of the columns,
+    in different 4-k-block groups, reach exactly their own row / column and
+    32-element block."""
+    M, N, K = 256, 2 * tn, 1024
+    w = wl.mxfp8(M, N, K, seed=5 + tn)
+    w["sa"][:] = 127
+    w["sb"][:] = 127
+    w["sa"][37, 13] = 130          # leader's rows: x8 on row 37, k-block 3
+    w["sa"][200, 20] = 125         # peer's rows: /4 on row 200, k-block 5 (second group)
+    w["sa"][255, 0] = 128          # last row, first block
+    w["sb"][5, 30] = 124           # first half of the first tile's columns
+    w["sb"][tn - 1, 1] = 129       # second half of the first tile's columns
+    w["sb"][tn + 3, 9] = 126       # the second column tile
+    trace = torch.zeros(2 * 5, dtype=torch.int32, device="cuda")
+    got = run_mx(w, bst.sched(1, 0, tile_m=256, tile_n=tn, trace=trace), out="f32")
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"], "f32"), "f32")
+    assert_close_fro(got, ref, 1e-5)
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 256, tn, 1, 0), dtype=np.uint32))
+
+
+@pytest.mark.parametrize("tn", [128, 256])
+@pytest.mark.parametrize("mnk", [(300, 520, 1024), (129, 257, 3072), (1, 40, 1024), (700, 1000, 2048)])
+def test_mxfp8_pair_shapes(tn, mnk):
+    """Ragged tails in M and N on CTA-pair tiles, several tiles per pair
+    (persistent grid), K of one to three 8-k-block groups."""
+    M, N, K = mnk
+    w = wl.mxfp8(M, N, K, seed=M + N + tn)
+    lm, ln = -(-M // 256), -(-N // tn)
+    trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
+    got = run_mx(w, bst.sched(3, 1, tile_m=256, tile_n=tn, num_ctas=4, trace=trace))
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"]), "bf16")
+    assert_close_fro(got, ref, FRO_MX)
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 256, tn, 3, 1), dtype=np.uint32))
+
+
+@pytest.mark.parametrize("K", [384, 512])
+def test_mxfp8_pair_needs_whole_code_groups(K):
+    """CTA-pair MXFP8 tiles take the scale codes in groups of 8 k-blocks (K a
+    multiple of 1024): forcing them with K = 384 or 512 is refused; the
+    automatic choice still runs (on one-CTA tiles)."""
+    w = wl.mxfp8(256, 256, K, seed=6)
+    with pytest.raises(bst.BstError) as e:
+        run_mx(w, bst.sched(1, 0, tile_m=256))
+    assert e.value.status == bst.ERR_UNSUPPORTED
+    ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"]), "bf16")
+    assert_close_fro(run_mx(w, bst.sched(1, 0)), ref, FRO_MX)
+
+
 def test_mxfp8_full_workload():
     """e4m3 1024x2048x4096 with E8M0 scales 2^U{-4..4} per 32 K."""
     w = wl.mxfp8()
     ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"]), "bf16")
-    for S, d in [(1, 0), (4, 1)]:
-        got = run_mx(w, bst.sched(S, d))
+    # the automatic choice (CTA pairs), then one-CTA tiles split in two
+    for S, d, kw in [(1, 0, {}), (8, 1, {}), (4, 1, dict(tile_m=128, split_k=2))]:
+        got = run_mx(w, bst.sched(S, d, **kw))
         assert_close_fro(got, ref, FRO_MX)
 
 

@@ -64,13 +64,21 @@ def code_text(src):
     return " ".join(src.split())
 
 
+# host-only source (argument checks, tile and split choice, launches): not
+# part of the device-code hash
+HOST_ONLY_SOURCES = ("api.cu",)
+
+
 def csrc_hash():
-    """Hash of the CUDA sources' code (comments and whitespace removed), so
-    stored profiler counters are only used for the kernels they were taken
-    from, and an edit of a comment does not discard them."""
+    """Hash of the device code (every CUDA source but the host-only ones, with
+    comments and whitespace removed), so stored profiler counters are only
+    used for the kernels they were taken from, and an edit of a comment or of
+    host code does not discard them."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_swizzled_tile_gb300", "csrc")
     for f in sorted(os.listdir(d)):
+        if f in HOST_ONLY_SOURCES:
+            continue
         with open(os.path.join(d, f), encoding="utf-8") as fh:
             h.update(f.encode() + code_text(fh.read()).encode())
     return h.hexdigest()[:16]

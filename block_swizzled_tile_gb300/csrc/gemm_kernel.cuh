@@ -415,10 +415,11 @@ __device__ __noinline__ static void load_tile_regs(uint8_t* dst, const uint8_t* 
 // out-of-range bytes zero-filled by the copy itself.  The caller follows
 // with cp.async.mbarrier.arrive, so the stage's barrier completes when this
 // lane's copies have landed (the MMA thread fences for the async proxy).
+// Inlined: as a called function it took ~0.3 us of issue time per k-block.
 template <uint32_t V, bool MN>
-__device__ __noinline__ static void load_tile_async(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t lines,
-                                                    uint32_t mn0, uint32_t mn_lim, uint32_t k0, uint32_t k_lim,
-                                                    uint32_t lane, uint32_t part, uint32_t nparts) {
+__device__ __forceinline__ static void load_tile_async(uint8_t* dst, const uint8_t* base, int64_t ld, uint32_t lines,
+                                                       uint32_t mn0, uint32_t mn_lim, uint32_t k0, uint32_t k_lim,
+                                                       uint32_t lane, uint32_t part, uint32_t nparts) {
     constexpr uint32_t kEsize = 2;
     constexpr uint32_t kLineElems = kLine / kEsize;   // 64
     constexpr uint32_t vpl = kLine / V;               // vectors per 128-byte line: 8, 16 or 32
@@ -637,6 +638,13 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     const uint32_t lane = threadIdx.x & 31;
     const bool lanes_copy = KIND == kKindMXF8 || !(a_tma && b_tma);
     const bool lanes_copy_ops = !(a_tma && b_tma);      // an operand TMA cannot fetch
+    // Operands TMA cannot fetch go through the load/store unit, whose
+    // throughput per warp is the limit: for the CTA's first tile the epilogue
+    // warps, idle until its accumulator is ready, copy too (six warps in all).
+    // One accumulator chunk per tile, so that no epilogue is due before the
+    // first tile's copies are issued.
+    const bool copy_helpers = KIND == kKindF16 && EPI == kEpiStore && SPLIT == 1 && lanes_copy_ops &&
+                              prm.g.chunk_kb >= num_kb;
 
     GroupTable gt;
     gt.G = G;
@@ -648,9 +656,12 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             // 1 arrival from the issuing lane (+ TMA bytes), plus one per lane
             // when lanes also copy (MXFP8 scale factors, non-TMA operands)
             // (MXFP8 with scale TMA: the A thread and one arrival of the scale warp)
-            // (fp16/bf16 with an operand TMA cannot fetch: warps 0 and kBWarp both copy)
+            // (fp16/bf16 with an operand TMA cannot fetch: warps 0 and kBWarp both
+            // copy, and with copy helpers so do warps 2-5 -- on later tiles warp 0
+            // arrives for them)
             mbar_init(&full[s], (KIND == kKindMXF8 && prm.g.sf_tma) ? 2u
-                                : lanes_copy ? (KIND == kKindF16 && lanes_copy_ops ? 65u : 33u) : 1u);
+                                : lanes_copy ? (KIND == kKindF16 && lanes_copy_ops ? (copy_helpers ? 193u : 65u) : 33u)
+                                             : 1u);
             mbar_init(&empty[s], 1);
         }
         for (uint32_t a = 0; a < ACC; ++a) {
@@ -677,7 +688,12 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         tmem_alloc(tmem_holder, Lay::kTmemCols);
         tmem_relinquish();
     }
-    // set-up above touches no global memory: it overlaps the previous kernel
+    // small problems: the epilogue warps (idle until the first accumulator is
+    // ready) pull the operands into L2 while the previous kernel finishes (a
+    // prefetch reads nothing into the SM, and L2 is coherent with whatever
+    // that kernel still writes)
+    if (SPLIT == 1 && warp >= 2 && warp < 6) prefetch_operands(prm.g, threadIdx.x - 64, 128);
+    // set-up above reads no global memory into the SM: it overlaps the previous kernel
     griddep_wait();
     griddep_launch_dependents();
     if (mode == kModeGrouped && warp == 2)
@@ -872,8 +888,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 const uint32_t n0 = ti.n * BN;
                 const int32_t zc = static_cast<int32_t>(ti.tag);
                 const uint32_t rot = shuffle_rot(t);
+                const bool helped = copy_helpers && t == t_first;
+                const uint32_t parts = helped ? 6u : copy_parts;
                 for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
-                    if (!warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+                    // the ring starts empty: only a stage being reused is waited for
+                    if (issued >= STAGES && !warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     uint8_t* sb_s = sa_s + Lay::kABytes;
                     const uint32_t k0 = shuffled(kb, rot) * bk_elems;
@@ -906,15 +925,24 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                         // operands TMA cannot fetch: cp.async where the vectors
                         // allow it (the lane's arrival fires when its copies
                         // land), else register copies, fenced before the arrival
-                        if (!a_tma)
-                            load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld, a_mn, a_vec,
-                                            esize, kBM, ti.row0, ti.m_lim, k0, K, lane, copy_part, copy_parts);
-                        if (!b_tma)
-                            load_tile_plain(sb_s,
-                                            b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
-                                            b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane, copy_part, copy_parts);
-                        fence_proxy_async_smem();        // register-copied bytes -> the MMA's reads
+                        bool async_only = true;
+                        if (!a_tma && !load_tile_plain(sa_s, a_ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), a_ld,
+                                                       a_mn, a_vec, esize, kBM, ti.row0, ti.m_lim, k0, K, lane,
+                                                       copy_part, parts))
+                            async_only = false;
+                        if (!b_tma && !load_tile_plain(sb_s,
+                                                       b_ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
+                                                       b_ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane, copy_part, parts))
+                            async_only = false;
+                        // register-copied bytes -> the MMA's reads.  Not after
+                        // cp.async alone: the fence would wait for the copies to
+                        // land, serialising the k-blocks; the MMA warp fences
+                        // for them once the stage's barrier has completed.
+                        if (!async_only) fence_proxy_async_smem();
                         cp_async_arrive_noinc(&full[stage]);
+                        if (tl && warp == 0 && lane == 0 && issued < 7) tl[1 + issued] = globaltimer_ns();
+                        // the helpers' 128 arrivals, on the tiles they do not copy
+                        if (copy_helpers && !helped && warp == 0 && lane == 0) mbar_arrive_cnt(&full[stage], 128u);
                         if (tma_thread) {                // the TMA half of a mixed stage
                             mbar_arrive_expect_tx(&full[stage], tx);
                             if (a_tma)
@@ -1014,8 +1042,39 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // follows the cluster barrier below
         if (has_k && t_first < total_tiles) acc_ok = warp_wait(&tfull[0], 0, ctl, 4);
     } else if (warp >= 2 && warp < 6) {
+        if (copy_helpers && t_first < total_tiles) {
+            // -------------------------- copy helpers (first tile only) --
+            // parts 2-5 of the six-way split of every k-block's copies (warps
+            // 0 and kBWarp take parts 0 and 1); TMA, where an operand allows
+            // it, stays with the load thread
+            const TileInfo ti = tile_info(sa, t_first, kBM, BN, gt);
+            const uint32_t n0 = ti.n * BN;
+            const uint32_t rot = shuffle_rot(t_first);
+            const uint32_t a_vec = prm.g.a.vec_bytes, b_vec = prm.g.b.vec_bytes;
+            const int64_t a_bs = prm.g.a.batch_stride, b_bs = prm.g.b.batch_stride;
+            uint32_t stage = 0, phase = 0, issued = 0;
+            for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
+                if (issued >= STAGES && !warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) break;
+                uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+                uint8_t* sb_s = sa_s + Lay::kABytes;
+                const uint32_t k0 = shuffled(kb, rot) * bk_elems;
+                bool async_only = true;
+                if (!a_tma && !load_tile_plain(sa_s, prm.g.a.ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), prm.g.a.ld,
+                                               a_mn, a_vec, esize, kBM, ti.row0, ti.m_lim, k0, K, lane, warp, 6u))
+                    async_only = false;
+                if (!b_tma && !load_tile_plain(sb_s,
+                                               prm.g.b.ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
+                                               prm.g.b.ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane, warp, 6u))
+                    async_only = false;
+                if (!async_only) fence_proxy_async_smem();
+                cp_async_arrive_noinc(&full[stage]);
+                if (tl && warp == 2 && lane == 0 && issued < 7) tl[8 + issued] = globaltimer_ns();
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            __syncwarp();
+        }
         // ----------------------------------------------------- epilogue --
-        prefetch_operands(prm.g, threadIdx.x - 64, 128);
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread
         const uint32_t c_type = prm.g.c_type, c_vec = prm.g.c_vec, acc_vec = prm.g.acc_vec;

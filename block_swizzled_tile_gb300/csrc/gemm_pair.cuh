@@ -659,6 +659,7 @@ __global__ void __launch_bounds__(256, 1) gemm_pair_splitk_kernel(const __grid_c
     // and an L2 prefetch reads nothing into the SM) overlaps the previous
     // kernel
     griddep_wait();
+    if (tl && threadIdx.x == 0) tl[44] = globaltimer_ns();
     griddep_launch_dependents();
     if (tl && threadIdx.x == 0) { tl[0] = t_entry; tl[1] = globaltimer_ns(); }
 

@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(kPairMxThreads, 1) gemm_pair_mx_kernel(const _
         prefetch_scale_rows<BN>(prm.g, ti0, rank, threadIdx.x - 64, 128);
     }
     griddep_wait();
+    if (tl && threadIdx.x == 0) tl[53] = globaltimer_ns();
     griddep_launch_dependents();
     if (tl && threadIdx.x == 0) { tl[0] = t_entry; tl[52] = globaltimer_ns(); }
 
@@ -196,14 +197,14 @@ __global__ void __launch_bounds__(kPairMxThreads, 1) gemm_pair_mx_kernel(const _
         bool ok = true;
         // The A thread also loads this CTA's scale codes by TMA, a raw group
         // (kGroupKb k-blocks) at a time, kRawSlots - 1 groups ahead of the
-        // k-block it issues: one thread feeds the TMA queue in order, so the
-        // first groups go out ahead of every operand tile, and no other role
-        // waits behind a full queue.  A raw slot is refilled once the scale
-        // warp has read it (raw_empty).
+        // k-block it issues: one thread feeds the TMA queue in order, so no
+        // other role waits behind a full queue (group 0 alone is issued by the
+        // scale warp, before any operand tile is queued).  A raw slot is
+        // refilled once the scale warp has read it (raw_empty).
         const uint32_t ngroups = num_kb / kGroupKb;
         const uint32_t my_tiles = cid < total_tiles ? (total_tiles - cid + nclusters - 1) / nclusters : 0u;
         const uint32_t total_groups = my_tiles * ngroups;
-        uint32_t rg = 0;                             // raw groups issued
+        uint32_t rg = total_groups ? 1u : 0u;        // raw groups issued (group 0 by the scale warp)
         TileInfo ti_issue = ti0;
         uint32_t t_issue = cid;
         auto issue_raw = [&]() -> bool {
@@ -219,9 +220,9 @@ __global__ void __launch_bounds__(kPairMxThreads, 1) gemm_pair_mx_kernel(const _
             ++rg;
             return true;
         };
-        // the first group ahead of every operand tile, the next ones after
-        // k-blocks 0, 8, 16, ... (each about two groups ahead of the MMAs)
-        if (is_a && total_groups) ok = issue_raw();
+        // the next groups after k-blocks 0, 8, 16, ... (each about two groups
+        // ahead of the MMAs)
+        if (tl && is_a) tl[54] = globaltimer_ns();
         for (uint32_t t = cid; ok && t < total_tiles; t += nclusters) {
             const TileInfo ti = t == cid ? ti0 : tile_info(sa, t, TM, BN, gt);
             const int32_t row = is_a ? static_cast<int32_t>(ti.row0 + rank * kBM)
@@ -263,6 +264,15 @@ __global__ void __launch_bounds__(kPairMxThreads, 1) gemm_pair_mx_kernel(const _
         const uint32_t ngroups = num_kb / kGroupKb;
         const uint32_t my_tiles = cid < total_tiles ? (total_tiles - cid + nclusters - 1) / nclusters : 0u;
         const uint32_t total_groups = my_tiles * ngroups;
+        if (lane == 0 && total_groups) {
+            // group 0 goes out from here, in parallel with the A thread's
+            // first operand tile
+            uint8_t* slot = smem + Lay::kRawOff;
+            mbar_arrive_expect_tx(&raw_full[0], Lay::kRawSlotBytes);
+            tma_load_2d(slot, &prm.tmap_sfa, &raw_full[0], 0, static_cast<int32_t>(ti0.row0 + rank * kBM));
+            tma_load_2d(slot + Lay::kRawA, &prm.tmap_sfb, &raw_full[0], 0, static_cast<int32_t>(ti0.n * BN));
+        }
+        __syncwarp();
         for (uint32_t G = 0; G < total_groups; ++G) {
             if (!warp_wait(&raw_full[G % kRawSlots], (G / kRawSlots) & 1u, ctl, 6)) break;
             const uint32_t slot = G % kSfGroups, ph = (G / kSfGroups) & 1u;

@@ -149,6 +149,20 @@ def test_padded_and_unaligned_leading_dims(lda_pad, ldb_pad, ldc_pad):
     assert_close_f16(got, oracle_dense(w, "f16"))
 
 
+@pytest.mark.parametrize("tn", [64, 128, 256])
+@pytest.mark.parametrize("acol,lda_pad,ldb_pad", [(False, 0, 4), (False, 0, 1), (True, 4, 0), (False, 3, 3)])
+def test_copied_operands_several_tiles_per_cta(tn, acol, lda_pad, ldb_pad):
+    """Operands TMA cannot fetch (8-byte and 2-byte aligned pitches), with
+    fewer CTAs than tiles and more k-blocks than ring stages: the epilogue
+    warps help copy only each CTA's first tile, and on the later tiles the
+    load warps arrive for them."""
+    M, N, K = 700, 520, 1100
+    w = wl.dense16(M, N, K, "f16", a_col_major=acol, b_col_major=False, seed=tn + lda_pad * 5 + ldb_pad,
+                   lda=(M if acol else K) + lda_pad, ldb=N + ldb_pad)
+    got = run_dense(w, "f16", bst.sched(2, 1, tile_n=tn, num_ctas=5))
+    assert_close_f16(got, oracle_dense(w, "f16"))
+
+
 @pytest.mark.parametrize("tm", [128, 256])
 @pytest.mark.parametrize("out,ldc_pad", [("f16", 1), ("f16", 2), ("bf16", 4), ("f16", 8), ("f32", 1), ("f32", 2),
                                          ("f32", 4)])

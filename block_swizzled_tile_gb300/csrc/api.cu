@@ -337,6 +337,51 @@ SplitChoice choose_splits(const Sched& sch, bool eligible, uint64_t M, uint64_t 
     return best;
 }
 
+// Split-K of one-CTA tiles for fp16/bf16 operands that TMA cannot fetch.
+// Their copies go through the load/store units, whose issue rate per SM is
+// the limit (about 0.6 us per 8 KB k-block of copied operand): when the tiles
+// leave SMs idle, spreading each tile's k-blocks over a cluster of S CTAs
+// divides the copy time per CTA, for the exchange of the partials through
+// distributed shared memory (about 1 us per 32 KB received).  Cost, in units
+// of one 8 KB copy: k-blocks per CTA x copied KB per k-block / 8, plus the
+// exchange; the split is taken when it beats the unsplit tile.  splits = 0:
+// a forced split this problem cannot take.
+SplitChoice choose_copy_splits(const Sched& sch, bool eligible, bool a_copied, bool b_copied, uint64_t M,
+                               uint64_t N, uint32_t num_kb, uint32_t sms, uint32_t bn_unsplit) {
+    SplitChoice none;
+    if (sch.split_k == 1 || sch.dynamic) return none;
+    const bool forced = sch.split_k >= 2;
+    if (!eligible || (sch.tile_m && sch.tile_m != 128)) {
+        if (forced) none.splits = 0;
+        return none;
+    }
+    auto copy_units = [&](uint32_t bn) { return ((a_copied ? 16.0 : 0.0) + (b_copied ? bn * 0.125 : 0.0)) / 8.0; };
+    auto tiles_of = [&](uint64_t bn) { return ((M + 127) / 128) * ((N + bn - 1) / bn); };
+    const uint64_t t1 = tiles_of(bn_unsplit);
+    double best_cost = static_cast<double>((t1 + sms - 1) / sms) * num_kb * copy_units(bn_unsplit);
+    SplitChoice best;
+    const std::pair<uint32_t, uint32_t> cands[] = {{64u, 2u}, {128u, 2u}, {128u, 4u}};
+    for (const auto& c : cands) {
+        const uint32_t bn = c.first, s = c.second;
+        if (sch.tile_n && sch.tile_n != bn) continue;
+        if (forced && sch.split_k != s) continue;
+        const uint64_t tiles = tiles_of(bn);
+        uint32_t resident = 0;
+        if (!forced && (tiles * s > sms || num_kb < s)) continue;
+        if (dense_split_resident(bn, s, &resident) != cudaSuccess) { cudaGetLastError(); continue; }
+        if (resident == 0 || (!forced && tiles > resident)) continue;
+        const double xchg = (s - 1) * (128.0 * bn / s * 4.0) / 32768.0 * (1.0 / 0.6);
+        const double cost = ((num_kb + s - 1) / s) * copy_units(bn) + xchg;
+        if (forced ? (best.splits == 1) : cost < best_cost * 0.95) {
+            best.splits = s;
+            best.bn = bn;
+            best_cost = cost;
+        }
+    }
+    if (forced && best.splits == 1) best.splits = 0;
+    return best;
+}
+
 CUtensorMapDataType tmap_type(bst_dtype t) {
     if (t == BST_F16) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (t == BST_BF16) return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -392,17 +437,30 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
 
     const bool pair_ok = tma_ok(a) && tma_ok(b);
     const uint32_t num_kb = static_cast<uint32_t>((K + 63) / 64);
-    const SplitChoice sc_k = choose_splits(sch, pair_ok && mode == kModePlain, M, N, num_kb, dev.sms);
+    SplitChoice sc_k = choose_splits(sch, pair_ok && mode == kModePlain, M, N, num_kb, dev.sms);
+    TileChoice tc;
+    bool copy_split = false;
+    if (!pair_ok) {
+        // operands TMA cannot fetch: one-CTA tiles, optionally split along K
+        Sched plain = sch;
+        plain.split_k = 0;
+        if (bst_status s = choose_tile(plain, false, false, M, batch, N, dev.sms, tc)) return s;
+        sc_k = choose_copy_splits(sch, mode == kModePlain, !tma_ok(a), !tma_ok(b), M, N, num_kb, dev.sms, tc.bn);
+        copy_split = sc_k.splits > 1;
+        if (copy_split) tc.bn = sc_k.bn;
+    }
     const uint32_t splits = sc_k.splits;
     if (splits == 0) return BST_ERR_UNSUPPORTED;
-    TileChoice tc;
-    if (splits > 1) { tc.tm = 256; tc.bn = sc_k.bn; }
-    else if (bst_status s = choose_tile(sch, pair_ok, false, M, batch, N, dev.sms, tc)) return s;
+    if (splits > 1 && !copy_split) { tc.tm = 256; tc.bn = sc_k.bn; }
+    else if (pair_ok) {
+        if (bst_status s = choose_tile(sch, pair_ok, false, M, batch, N, dev.sms, tc)) return s;
+    }
     const uint32_t bn = tc.bn;
     const bool pair = tc.tm == 256;
     const uint64_t tiles = ((M + tc.tm - 1) / tc.tm) * ((N + bn - 1) / bn) * batch;
     if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
-    const uint32_t smem_need = splits > 1 ? smem_splitk(bn, splits) : pair ? smem_pair(bn, 0) : smem_dense(bn, 0);
+    const uint32_t smem_need = copy_split ? smem_dense_split(bn, splits)
+                               : splits > 1 ? smem_splitk(bn, splits) : pair ? smem_pair(bn, 0) : smem_dense(bn, 0);
     if (smem_need == 0 || smem_need > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
     GemmParams p;
@@ -434,6 +492,7 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.shuffle_k = sch.shuffle_k;
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
+    if (copy_split) return cuda_status(launch_dense_split(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     if (splits > 1) return cuda_status(launch_pair_splitk(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     if (pair)
         return cuda_status(launch_pair(p, bn, pair_grid(sch, tiles, dev.sms),

@@ -34,4 +34,30 @@ uint32_t smem_dense(uint32_t bn, uint32_t groups) {
     }
 }
 
+template <uint32_t BN, uint32_t S>
+using DenseSplit = OneCtaSplit<BN, BN == 64 ? kDenseStages64 : kDenseStages128, kKindF16, S>;
+
+cudaError_t launch_dense_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream) {
+    if (bn == 64 && splits == 2) return DenseSplit<64, 2>::launch(p, tiles, stream);
+    if (bn == 128 && splits == 2) return DenseSplit<128, 2>::launch(p, tiles, stream);
+    if (bn == 128 && splits == 4) return DenseSplit<128, 4>::launch(p, tiles, stream);
+    return cudaErrorInvalidValue;
+}
+
+// 0 when there is no such instantiation
+cudaError_t dense_split_resident(uint32_t bn, uint32_t splits, uint32_t* out) {
+    *out = 0;
+    if (bn == 64 && splits == 2) return DenseSplit<64, 2>::resident(out);
+    if (bn == 128 && splits == 2) return DenseSplit<128, 2>::resident(out);
+    if (bn == 128 && splits == 4) return DenseSplit<128, 4>::resident(out);
+    return cudaSuccess;
+}
+
+uint32_t smem_dense_split(uint32_t bn, uint32_t splits) {
+    if (bn == 64 && splits == 2) return DenseSplit<64, 2>::Lay::smem_bytes(0);
+    if (bn == 128 && splits == 2) return DenseSplit<128, 2>::Lay::smem_bytes(0);
+    if (bn == 128 && splits == 4) return DenseSplit<128, 4>::Lay::smem_bytes(0);
+    return 0xFFFFFFFFu;
+}
+
 }  // namespace bst

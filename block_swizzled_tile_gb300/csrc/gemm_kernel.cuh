@@ -209,14 +209,15 @@ struct GemmLayout {
     static_assert(SPLIT == 1 || (ACC == 1 && kSplitW % 32 == 0 &&
                                  2 * kSplitSlots * kSplitSlotBytes <= STAGES * kStageBytes),
                   "split-K slots reuse the ring");
-    // Split-K epilogue groups: warps 2-5, and (kSplitEH = 2) warps 0, 1, 6, 7,
+    // Split-K epilogue groups: warps 2-5, and (kSplitEH = 2, MXFP8) warps 0, 1, 6, 7,
     // idle once the main loop is done; the group of warp w sums and stores
     // columns [h*kSplitWH, (h+1)*kSplitWH) of each split's W in TMEM lane
     // quarter w % 4.  Both groups stage their stores in the ring, after the
     // receive slots and the send staging.
     static constexpr uint32_t kSplitEH =
-        (SPLIT > 1 && kSplitW >= 64 && 2 * kSplitSlots * kSplitSlotBytes + 8 * kEpiWarpBytes <= STAGES * kStageBytes)
-            ? 2u : 1u;
+        (KIND == kKindMXF8 && SPLIT > 1 && kSplitW >= 64 &&
+         2 * kSplitSlots * kSplitSlotBytes + 8 * kEpiWarpBytes <= STAGES * kStageBytes)
+            ? 2u : 1u;                       // the second group needs an 8th warp (MXFP8 CTAs only)
     static constexpr uint32_t kSplitWH = kSplitW / kSplitEH;
     static constexpr uint32_t kSplitSubBytes = 32 * kSplitWH * 4;    // one warp's rows of its kSplitWH columns
     static constexpr uint32_t kSplitEpi0Off = 2 * kSplitSlots * kSplitSlotBytes;
@@ -643,8 +644,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     // warps, idle until its accumulator is ready, copy too (six warps in all).
     // One accumulator chunk per tile, so that no epilogue is due before the
     // first tile's copies are issued.
-    const bool copy_helpers = KIND == kKindF16 && EPI == kEpiStore && SPLIT == 1 && lanes_copy_ops &&
-                              prm.g.chunk_kb >= num_kb;
+    const bool copy_helpers = KIND == kKindF16 && EPI == kEpiStore && lanes_copy_ops && prm.g.chunk_kb >= num_kb;
 
     GroupTable gt;
     gt.G = G;
@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     // ready) pull the operands into L2 while the previous kernel finishes (a
     // prefetch reads nothing into the SM, and L2 is coherent with whatever
     // that kernel still writes)
-    if (SPLIT == 1 && warp >= 2 && warp < 6) prefetch_operands(prm.g, threadIdx.x - 64, 128);
+    if ((SPLIT == 1 || KIND == kKindF16) && warp >= 2 && warp < 6) prefetch_operands(prm.g, threadIdx.x - 64, 128);
     // set-up above reads no global memory into the SM: it overlaps the previous kernel
     griddep_wait();
     griddep_launch_dependents();
@@ -730,6 +730,40 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         return kx < kb_hi ? kx : kx - nk_span;
     };
     bool acc_ok = true;                                  // split-K: this CTA's partial is complete
+
+    // ------------------------------ copy helpers (first tile only) --
+    auto copy_first_tile_as_helper = [&]() {
+        if (!copy_helpers || t_first >= total_tiles) return;
+        // parts 2-5 of the six-way split of every k-block's copies (warps
+        // 0 and kBWarp take parts 0 and 1); TMA, where an operand allows
+        // it, stays with the load thread
+        const TileInfo ti = tile_info(sa, t_first, kBM, BN, gt);
+        const uint32_t n0 = ti.n * BN;
+        const uint32_t rot = shuffle_rot(t_first);
+        const uint32_t a_vec = prm.g.a.vec_bytes, b_vec = prm.g.b.vec_bytes;
+        const int64_t a_bs = prm.g.a.batch_stride, b_bs = prm.g.b.batch_stride;
+        uint32_t stage = 0, phase = 0, issued = 0;
+        for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
+            if (issued >= STAGES && !warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) break;
+            uint8_t* sa_s = smem + stage * Lay::kStageBytes;
+            uint8_t* sb_s = sa_s + Lay::kABytes;
+            const uint32_t k0 = shuffled(kb, rot) * bk_elems;
+            bool async_only = true;
+            if (!a_tma && !load_tile_plain(sa_s, prm.g.a.ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), prm.g.a.ld,
+                                           a_mn, a_vec, esize, kBM, ti.row0, ti.m_lim, k0, K, lane, warp, 6u))
+                async_only = false;
+            if (!b_tma && !load_tile_plain(sb_s,
+                                           prm.g.b.ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
+                                           prm.g.b.ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane, warp, 6u))
+                async_only = false;
+            if (!async_only) fence_proxy_async_smem();
+            cp_async_arrive_noinc(&full[stage]);
+            if (tl && warp == 2 && lane == 0 && issued < 7) tl[8 + issued] = globaltimer_ns();
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        __syncwarp();
+    };
 
     constexpr uint32_t kBWarp = b_warp_for<KIND>();
     if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp) ||
@@ -1040,40 +1074,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         // ------------------------------------- split-K epilogue, part 1 --
         // this CTA's partial is final once its MMAs are done; the exchange
         // follows the cluster barrier below
+        copy_first_tile_as_helper();
         if (has_k && t_first < total_tiles) acc_ok = warp_wait(&tfull[0], 0, ctl, 4);
     } else if (warp >= 2 && warp < 6) {
-        if (copy_helpers && t_first < total_tiles) {
-            // -------------------------- copy helpers (first tile only) --
-            // parts 2-5 of the six-way split of every k-block's copies (warps
-            // 0 and kBWarp take parts 0 and 1); TMA, where an operand allows
-            // it, stays with the load thread
-            const TileInfo ti = tile_info(sa, t_first, kBM, BN, gt);
-            const uint32_t n0 = ti.n * BN;
-            const uint32_t rot = shuffle_rot(t_first);
-            const uint32_t a_vec = prm.g.a.vec_bytes, b_vec = prm.g.b.vec_bytes;
-            const int64_t a_bs = prm.g.a.batch_stride, b_bs = prm.g.b.batch_stride;
-            uint32_t stage = 0, phase = 0, issued = 0;
-            for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
-                if (issued >= STAGES && !warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) break;
-                uint8_t* sa_s = smem + stage * Lay::kStageBytes;
-                uint8_t* sb_s = sa_s + Lay::kABytes;
-                const uint32_t k0 = shuffled(kb, rot) * bk_elems;
-                bool async_only = true;
-                if (!a_tma && !load_tile_plain(sa_s, prm.g.a.ptr + (a_rank3 ? ti.tag * a_bs * esize : 0), prm.g.a.ld,
-                                               a_mn, a_vec, esize, kBM, ti.row0, ti.m_lim, k0, K, lane, warp, 6u))
-                    async_only = false;
-                if (!b_tma && !load_tile_plain(sb_s,
-                                               prm.g.b.ptr + ((mode != kModePlain && b_bs != 0) ? ti.tag * b_bs * esize : 0),
-                                               prm.g.b.ld, b_mn, b_vec, esize, BN, n0, N, k0, K, lane, warp, 6u))
-                    async_only = false;
-                if (!async_only) fence_proxy_async_smem();
-                cp_async_arrive_noinc(&full[stage]);
-                if (tl && warp == 2 && lane == 0 && issued < 7) tl[8 + issued] = globaltimer_ns();
-                ++issued;
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            }
-            __syncwarp();
-        }
+        copy_first_tile_as_helper();
         // ----------------------------------------------------- epilogue --
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread

@@ -28,57 +28,8 @@ cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStr
     }
 }
 
-// Split-K: clusters of S CTAs, one 128 x BN tile per cluster.
 template <uint32_t BN, uint32_t STAGES, uint32_t S>
-struct MxSplit {
-    using Lay = GemmLayout<BN, STAGES, 1, kKindMXF8, S>;
-    static_assert(Lay::smem_bytes(0) <= 232448, "shared memory per CTA");
-    static constexpr auto kern = gemm_kernel<BN, STAGES, 1, kKindMXF8, kEpiStore, S>;
-
-    static cudaLaunchConfig_t config(uint32_t tiles, cudaStream_t stream, cudaLaunchAttribute* attr) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(S * tiles);
-        cfg.blockDim = dim3(threads_for<kKindMXF8>());
-        cfg.dynamicSmemBytes = Lay::smem_bytes(0);
-        cfg.stream = stream;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = S;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cfg;
-    }
-    static cudaError_t prepare() {
-        static std::atomic<uint64_t> attr_done{0};
-        return set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(0), attr_done);
-    }
-    static cudaError_t resident(uint32_t* out) {
-        static std::atomic<int> cache[64];
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        int n = cache[dev & 63].load();
-        if (n <= 0) {
-            if ((e = prepare()) != cudaSuccess) return e;
-            cudaLaunchAttribute attr[1];
-            cudaLaunchConfig_t cfg = config(1, nullptr, attr);
-            if ((e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg)) != cudaSuccess)
-                return e;
-            cache[dev & 63].store(n);
-        }
-        *out = n > 0 ? static_cast<uint32_t>(n) : 0u;
-        return cudaSuccess;
-    }
-    static cudaError_t launch(const GemmParams& p, uint32_t tiles, cudaStream_t stream) {
-        cudaError_t e = prepare();
-        if (e != cudaSuccess) return e;
-        cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = config(tiles, stream, attr);
-        add_pdl(cfg, attr);
-        return cudaLaunchKernelEx(&cfg, kern, p);
-    }
-};
+using MxSplit = OneCtaSplit<BN, STAGES, kKindMXF8, S>;
 
 cudaError_t launch_mxf8_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream) {
     if (bn == 256 && splits == 2) return MxSplit<256, kMxSplitStages256, 2>::launch(p, tiles, stream);

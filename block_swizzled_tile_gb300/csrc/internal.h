@@ -62,9 +62,69 @@ inline cudaError_t launch_gemm(Kern kern, const GemmParams& p, uint32_t grid, ui
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Split-K of one-CTA tiles: clusters of S CTAs, one 128 x BN tile per
+// cluster, K divided among the cluster's CTAs and the partials summed
+// through distributed shared memory.
+template <uint32_t BN, uint32_t STAGES, uint32_t KIND, uint32_t S>
+struct OneCtaSplit {
+    using Lay = GemmLayout<BN, STAGES, 1, KIND, S>;
+    static_assert(Lay::smem_bytes(0) <= 232448, "shared memory per CTA");
+    static constexpr auto kern = gemm_kernel<BN, STAGES, 1, KIND, kEpiStore, S>;
+
+    static cudaLaunchConfig_t config(uint32_t tiles, cudaStream_t stream, cudaLaunchAttribute* attr) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(S * tiles);
+        cfg.blockDim = dim3(threads_for<KIND>());
+        cfg.dynamicSmemBytes = Lay::smem_bytes(0);
+        cfg.stream = stream;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cfg;
+    }
+    static cudaError_t prepare() {
+        static std::atomic<uint64_t> attr_done{0};
+        return set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(0), attr_done);
+    }
+    // clusters of S that can be resident at once
+    static cudaError_t resident(uint32_t* out) {
+        static std::atomic<int> cache[64];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        int n = cache[dev & 63].load();
+        if (n <= 0) {
+            if ((e = prepare()) != cudaSuccess) return e;
+            cudaLaunchAttribute attr[1];
+            cudaLaunchConfig_t cfg = config(1, nullptr, attr);
+            if ((e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg)) != cudaSuccess)
+                return e;
+            cache[dev & 63].store(n);
+        }
+        *out = n > 0 ? static_cast<uint32_t>(n) : 0u;
+        return cudaSuccess;
+    }
+    static cudaError_t launch(const GemmParams& p, uint32_t tiles, cudaStream_t stream) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = config(tiles, stream, attr);
+        add_pdl(cfg, attr);
+        return cudaLaunchKernelEx(&cfg, kern, p);
+    }
+};
+
 // Kernel launches.  Each returns the cudaError_t of the launch (attribute
 // setting included); `grid` CTAs of kNumThreads threads on `stream`.
 cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
+// fp16 / bf16 one-CTA split-K (operands that TMA cannot fetch): bn 64 with 2
+// splits, bn 128 with 2 or 4
+cudaError_t launch_dense_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream);
+cudaError_t dense_split_resident(uint32_t bn, uint32_t splits, uint32_t* out);
+uint32_t smem_dense_split(uint32_t bn, uint32_t splits);
 cudaError_t launch_mxf8(const GemmParams& p, uint32_t bn, uint32_t grid, cudaStream_t stream);
 // MXFP8 split-K over clusters of `splits` CTAs (tile 128 x bn), one tile per cluster
 cudaError_t launch_mxf8_split(const GemmParams& p, uint32_t bn, uint32_t splits, uint32_t tiles, cudaStream_t stream);

@@ -340,6 +340,26 @@ def test_splitk_auto_choice_matches_oracle():
     assert_close_f16(got, oracle_dense(w, "f16"))
 
 
+@pytest.mark.parametrize("tn,splits", [(64, 2), (128, 2), (128, 4)])
+@pytest.mark.parametrize("mnk,acol,lda_pad,ldb_pad", [((500, 380, 256), False, 0, 0), ((300, 200, 1000), True, 4, 3),
+                                                      ((129, 127, 200), False, 3, 0), ((64, 90, 64), False, 0, 0)])
+@pytest.mark.parametrize("out", ["f16", "f32"])
+def test_copied_operands_split_k(tn, splits, mnk, acol, lda_pad, ldb_pad, out):
+    """One-CTA split-K for operands TMA cannot fetch (8- and 2-byte aligned
+    pitches): the partials of a cluster's CTAs summed by column ownership,
+    the tile order still the scheduler's; K = 64 leaves splits without
+    k-blocks."""
+    M, N, K = mnk
+    w = wl.dense16(M, N, K, "bf16", a_col_major=acol, b_col_major=False, seed=M + N + K + tn + splits,
+                   lda=(M if acol else K) + lda_pad, ldb=N + ldb_pad, dist="normal")
+    lm, ln = -(-M // 128), -(-N // tn)
+    trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
+    got = run_dense(w, out, bst.sched(3, 1, split_k=splits, tile_n=tn, tile_m=128, trace=trace))
+    assert_close_f16(got, oracle_dense(w, out))
+    tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+    assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, tn, 3, 1), dtype=np.uint32))
+
+
 def test_splitk_more_splits_than_kblocks_and_f32_out():
     # K = 64: one k-block, four splits -> three splits contribute zeros
     w = wl.dense16(256, 256, 64, "bf16", b_col_major=True, seed=8)

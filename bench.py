@@ -92,19 +92,24 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def stored_traffic(kernel_key):
-    """Per-launch DRAM bytes recorded from an ncu capture of this kernel, if
-    the capture was taken from the current sources."""
+def stored_traffic(kernel_key, setting=None):
+    """DRAM bytes per step recorded from ncu captures of this step's
+    kernels, if they were taken from the current device sources: the entry
+    of this swizzle setting (key@Zn4 and the like) where the traffic depends
+    on it, else the entry of the kernel alone."""
     p = os.path.join(PROFILE_DIR, "traffic.txt")
     if not os.path.exists(p):
         return None
     cur = csrc_hash()
+    found = {}
     with open(p) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and parts[0] == kernel_key and parts[1] == cur:
-                return float(parts[2])
-    return None
+            if len(parts) >= 3 and not parts[0].startswith("#") and parts[1] == cur:
+                found[parts[0]] = float(parts[2])
+    if setting and "%s@%s" % (kernel_key, setting) in found:
+        return found["%s@%s" % (kernel_key, setting)]
+    return found.get(kernel_key)
 
 
 # ------------------------------------------------------------- workloads --
@@ -640,7 +645,7 @@ def choose_swizzle(work, args, stream, opts):
     return sweep, warm_ms
 
 
-def roofline_of(work, per_step_ms, clocks, peaks, src):
+def roofline_of(work, per_step_ms, clocks, peaks, src, setting=None):
     """The dominant kernel's roofline entry: tensor-bound GEMMs against the
     dtype's dense peak; a GEMM whose arithmetic intensity is below the ridge
     of the measured peaks (the fp16 tail) against the measured HBM copy rate,
@@ -661,7 +666,7 @@ def roofline_of(work, per_step_ms, clocks, peaks, src):
     ai = work.flops / alg_bytes
     ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     entry = {"achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak, "bound": "tensor",
-             "traffic": stored_traffic(work.kernel_key), "peak_source": peak_note, "kernel": work.kernel_key,
+             "traffic": stored_traffic(work.kernel_key, setting), "peak_source": peak_note, "kernel": work.kernel_key,
              "launches_covered": work.launches_per_step, "per_launch_us": per_step_ms * 1e3,
              "algorithmic_bytes": alg_bytes, "arithmetic_intensity": round(ai, 1), "ridge": round(ridge, 1)}
     if ai < ridge:
@@ -742,7 +747,9 @@ def measure(name, args, world, rank, stream, sampler, cpu_budget, steps):
                    "launch": "CUDA graphs, one stream, queued behind an untimed device wait so that the host's "
                              "graph submission is outside the timed region",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roofline_of(work, per_step_ms, clocks, peaks, src),
+        "roofline": roofline_of(work, per_step_ms, clocks, peaks, src,
+                                setting=None if any(opts.values()) else "%s%d" % ("Zn" if work.sched.swizzle_direction == 0 else "Nz",
+                                                                    work.sched.swizzle_offset)),
         "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
         "gpu_launches": steps * work.launches_per_step,
     }

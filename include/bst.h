@@ -78,15 +78,18 @@ typedef struct {
                                    or 256)                                             */
     uint32_t num_ctas;          /* persistent CTAs; 0 = one per SM                      */
     uint32_t split_k;           /* 0 = automatic, 1 = off, 2 or 4: each output tile
-                                   is computed by 2 or 4 CTAs (fp16/bf16: CTA pairs,
-                                   tiles 256 x 256 or 256 x 128; MXFP8: single CTAs,
-                                   tiles 128 x 256 (2 splits) or 128 x 128) over
+                                   is computed by 2 or 4 CTAs (or CTA pairs) over
                                    disjoint K ranges and summed through distributed
-                                   shared memory (plain GEMMs; fp16/bf16 need
-                                   16-byte-aligned operands; used when the tiles
-                                   alone cannot fill the GPU).  The K ranges differ in size by at most
-                                   one 64-wide k-block; a range left empty (fewer
-                                   k-blocks than splits) contributes zeros          */
+                                   shared memory.  Plain GEMMs only.  fp16/bf16 with
+                                   16-byte-aligned operands: CTA pairs, tiles 256 x 256
+                                   or 256 x 128.  fp16/bf16 with an operand TMA cannot
+                                   fetch: single CTAs, tiles 128 x 64 (2 splits) or
+                                   128 x 128 (2 or 4).  MXFP8: single CTAs, tiles
+                                   128 x 256 (2 splits) or 128 x 128.  The automatic
+                                   choice splits when the tiles alone leave SMs idle.
+                                   The K ranges differ in size by at most one k-block;
+                                   a range left empty (fewer k-blocks than splits)
+                                   contributes zeros                                   */
     uint32_t* trace;            /* optional DEVICE buffer of 5 uint32 per task; when
                                    non-NULL the kernel writes, for task index t, the
                                    tile it computed: {batch or group, m, n, mActual,

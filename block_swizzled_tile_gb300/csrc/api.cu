@@ -199,6 +199,41 @@ bst_status encode(CUtensorMap* map, const OperandSpec& o, uint32_t tile_mn, CUte
     return r == CUDA_SUCCESS ? BST_OK : BST_ERR_ALIGNMENT;
 }
 
+// An MN-major 16-bit operand whose row pitch is 8 bytes off a multiple of 16
+// (ld = 4 mod 8 elements) has no tensor map, but pairs of its rows do: a
+// view whose rows are two rows (ld + mn elements: row 2j whole, then the
+// mn elements of row 2j+1; a pitch of 4*ld bytes) and whose K/2 rows end at
+// the operand's last element.  Even rows are then boxes of 64 x 32 at x = n0,
+// odd rows boxes of 72 x 32 at x = ld + n0 - 4, both 16-byte aligned.  Plain
+// (unbatched) operands with an even K and a 16-byte-aligned base.
+bool rows2_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("BST_ROWS2");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+bool rows2_ok(const OperandSpec& o) {
+    return o.mn_major && o.esize == 2 && o.batch == 1 && o.ld % 8 == 4 && o.k >= 2 && o.k % 2 == 0 &&
+           reinterpret_cast<uintptr_t>(o.ptr) % 16 == 0 && static_cast<uint64_t>(o.ld) + o.mn < (1ull << 30);
+}
+
+bst_status encode_rows2(CUtensorMap* even, CUtensorMap* odd, const OperandSpec& o, CUtensorMapDataType dt) {
+    if (!encoder()) return BST_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.ld) + o.mn, o.k / 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ld) * 2 * o.esize};
+    cuuint32_t estr[2] = {1, 1};
+    cuuint32_t box_even[2] = {64, 32}, box_odd[2] = {72, 32};
+    CUresult r = g_encode(even, dt, 2, const_cast<void*>(o.ptr), dims, strides, box_even, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return BST_ERR_ALIGNMENT;
+    r = g_encode(odd, dt, 2, const_cast<void*>(o.ptr), dims, strides, box_odd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BST_OK : BST_ERR_ALIGNMENT;
+}
+
 bst_status fill_operand(OperandDesc& d, CUtensorMap* map, const OperandSpec& o, uint32_t tile_mn,
                         CUtensorMapDataType dt, bool require_tma) {
     d.ptr = static_cast<const uint8_t*>(o.ptr);
@@ -209,6 +244,7 @@ bst_status fill_operand(OperandDesc& d, CUtensorMap* map, const OperandSpec& o, 
     d.vec_bytes = plain_vec(o);
     // a batch stride of 0 broadcasts one matrix to every batch: 2-D map, z ignored
     d.tma_rank = (o.batch > 1 && o.batch_stride != 0) ? 3u : 2u;
+    d.rows2 = 0;
     if (!d.use_tma) {
         if (require_tma) return BST_ERR_ALIGNMENT;
         std::memset(map, 0, sizeof(*map));
@@ -440,7 +476,14 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     SplitChoice sc_k = choose_splits(sch, pair_ok && mode == kModePlain, M, N, num_kb, dev.sms);
     TileChoice tc;
     bool copy_split = false;
-    if (!pair_ok) {
+    // B through the two-row view (one-CTA 128 x 64 tiles, no split)
+    const bool b_rows2 = !pair_ok && mode == kModePlain && tma_ok(a) && rows2_ok(b) && rows2_enabled() &&
+                         (sch.tile_m == 0 || sch.tile_m == 128) && (sch.tile_n == 0 || sch.tile_n == 64) &&
+                         sch.split_k <= 1;
+    if (b_rows2) {
+        tc.tm = 128;
+        tc.bn = 64;
+    } else if (!pair_ok) {
         // operands TMA cannot fetch: one-CTA tiles, optionally split along K
         Sched plain = sch;
         plain.split_k = 0;
@@ -459,7 +502,8 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     const bool pair = tc.tm == 256;
     const uint64_t tiles = ((M + tc.tm - 1) / tc.tm) * ((N + bn - 1) / bn) * batch;
     if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
-    const uint32_t smem_need = copy_split ? smem_dense_split(bn, splits)
+    const uint32_t smem_need = b_rows2 ? smem_dense_rows2()
+                               : copy_split ? smem_dense_split(bn, splits)
                                : splits > 1 ? smem_splitk(bn, splits) : pair ? smem_pair(bn, 0) : smem_dense(bn, 0);
     if (smem_need == 0 || smem_need > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
@@ -467,6 +511,10 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     std::memset(&p, 0, sizeof(p));
     if (bst_status s = fill_operand(p.g.a, &p.tmap_a, a, kBM, tmap_type(at), false)) return s;
     if (bst_status s = fill_operand(p.g.b, &p.tmap_b, b, pair ? bn / 2 : bn, tmap_type(bt), false)) return s;
+    if (b_rows2) {
+        if (bst_status s = encode_rows2(&p.tmap_sfa, &p.tmap_sfb, b, tmap_type(bt))) return s;
+        p.g.b.rows2 = 1;
+    }
     p.g.M = M; p.g.N = N; p.g.K = K;
     p.g.batch = batch;
     p.g.mode = mode;

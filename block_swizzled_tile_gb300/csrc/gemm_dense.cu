@@ -9,9 +9,15 @@ static cudaError_t launch_one(const GemmParams& p, uint32_t grid, cudaStream_t s
     using Lay = GemmLayout<BN, STAGES, 2, kKindF16>;
     static std::atomic<uint64_t> attr_done{0};
     auto kern = gemm_kernel<BN, STAGES, 2, kKindF16, kEpiStore>;
-    const uint32_t smem = Lay::smem_bytes(p.g.mode == kModeGrouped ? p.g.G : 0);
-    // the limit is set once for the largest group table any call can need
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), Lay::smem_bytes(kMaxGroups), attr_done);
+    // BN 64 also serves B through the two-row view, whose staging takes the
+    // place of the group table
+    constexpr uint32_t kMax = (BN == 64 && Lay::smem_bytes_rows2() > Lay::smem_bytes(kMaxGroups))
+                                  ? Lay::smem_bytes_rows2() : Lay::smem_bytes(kMaxGroups);
+    static_assert(kMax <= 232448, "shared memory per CTA");
+    if (p.g.b.rows2 && BN != 64) return cudaErrorInvalidValue;
+    const uint32_t smem = p.g.b.rows2 ? Lay::smem_bytes_rows2() : Lay::smem_bytes(p.g.mode == kModeGrouped ? p.g.G : 0);
+    // the limit is set once for the largest group table (or staging) any call can need
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kMax, attr_done);
     if (e != cudaSuccess) return e;
     return launch_gemm(kern, p, grid, threads_for<kKindF16>(), smem, stream);
 }
@@ -24,6 +30,8 @@ cudaError_t launch_dense(const GemmParams& p, uint32_t bn, uint32_t grid, cudaSt
         default: return cudaErrorInvalidValue;
     }
 }
+
+uint32_t smem_dense_rows2() { return GemmLayout<64, kDenseStages64, 2, kKindF16>::smem_bytes_rows2(); }
 
 uint32_t smem_dense(uint32_t bn, uint32_t groups) {
     switch (bn) {

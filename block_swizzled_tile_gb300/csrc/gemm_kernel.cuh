@@ -74,6 +74,8 @@ struct OperandDesc {
     uint32_t use_tma;
     uint32_t vec_bytes;    // cp.async / plain-load vector width when !use_tma
     uint32_t tma_rank;     // 2, or 3 when the tensor map has a batch/group dimension
+    uint32_t rows2;        // MN-major B with a pitch 8 bytes off a multiple of 16: loaded by TMA
+                           // through the two-row view (tmap_sfa: even rows, tmap_sfb: odd rows)
 };
 
 // Every scalar argument of the kernel.
@@ -165,8 +167,9 @@ __device__ __forceinline__ void prefetch_tile_l2(const OperandDesc& od, uint32_t
 struct GemmParams {
     CUtensorMap tmap_a;
     CUtensorMap tmap_b;
-    CUtensorMap tmap_sfa;   // MXFP8 scale factors as uint8 [rows, K/32], boxes of 16 bytes x 128 / BN rows
-    CUtensorMap tmap_sfb;
+    CUtensorMap tmap_sfa;   // MXFP8 scale factors as uint8 [rows, K/32], boxes of 16 bytes x 128 / BN rows;
+                            // fp16/bf16 with b.rows2: B's even rows (boxes of 64 x 32)
+    CUtensorMap tmap_sfb;   // ... fp16/bf16 with b.rows2: B's odd rows (boxes of 72 x 32, 8 bytes early)
     GemmArgs g;
 };
 
@@ -188,7 +191,7 @@ struct GemmLayout {
     // ring instead (after the main loop), which leaves room for a deeper ring
     static constexpr uint32_t kEpiOff = kRawOff + 2 * kRawSlotBytes;
     static constexpr uint32_t kBarOff = kEpiOff + (SPLIT > 1 ? 0u : 4 * kEpiWarpBytes);
-    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 2 + 8; // ..., drain, raw_full[2], recv[8]
+    static constexpr uint32_t kNumBars = 2 * STAGES + 2 * ACC + 1 + 4 + 8; // ..., drain, raw_full[4], recv[8]
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kMiscOff + 16 + 15) & ~15u;
     // TMEM: ACC accumulators of BN fp32 columns, then (MXFP8) per stage 4
@@ -226,6 +229,15 @@ struct GemmLayout {
     static_assert(SPLIT == 1 || kSplitEpi0Off + kSplitEH * 4 * kEpiWarpBytes <= STAGES * kStageBytes,
                   "split-K store staging in the ring");
     static constexpr uint32_t smem_bytes(uint32_t groups) { return 1024 + kTableOff + 8 * (groups + 1); }
+    // fp16/bf16, BN 64, plain GEMMs whose B has the two-row view (b.rows2):
+    // kRows2Slots staging slots of one k-block's even rows (32 x 128 bytes)
+    // and odd rows (32 x 144 bytes, 8 bytes early), where the group table
+    // would be
+    static constexpr uint32_t kRows2Slots = 4;
+    static constexpr uint32_t kRows2EvenBytes = 32 * 128;
+    static constexpr uint32_t kRows2Slot = kRows2EvenBytes + 32 * 144;
+    static constexpr uint32_t kRows2Off = (kTableOff + 127) & ~127u;
+    static constexpr uint32_t smem_bytes_rows2() { return 1024 + kRows2Off + kRows2Slots * kRows2Slot; }
 };
 
 // Warp-wide wait: every lane polls the barrier itself and the result is made
@@ -629,7 +641,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     uint64_t* tempty = bars + 2 * STAGES + ACC;
     uint64_t* drain = bars + 2 * STAGES + 2 * ACC;
     uint64_t* raw_full = bars + 2 * STAGES + 2 * ACC + 1;
-    uint64_t* recv = bars + 2 * STAGES + 2 * ACC + 3;
+    uint64_t* recv = bars + 2 * STAGES + 2 * ACC + 5;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     uint32_t* tmem_holder = misc;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -637,8 +649,11 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
-    const bool lanes_copy = KIND == kKindMXF8 || !(a_tma && b_tma);
-    const bool lanes_copy_ops = !(a_tma && b_tma);      // an operand TMA cannot fetch
+    // B through the two-row view (plain fp16/bf16, BN 64, A by TMA): warp
+    // kBWarp loads it by TMA into staging and rewrites it into the ring
+    const bool b_rows2 = KIND == kKindF16 && BN == 64 && prm.g.b.rows2 != 0;
+    const bool lanes_copy = KIND == kKindMXF8 || !(a_tma && (b_tma || b_rows2));
+    const bool lanes_copy_ops = !(a_tma && (b_tma || b_rows2));   // an operand goes through the load/store units
     // Operands TMA cannot fetch go through the load/store unit, whose
     // throughput per warp is the limit: for the CTA's first tile the epilogue
     // warps, idle until its accumulator is ready, copy too (six warps in all).
@@ -659,8 +674,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             // (fp16/bf16 with an operand TMA cannot fetch: warps 0 and kBWarp both
             // copy, and with copy helpers so do warps 2-5 -- on later tiles warp 0
             // arrives for them)
+            // (B through the two-row view: the A thread and the B warp's lane 0)
             mbar_init(&full[s], (KIND == kKindMXF8 && prm.g.sf_tma) ? 2u
                                 : lanes_copy ? (KIND == kKindF16 && lanes_copy_ops ? (copy_helpers ? 193u : 65u) : 33u)
+                                : b_rows2    ? 2u
                                              : 1u);
             mbar_init(&empty[s], 1);
         }
@@ -669,8 +686,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             mbar_init(&tempty[a], 128);
         }
         mbar_init(drain, 1);
-        mbar_init(&raw_full[0], 1);
-        mbar_init(&raw_full[1], 1);
+        for (uint32_t r = 0; r < 4; ++r) mbar_init(&raw_full[r], 1);   // MXFP8: 2 raw slots; two-row B: 4
         for (uint32_t o = 0; o < 8; ++o) mbar_init(&recv[o], 1);
         *abort_flag = 0;
         *tiles_smem = prm.g.total_tiles;
@@ -683,6 +699,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     if (warp == 0 && lane == 0) {
         if (a_tma) prefetch_tmap(&prm.tmap_a);
         if (b_tma) prefetch_tmap(&prm.tmap_b);
+        if (b_rows2) {
+            prefetch_tmap(&prm.tmap_sfa);
+            prefetch_tmap(&prm.tmap_sfb);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, Lay::kTmemCols);
@@ -765,9 +785,89 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         __syncwarp();
     };
 
+    // ------------------------------- B through the two-row view (warp kBWarp) --
+    // A 16-bit MN-major B whose pitch is 8 bytes off a multiple of 16 has no
+    // tensor map, but pairs of rows do: in a view with rows of 2*ld elements,
+    // a k-block's 32 even rows are one 64 x 32 box at x = n0 and its 32 odd
+    // rows one 72 x 32 box at x = ld + n0 - 4 (the nearest 16-byte boundary,
+    // 8 bytes early).  Lane 0 keeps four k-blocks of these boxes in flight in
+    // four staging slots (raw_full[] completes them); the whole warp then
+    // rewrites a k-block into the ring's B slot in the SW128 layout (line L
+    // = k-row L, 16-byte granule g at g ^ (L % 8)), fences it for the async
+    // proxy and arrives on the stage's full barrier (the A thread makes the
+    // other arrival, with A's bytes).
+    auto load_b_rows2 = [&]() {
+        constexpr uint32_t kSlot = Lay::kRows2Slot;
+        constexpr uint32_t kSlots = Lay::kRows2Slots;
+        constexpr uint32_t kTx = kSlot;                  // both boxes, out-of-range parts included
+        uint8_t* const stg = smem + Lay::kRows2Off;
+        const uint32_t nk = kb_hi - kb_lo;
+        const uint32_t my_tiles = t_first < total_tiles ? (total_tiles - t_first + t_step - 1) / t_step : 0u;
+        const uint32_t items = my_tiles * nk;
+        const int32_t ld = static_cast<int32_t>(prm.g.b.ld);
+        uint32_t t_cached = 0xFFFFFFFFu;
+        TileInfo ti_cached{};
+        auto issue = [&](uint32_t i) {                   // lane 0: item i into slot i % kSlots
+            const uint32_t t = t_first + (i / nk) * t_step;
+            if (t != t_cached) { ti_cached = tile_info(sa, t, kBM, BN, gt); t_cached = t; }
+            const int32_t n0 = static_cast<int32_t>(ti_cached.n * BN);
+            const int32_t y = static_cast<int32_t>(shuffled(kb_lo + i % nk, shuffle_rot(t)) * bk_elems / 2);
+            uint8_t* slot = stg + (i % kSlots) * kSlot;
+            mbar_arrive_expect_tx(&raw_full[i % kSlots], kTx);
+            tma_load_2d(slot, &prm.tmap_sfa, &raw_full[i % kSlots], n0, y);
+            tma_load_2d(slot + Lay::kRows2EvenBytes, &prm.tmap_sfb, &raw_full[i % kSlots], ld + n0 - 4, y);
+        };
+        if (lane == 0)
+            for (uint32_t i = 0; i < kSlots && i < items; ++i) issue(i);
+        __syncwarp();
+        uint32_t stage = 0, phase = 0;
+        uint32_t i = 0;
+        for (; i < items; ++i) {
+            if (!warp_wait(&raw_full[i % kSlots], (i / kSlots) & 1u, ctl, 9)) break;
+            if (i >= STAGES && !warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) break;
+            const uint8_t* even = stg + (i % kSlots) * kSlot;
+            const uint8_t* odd = even + Lay::kRows2EvenBytes;
+            uint8_t* dst = smem + stage * Lay::kStageBytes + Lay::kABytes;
+            const uint32_t g = lane & 7u;
+            // two batches of 8 granules per lane, all loads of a batch before
+            // its stores (loads and stores interleaved wait for each other)
+#pragma unroll
+            for (uint32_t half = 0; half < 2; ++half) {
+                uint2 lo[8], hi[8];
+#pragma unroll
+                for (uint32_t r = 0; r < 8; ++r) {
+                    const uint32_t L = (lane >> 3) + 4 * (half * 8 + r);
+                    const uint8_t* src = (L & 1u) ? odd + (L >> 1) * 144 + 8 + g * 16 : even + (L >> 1) * 128 + g * 16;
+                    lo[r] = *reinterpret_cast<const uint2*>(src);
+                    hi[r] = *reinterpret_cast<const uint2*>(src + 8);
+                }
+#pragma unroll
+                for (uint32_t r = 0; r < 8; ++r) {
+                    const uint32_t L = (lane >> 3) + 4 * (half * 8 + r);
+                    *reinterpret_cast<uint4*>(dst + L * kLine + ((g ^ (L & 7u)) << 4)) =
+                        make_uint4(lo[r].x, lo[r].y, hi[r].x, hi[r].y);
+                }
+            }
+            // the ring's bytes -> the MMA's reads; the staging slot's reads ->
+            // the next TMA writes into it
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&full[stage]);
+                if (tl && i < 7) tl[8 + i] = globaltimer_ns();
+                if (i + kSlots < items) issue(i + kSlots);
+            }
+            __syncwarp();
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (lane == 0)                                   // staging copies still in flight land before exit
+            for (uint32_t j = i; j < items && j < i + kSlots; ++j)
+                mbar_wait_drain(&raw_full[j % kSlots], (j / kSlots) & 1u, ctl.timeout_ns);
+    };
+
     constexpr uint32_t kBWarp = b_warp_for<KIND>();
     if (warp == 0 || (KIND == kKindMXF8 && warp == kScaleWarp) ||
-        (warp == kBWarp && (lanes_copy_ops ? KIND == kKindF16 : lane == 0))) {
+        (warp == kBWarp && ((lanes_copy_ops || b_rows2) ? KIND == kKindF16 : lane == 0))) {
         // ------------------------------------------------------ producer --
         const uint8_t* a_ptr = prm.g.a.ptr;
         const uint8_t* b_ptr = prm.g.b.ptr;
@@ -797,7 +897,9 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp)
                                                      : ((warp == 0 || (copy_split && warp == kBWarp)) && lanes_copy);
         const uint32_t copy_part = warp == kBWarp ? 1u : 0u, copy_parts = copy_split ? 2u : 1u;
-        if (tma_thread && !warp_copies) {
+        if (b_rows2 && warp == kBWarp) {
+            if constexpr (KIND == kKindF16 && BN == 64) load_b_rows2(); 
+        } else if (tma_thread && !warp_copies) {
             const bool is_a = warp == 0;
             const bool simple = !a_mn && !b_mn && !a_rank3 && !b_rank3;
             uint32_t stage = 0, phase = 0, issued = 0;
@@ -815,7 +917,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                     const int32_t row = is_a ? static_cast<int32_t>(ti.row0) : static_cast<int32_t>(n0);
                     const uint32_t rot = shuffle_rot(t);
                     for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+                        // the ring starts empty: only a stage being reused is waited for
+                        if (issued >= STAGES && !mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                         uint8_t* st = smem + stage * Lay::kStageBytes;
                         const int32_t k0 = static_cast<int32_t>(shuffled(kb, rot) * bk_elems);
                         if (is_a) mbar_arrive_expect_tx(&full[stage], tx);
@@ -828,7 +931,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
                 }
                 const uint32_t rot = shuffle_rot(t);
                 for (uint32_t kb = kb_lo; kb < kb_hi; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
+                    if (issued >= STAGES && !mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     const uint32_t k0 = shuffled(kb, rot) * bk_elems;
                     if (is_a) {

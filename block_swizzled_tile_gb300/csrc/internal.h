@@ -149,6 +149,7 @@ uint32_t smem_splitk(uint32_t bn, uint32_t splits);
 
 // Shared-memory bytes a launch needs (for validation of the device limit).
 uint32_t smem_dense(uint32_t bn, uint32_t groups);
+uint32_t smem_dense_rows2();   // BN 64 with B through the two-row view
 uint32_t smem_mxf8(uint32_t bn);
 uint32_t smem_dequant();
 uint32_t smem_pair(uint32_t bn, uint32_t groups);
@@ -179,7 +180,7 @@ cudaError_t launch_swizzle_map_grouped(const int32_t* group_m, uint32_t G, uint3
                                        uint32_t max_tasks, uint32_t* err, cudaStream_t stream);
 
 // Configurations instantiated for each kernel family.
-constexpr uint32_t kDenseStages64 = 8, kDenseStages128 = 6, kDenseStages256 = 4;
+constexpr uint32_t kDenseStages64 = 7, kDenseStages128 = 6, kDenseStages256 = 4;
 constexpr uint32_t kMxStages128 = 6, kMxStages256 = 3;
 // split-K tiles stage their epilogue stores in the idle ring, so 128 x 256
 // split tiles fit a fourth stage (more bytes in flight per SM)

@@ -163,6 +163,30 @@ def test_copied_operands_several_tiles_per_cta(tn, acol, lda_pad, ldb_pad):
     assert_close_f16(got, oracle_dense(w, "f16"))
 
 
+ROWS2 = [(500, 380, 256, 0), (300, 300, 1000, 0), (129, 60, 64, 0), (257, 500, 130, 0), (64, 132, 2, 0),
+         (500, 380, 256, 8), (200, 76, 255, 0)]
+
+
+@pytest.mark.parametrize("mnk_pad", ROWS2)
+@pytest.mark.parametrize("dt,out", [("f16", "f16"), ("bf16", "f32")])
+@pytest.mark.parametrize("kw", [{}, {"num_ctas": 3}, {"shuffle_k": 1}])
+def test_b_through_two_row_view(mnk_pad, dt, out, kw):
+    """Row-major B whose pitch is 8 bytes off a multiple of 16 (ldb = 4 mod 8)
+    goes through the two-row tensor-map view with 128 x 64 tiles: ragged N and
+    K tails, K = 2, several tiles per CTA, ShuffleK; an odd K (255) takes the
+    copy path instead."""
+    M, N, K, pad = mnk_pad
+    w = wl.dense16(M, N, K, dt, b_col_major=False, seed=M + N + K + pad, ldb=N + pad, dist="normal")
+    assert w["ldb"] % 8 == 4
+    lm, ln = -(-M // 128), -(-N // 64)
+    trace = torch.zeros(lm * ln * 5, dtype=torch.int32, device="cuda")
+    got = run_dense(w, out, bst.sched(2, 1, trace=trace, **kw))
+    assert_close_f16(got, oracle_dense(w, out))
+    if K % 2 == 0:
+        tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
+        assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, 64, 2, 1), dtype=np.uint32))
+
+
 @pytest.mark.parametrize("tm", [128, 256])
 @pytest.mark.parametrize("out,ldc_pad", [("f16", 1), ("f16", 2), ("bf16", 4), ("f16", 8), ("f32", 1), ("f32", 2),
                                          ("f32", 4)])

@@ -37,6 +37,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -642,6 +644,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     uint64_t* drain = bars + 2 * STAGES + 2 * ACC;
     uint64_t* raw_full = bars + 2 * STAGES + 2 * ACC + 1;
     uint64_t* recv = bars + 2 * STAGES + 2 * ACC + 5;
+    uint64_t* rows2_free = recv;                          // two-row view B (never split): 4 slot barriers
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     uint32_t* tmem_holder = misc;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -674,10 +677,10 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             // (fp16/bf16 with an operand TMA cannot fetch: warps 0 and kBWarp both
             // copy, and with copy helpers so do warps 2-5 -- on later tiles warp 0
             // arrives for them)
-            // (B through the two-row view: the A thread and the B warp's lane 0)
+            // (B through the two-row view: the A thread, and four from the rewriting warps)
             mbar_init(&full[s], (KIND == kKindMXF8 && prm.g.sf_tma) ? 2u
                                 : lanes_copy ? (KIND == kKindF16 && lanes_copy_ops ? (copy_helpers ? 193u : 65u) : 33u)
-                                : b_rows2    ? 2u
+                                : b_rows2    ? 5u
                                              : 1u);
             mbar_init(&empty[s], 1);
         }
@@ -687,7 +690,8 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         }
         mbar_init(drain, 1);
         for (uint32_t r = 0; r < 4; ++r) mbar_init(&raw_full[r], 1);   // MXFP8: 2 raw slots; two-row B: 4
-        for (uint32_t o = 0; o < 8; ++o) mbar_init(&recv[o], 1);
+        // (two-row view B: recv[0..3] are the staging slots' rows2_free, four arrivals each)
+        for (uint32_t o = 0; o < 8; ++o) mbar_init(&recv[o], (b_rows2 && o < 4) ? 4u : 1u);
         *abort_flag = 0;
         *tiles_smem = prm.g.total_tiles;
         fence_barrier_init();
@@ -790,20 +794,70 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
     // tensor map, but pairs of rows do: in a view with rows of 2*ld elements,
     // a k-block's 32 even rows are one 64 x 32 box at x = n0 and its 32 odd
     // rows one 72 x 32 box at x = ld + n0 - 4 (the nearest 16-byte boundary,
-    // 8 bytes early).  Lane 0 keeps four k-blocks of these boxes in flight in
-    // four staging slots (raw_full[] completes them); the whole warp then
-    // rewrites a k-block into the ring's B slot in the SW128 layout (line L
-    // = k-row L, 16-byte granule g at g ^ (L % 8)), fences it for the async
-    // proxy and arrives on the stage's full barrier (the A thread makes the
-    // other arrival, with A's bytes).
+    // 8 bytes early).  Lane 0 of warp kBWarp keeps four k-blocks of these
+    // boxes in flight in four staging slots (raw_full[] completes them).  A
+    // k-block is rewritten into the ring's B slot in the SW128 layout (line L
+    // = k-row L, 16-byte granule g at g ^ (L % 8)), fenced for the async proxy
+    // and arrived on the stage's full barrier, which expects the A thread (with
+    // A's bytes) and four arrivals: for the CTA's first tile the four epilogue
+    // warps (idle until its accumulator is ready) each rewrite 16 lines and
+    // arrive, and arrive on the slot's rows2_free barrier so that the slot is
+    // refilled only once all four have read it; for later tiles warp kBWarp
+    // rewrites all 64 lines and arrives for four.
+    const uint32_t rows2_nk = kb_hi - kb_lo;
+    const uint32_t rows2_items =
+        (t_first < total_tiles ? (total_tiles - t_first + t_step - 1) / t_step : 0u) * rows2_nk;
+    // lines [line0, line0 + 4 * reps) of item i's staging slot into the ring
+    auto rows2_convert = [&](uint32_t i, uint32_t line0, auto reps_c) {
+        constexpr uint32_t kReps = decltype(reps_c)::value;     // granules per lane
+        const uint8_t* even = smem + Lay::kRows2Off + (i % Lay::kRows2Slots) * Lay::kRows2Slot;
+        const uint8_t* odd = even + Lay::kRows2EvenBytes;
+        uint8_t* dst = smem + (i % STAGES) * Lay::kStageBytes + Lay::kABytes;
+        const uint32_t g = lane & 7u;
+        // batches of up to 8 granules per lane, all loads of a batch before its
+        // stores (interleaved, every store waits for the loads before it)
+#pragma unroll
+        for (uint32_t b0 = 0; b0 < kReps; b0 += 8) {
+            constexpr uint32_t kB = kReps < 8 ? kReps : 8;
+            uint2 lo[kB], hi[kB];
+#pragma unroll
+            for (uint32_t r = 0; r < kB; ++r) {
+                const uint32_t L = line0 + (lane >> 3) + 4 * (b0 + r);
+                const uint8_t* src = (L & 1u) ? odd + (L >> 1) * 144 + 8 + g * 16 : even + (L >> 1) * 128 + g * 16;
+                lo[r] = *reinterpret_cast<const uint2*>(src);
+                hi[r] = *reinterpret_cast<const uint2*>(src + 8);
+            }
+#pragma unroll
+            for (uint32_t r = 0; r < kB; ++r) {
+                const uint32_t L = line0 + (lane >> 3) + 4 * (b0 + r);
+                *reinterpret_cast<uint4*>(dst + L * kLine + ((g ^ (L & 7u)) << 4)) =
+                    make_uint4(lo[r].x, lo[r].y, hi[r].x, hi[r].y);
+            }
+        }
+        // the ring's bytes -> the MMA's reads; the slot's reads -> the next
+        // TMA writes into it
+        fence_proxy_async_smem();
+        __syncwarp();
+    };
+    // warps 2-5: the first tile's k-blocks, 16 lines each
+    auto rows2_help_first_tile = [&]() {
+        if (!b_rows2) return;
+        const uint32_t n = min(rows2_nk, rows2_items);
+        for (uint32_t i = 0; i < n; ++i) {
+            if (!warp_wait(&raw_full[i % Lay::kRows2Slots], (i / Lay::kRows2Slots) & 1u, ctl, 9)) break;
+            if (i >= STAGES && !warp_wait(&empty[i % STAGES], ((i / STAGES) & 1u) ^ 1u, ctl, 1)) break;
+            rows2_convert(i, (warp - 2) * 16, std::integral_constant<uint32_t, 4>{});
+            if (lane == 0) {
+                mbar_arrive(&full[i % STAGES]);
+                mbar_arrive(&rows2_free[i % Lay::kRows2Slots]);
+            }
+            __syncwarp();
+        }
+    };
+    // warp kBWarp: issues every item's boxes; rewrites the items after the first tile
     auto load_b_rows2 = [&]() {
-        constexpr uint32_t kSlot = Lay::kRows2Slot;
         constexpr uint32_t kSlots = Lay::kRows2Slots;
-        constexpr uint32_t kTx = kSlot;                  // both boxes, out-of-range parts included
-        uint8_t* const stg = smem + Lay::kRows2Off;
-        const uint32_t nk = kb_hi - kb_lo;
-        const uint32_t my_tiles = t_first < total_tiles ? (total_tiles - t_first + t_step - 1) / t_step : 0u;
-        const uint32_t items = my_tiles * nk;
+        const uint32_t nk = rows2_nk, items = rows2_items;
         const int32_t ld = static_cast<int32_t>(prm.g.b.ld);
         uint32_t t_cached = 0xFFFFFFFFu;
         TileInfo ti_cached{};
@@ -812,53 +866,30 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
             if (t != t_cached) { ti_cached = tile_info(sa, t, kBM, BN, gt); t_cached = t; }
             const int32_t n0 = static_cast<int32_t>(ti_cached.n * BN);
             const int32_t y = static_cast<int32_t>(shuffled(kb_lo + i % nk, shuffle_rot(t)) * bk_elems / 2);
-            uint8_t* slot = stg + (i % kSlots) * kSlot;
-            mbar_arrive_expect_tx(&raw_full[i % kSlots], kTx);
+            uint8_t* slot = smem + Lay::kRows2Off + (i % kSlots) * Lay::kRows2Slot;
+            mbar_arrive_expect_tx(&raw_full[i % kSlots], Lay::kRows2Slot);   // both boxes, out-of-range parts included
             tma_load_2d(slot, &prm.tmap_sfa, &raw_full[i % kSlots], n0, y);
             tma_load_2d(slot + Lay::kRows2EvenBytes, &prm.tmap_sfb, &raw_full[i % kSlots], ld + n0 - 4, y);
         };
         if (lane == 0)
             for (uint32_t i = 0; i < kSlots && i < items; ++i) issue(i);
         __syncwarp();
-        uint32_t stage = 0, phase = 0;
         uint32_t i = 0;
         for (; i < items; ++i) {
-            if (!warp_wait(&raw_full[i % kSlots], (i / kSlots) & 1u, ctl, 9)) break;
-            if (i >= STAGES && !warp_wait(&empty[stage], phase ^ 1u, ctl, 1)) break;
-            const uint8_t* even = stg + (i % kSlots) * kSlot;
-            const uint8_t* odd = even + Lay::kRows2EvenBytes;
-            uint8_t* dst = smem + stage * Lay::kStageBytes + Lay::kABytes;
-            const uint32_t g = lane & 7u;
-            // two batches of 8 granules per lane, all loads of a batch before
-            // its stores (loads and stores interleaved wait for each other)
-#pragma unroll
-            for (uint32_t half = 0; half < 2; ++half) {
-                uint2 lo[8], hi[8];
-#pragma unroll
-                for (uint32_t r = 0; r < 8; ++r) {
-                    const uint32_t L = (lane >> 3) + 4 * (half * 8 + r);
-                    const uint8_t* src = (L & 1u) ? odd + (L >> 1) * 144 + 8 + g * 16 : even + (L >> 1) * 128 + g * 16;
-                    lo[r] = *reinterpret_cast<const uint2*>(src);
-                    hi[r] = *reinterpret_cast<const uint2*>(src + 8);
-                }
-#pragma unroll
-                for (uint32_t r = 0; r < 8; ++r) {
-                    const uint32_t L = (lane >> 3) + 4 * (half * 8 + r);
-                    *reinterpret_cast<uint4*>(dst + L * kLine + ((g ^ (L & 7u)) << 4)) =
-                        make_uint4(lo[r].x, lo[r].y, hi[r].x, hi[r].y);
-                }
+            if (i < nk) {
+                // the helpers rewrite it; refill its slot once they all have
+                if (i + kSlots < items && !warp_wait(&rows2_free[i % kSlots], (i / kSlots) & 1u, ctl, 10)) break;
+            } else {
+                if (!warp_wait(&raw_full[i % kSlots], (i / kSlots) & 1u, ctl, 9)) break;
+                if (i >= STAGES && !warp_wait(&empty[i % STAGES], ((i / STAGES) & 1u) ^ 1u, ctl, 1)) break;
+                rows2_convert(i, 0u, std::integral_constant<uint32_t, 16>{});
+                if (lane == 0) mbar_arrive_cnt(&full[i % STAGES], 4u);
             }
-            // the ring's bytes -> the MMA's reads; the staging slot's reads ->
-            // the next TMA writes into it
-            fence_proxy_async_smem();
-            __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&full[stage]);
                 if (tl && i < 7) tl[8 + i] = globaltimer_ns();
                 if (i + kSlots < items) issue(i + kSlots);
             }
             __syncwarp();
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (lane == 0)                                   // staging copies still in flight land before exit
             for (uint32_t j = i; j < items && j < i + kSlots; ++j)
@@ -1181,6 +1212,7 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         if (has_k && t_first < total_tiles) acc_ok = warp_wait(&tfull[0], 0, ctl, 4);
     } else if (warp >= 2 && warp < 6) {
         copy_first_tile_as_helper();
+        if constexpr (KIND == kKindF16 && BN == 64) rows2_help_first_tile();
         // ----------------------------------------------------- epilogue --
         const uint32_t q = warp & 3u;            // TMEM lane quarter of this warp
         const uint32_t r = q * 32 + lane;        // tile row of this thread

@@ -909,27 +909,26 @@ __global__ void __launch_bounds__(threads_for<KIND>(), 1) gemm_kernel(const __gr
         const uint8_t* sfb = prm.g.sfb;
         const uint32_t sf_ld = prm.g.sf_ld;
         const uint32_t tx = (a_tma ? Lay::kABytes : 0u) + (b_tma ? Lay::kBBytes : 0u);
-        // The TMA thread runs a loop of its own that contains no warp-synchronous
-        // operation: mixing it with the warp-wide copy loop (whose waits end in
-        // __syncwarp / shfl.sync) made every iteration pay for reconvergence
-        // bookkeeping, and a tight single-thread loop issues a k-block in about
-        // half the time.  Lanes copy only for the MXFP8 scale factors (their own
-        // warp) and for operands TMA cannot fetch (warp 0, which then also
-        // carries the TMA issue).
-        // Both operands through TMA: lane 0 of warp 0 issues the A loads and is
-        // the one arrival on full[] (expecting the bytes of A and B), lane 0 of
-        // warp kBWarp issues the B loads; both wait for the stage to be empty.
-        // A B load may land before the A thread's expect_tx: the transaction
-        // count goes negative meanwhile and the missing arrival keeps the phase
-        // open.  Lanes copy only for the MXFP8 scale factors (their own warp)
-        // and for operands TMA cannot fetch (warp 0 then issues every load).
+        // Roles of the load warps:
+        // - Both operands through TMA: lane 0 of warp 0 issues the A loads and
+        //   is the one arrival on full[] (expecting the bytes of A and B), lane
+        //   0 of warp kBWarp issues the B loads.  A B load may land before the A
+        //   thread's expect_tx: the transaction count goes negative meanwhile and
+        //   the missing arrival keeps the phase open.  A thread running such a
+        //   loop alone issues a k-block in about half the time of one that shares
+        //   a warp-synchronous loop.
+        // - B through the two-row view: warp kBWarp as a whole (load_b_rows2).
+        // - An operand TMA cannot fetch: warps 0 and kBWarp copy it with their
+        //   lanes (the epilogue warps help on the first tile); lane 0 of warp 0
+        //   also issues the TMA half of a mixed stage.
+        // - MXFP8: the scale warp copies the scale factors.
         const bool copy_split = KIND == kKindF16 && lanes_copy_ops;   // warps 0 and kBWarp share the copies
         const bool tma_thread = (warp == 0 && lane == 0) || (warp == kBWarp && lane == 0 && !copy_split);
         const bool warp_copies = (KIND == kKindMXF8) ? (warp == kScaleWarp)
                                                      : ((warp == 0 || (copy_split && warp == kBWarp)) && lanes_copy);
         const uint32_t copy_part = warp == kBWarp ? 1u : 0u, copy_parts = copy_split ? 2u : 1u;
         if (b_rows2 && warp == kBWarp) {
-            if constexpr (KIND == kKindF16 && BN == 64) load_b_rows2(); 
+            if constexpr (KIND == kKindF16 && BN == 64) load_b_rows2();
         } else if (tma_thread && !warp_copies) {
             const bool is_a = warp == 0;
             const bool simple = !a_mn && !b_mn && !a_rank3 && !b_rank3;

@@ -187,6 +187,17 @@ def test_b_through_two_row_view(mnk_pad, dt, out, kw):
         assert np.array_equal(tr, np.array(osw.swizzle_map(M, N, 128, 64, 2, 1), dtype=np.uint32))
 
 
+@pytest.mark.parametrize("mnk", [(256, 380, 128), (136, 124, 320)])
+def test_b_two_row_view_with_column_major_a(mnk):
+    """The two-row view of B beside an MN-major (column-major) A loaded by TMA
+    in 64-row atoms, with an output pitch that is not 16-byte aligned."""
+    M, N, K = mnk
+    w = wl.dense16(M, N, K, "f16", a_col_major=True, b_col_major=False, seed=M + K, dist="normal")
+    assert w["ldb"] % 8 == 4 and (w["lda"] * 2) % 16 == 0
+    got = run_dense(w, "f16", bst.sched(1, 0), ldc=N + 3)
+    assert_close_f16(got, oracle_dense(w, "f16"))
+
+
 @pytest.mark.parametrize("tm", [128, 256])
 @pytest.mark.parametrize("out,ldc_pad", [("f16", 1), ("f16", 2), ("bf16", 4), ("f16", 8), ("f32", 1), ("f32", 2),
                                          ("f32", 4)])

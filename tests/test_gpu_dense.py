@@ -164,7 +164,7 @@ def test_copied_operands_several_tiles_per_cta(tn, acol, lda_pad, ldb_pad):
 
 
 ROWS2 = [(500, 380, 256, 0), (300, 300, 1000, 0), (129, 60, 64, 0), (257, 500, 130, 0), (64, 132, 2, 0),
-         (500, 380, 256, 8), (200, 76, 255, 0)]
+         (500, 380, 256, 8), (200, 76, 255, 0), (70, 4, 66, 0), (33, 12, 130, 0)]
 
 
 @pytest.mark.parametrize("mnk_pad", ROWS2)

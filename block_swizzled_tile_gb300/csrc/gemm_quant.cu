@@ -12,6 +12,15 @@
 
 namespace bst {
 
+// BST_WIDEN_BULK=0 keeps the dense widening on ordinary loads and stores
+static bool widen_bulk_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("BST_WIDEN_BULK");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 cudaError_t launch_dequant(const GemmParams& p, uint32_t grid, cudaStream_t stream) {
     using Lay = GemmLayout<128, kDequantStages, 2, kKindF16>;
     static std::atomic<uint64_t> attr_done{0};
@@ -110,16 +119,106 @@ __global__ void widen_s8_bf16_flat_kernel(const int8_t* __restrict__ src, uint16
     }
 }
 
+// The dense widening as a bulk-copy stream: each CTA takes chunks of 16 KB of
+// int8 (grid stride), one thread loads them with cp.async.bulk into a ring
+// of four slots, the whole CTA converts a chunk into 32 KB of bf16 in shared
+// memory, and the same thread stores it with a bulk copy.  Loads run four
+// chunks ahead; a slot's output is refilled once its previous store has read
+// it.  The last CTA widens the tail (fewer than 16 KB) with plain loads.  A
+// wait for a chunk gives up after timeout_ns and records kErrTimeout.
+constexpr uint32_t kWidenChunk = 16384;                 // int8 bytes per chunk
+constexpr uint32_t kWidenSlots = 4;
+constexpr uint32_t kWidenThreads = 256;
+constexpr uint32_t kWidenSmem = kWidenSlots * (kWidenChunk + 2 * kWidenChunk) + kWidenSlots * 8;
+
+__global__ void __launch_bounds__(kWidenThreads, 1)
+widen_s8_bf16_bulk_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__ dst, uint64_t n, uint32_t* err,
+                          uint64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    uint8_t* const in = sm;
+    uint8_t* const out = sm + kWidenSlots * kWidenChunk;
+    uint64_t* const full = reinterpret_cast<uint64_t*>(out + kWidenSlots * 2 * kWidenChunk);
+    const uint64_t nchunks = n / kWidenChunk;
+    const uint64_t first = blockIdx.x, step = gridDim.x;
+    const uint64_t mine = first < nchunks ? (nchunks - first + step - 1) / step : 0;
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < kWidenSlots; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    auto load = [&](uint64_t i) {                       // thread 0: chunk i of this CTA into slot i % 4
+        const uint32_t s = static_cast<uint32_t>(i % kWidenSlots);
+        mbar_arrive_expect_tx(&full[s], kWidenChunk);
+        bulk_load_global(in + s * kWidenChunk, src + (first + i * step) * kWidenChunk, kWidenChunk, &full[s]);
+    };
+    if (threadIdx.x == 0)
+        for (uint64_t i = 0; i < kWidenSlots && i < mine; ++i) load(i);
+    uint64_t i = 0;
+    for (; i < mine; ++i) {
+        const uint32_t s = static_cast<uint32_t>(i % kWidenSlots);
+        const bool got = mbar_wait_drain(&full[s], static_cast<uint32_t>((i / kWidenSlots) & 1u), timeout_ns);
+        if (__syncthreads_or(!got)) {
+            if (threadIdx.x == 0) atomicOr(err, kErrTimeout);
+            break;
+        }
+        // the store that last read this output slot (chunk i - 4) has finished
+        // reading it: at most three newer stores are still pending
+        if (threadIdx.x == 0 && i >= kWidenSlots) bulk_wait_read_3();
+        __syncthreads();
+        const int4* q = reinterpret_cast<const int4*>(in + s * kWidenChunk);
+        uint4* o = reinterpret_cast<uint4*>(out + s * 2 * kWidenChunk);
+#pragma unroll
+        for (uint32_t u = 0; u < kWidenChunk / 16 / kWidenThreads; ++u) {
+            const uint32_t g = u * kWidenThreads + threadIdx.x;
+            const int4 r = q[g];
+            o[2 * g] = widen16_lo(r);
+            o[2 * g + 1] = widen16_hi(r);
+        }
+        fence_proxy_async_smem();                       // generic writes -> the bulk store's reads
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bulk_store_global(dst + (first + i * step) * kWidenChunk, out + s * 2 * kWidenChunk, 2 * kWidenChunk);
+            bulk_commit_group();
+            if (i + kWidenSlots < mine) load(i + kWidenSlots);
+        }
+    }
+    if (threadIdx.x == 0) {
+        bulk_wait_all();                                // the stores have completed
+        // chunks loaded but not consumed (an abort) land before the CTA exits
+        for (uint64_t j = i; j < mine && j < i + kWidenSlots; ++j)
+            mbar_wait_drain(&full[j % kWidenSlots], static_cast<uint32_t>((j / kWidenSlots) & 1u), timeout_ns);
+    }
+    if (blockIdx.x == gridDim.x - 1) {
+        // the tail: n - nchunks * 16 KB elements, a multiple of 16
+        const uint64_t t0 = nchunks * kWidenChunk / 16, t1 = n / 16;
+        const int4* s4 = reinterpret_cast<const int4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        for (uint64_t g = t0 + threadIdx.x; g < t1; g += kWidenThreads) {
+            const int4 r = __ldg(s4 + g);
+            d4[2 * g] = widen16_lo(r);
+            d4[2 * g + 1] = widen16_hi(r);
+        }
+    }
+}
+
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
                                  int64_t cols, uint32_t sms, cudaStream_t stream, int64_t batch, int64_t bs_src,
-                                 int64_t bs_dst) {
+                                 int64_t bs_dst, uint32_t* err, uint64_t timeout_ns) {
     if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
     const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (ld_src % 16 == 0) && (bs_src % 16 == 0) &&
                     (reinterpret_cast<uintptr_t>(dst) % 16 == 0) && (ld_dst % 8 == 0) && (bs_dst % 8 == 0);
     const bool dense = vec && cols % 16 == 0 && ld_src == cols && ld_dst == cols &&
                        (batch == 1 || (bs_src == rows * cols && bs_dst == rows * cols));
+    const uint64_t n = static_cast<uint64_t>(rows) * cols * batch;
+    if (dense && err && n >= 2ull * sms * kWidenChunk && widen_bulk_enabled()) {
+        static std::atomic<uint64_t> attr_done{0};
+        cudaError_t e = set_smem_once(reinterpret_cast<const void*>(widen_s8_bf16_bulk_kernel), kWidenSmem, attr_done);
+        if (e != cudaSuccess) return e;
+        widen_s8_bf16_bulk_kernel<<<sms, kWidenThreads, kWidenSmem, stream>>>(src, dst, n, err, timeout_ns);
+        return cudaGetLastError();
+    }
     if (dense) {
-        widen_s8_bf16_flat_kernel<<<sms * 4, 256, 0, stream>>>(src, dst, rows * cols * batch / 16);
+        widen_s8_bf16_flat_kernel<<<sms * 4, 256, 0, stream>>>(src, dst, n / 16);
         return cudaGetLastError();
     }
     widen_s8_bf16_kernel<<<sms * 4, 256, 0, stream>>>(src, ld_src, bs_src, dst, ld_dst, bs_dst, rows, cols, batch, vec);

@@ -155,9 +155,12 @@ uint32_t smem_dequant();
 uint32_t smem_pair(uint32_t bn, uint32_t groups);
 
 // int8 [rows, cols] (ld_src elements) -> bf16 [rows, cols] (ld_dst elements)
+// err / timeout_ns: the device error word and the wait limit of the bulk-copy
+// widening (large dense operands); without err the ordinary-load kernels run
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
                                  int64_t cols, uint32_t sms, cudaStream_t stream, int64_t batch = 1,
-                                 int64_t bs_src = 0, int64_t bs_dst = 0);
+                                 int64_t bs_src = 0, int64_t bs_dst = 0, uint32_t* err = nullptr,
+                                 uint64_t timeout_ns = 0);
 
 // grouped slice-K: per-group tensor maps (G x 256 bytes at `maps`) and
 // k-block counts plus a status word (G + 1 words at `group_kb`), from the

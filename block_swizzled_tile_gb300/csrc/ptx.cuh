@@ -606,6 +606,27 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, const
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// global -> this CTA's shared memory, bytes a multiple of 16, both addresses
+// 16-byte aligned; completes on bar
+__device__ __forceinline__ void bulk_load_global(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// this CTA's shared memory -> global (a bulk group; see bulk_commit_group)
+__device__ __forceinline__ void bulk_store_global(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// at most three committed bulk groups may still be reading their sources
+__device__ __forceinline__ void bulk_wait_read_3() { asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); }
+
+// every committed bulk group has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // waits until every committed bulk copy of this thread has finished reading its source
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 

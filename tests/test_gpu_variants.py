@@ -299,6 +299,20 @@ def test_int8_extreme_sums_exact():
         assert_close_fro(out, rout, FRO_MX)
 
 
+@pytest.mark.parametrize("mnk", [(3001, 1040, 2048), (2432, 1300, 2048)])
+def test_int8_bulk_widening_with_and_without_tail(mnk):
+    """A is large enough for the bulk-copy widening (at least 2 x SMs x 16 KB
+    of int8): 3001 x 2048 leaves a tail of 2048 elements past the last whole
+    16 KB chunk for the ordinary-load tail, 2432 x 2048 none.  Every int32
+    accumulator bit-exact."""
+    M, N, K = mnk
+    w = wl.int8_per_token(M, N, K, seed=M + N)
+    out, acc = run_int8(w, True)
+    racc, rout = oracle_int8_rows(w, np.arange(M))
+    assert np.array_equal(acc, racc)
+    assert_close_fro(out, rout, FRO_MX)
+
+
 @functools.lru_cache(maxsize=1)
 def _int8_full_oracle():
     w = wl.int8_per_token()

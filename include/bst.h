@@ -24,9 +24,17 @@
  *    wait that gave up, inconsistent group sizes) are recorded in a per-device
  *    error word and reported by bst_check_async.
  *  - Operands whose base address and leading dimension are 16-byte aligned
- *    are fetched with TMA; others are fetched with ordinary loads (slower,
- *    same results).  There is no CPU fallback: without a usable sm_103a
- *    device the call returns BST_ERR_CUDA.
+ *    are fetched with TMA.  A row-major fp16/bf16 B whose pitch is 8 bytes
+ *    off a multiple of 16 (plain GEMMs, even K) is fetched with TMA through
+ *    a view of pairs of its rows; other operands with ordinary loads
+ *    (slower, same results).  There is no CPU fallback: without a usable
+ *    sm_103a device the call returns BST_ERR_CUDA.
+ *  - Environment switches, read once per process (for measurement; the
+ *    results do not change): BST_PDL=0 launches without programmatic
+ *    dependent launch; BST_PREFETCH_MB=n sets the operand size up to which
+ *    a kernel pulls its operands into L2 at start (default 32, 0 = never);
+ *    BST_ROWS2=0 turns the two-row view of B off; BST_WIDEN_BULK=0 widens
+ *    int8 operands with ordinary loads instead of bulk copies.
  *  - Empty outputs (M == 0 or N == 0) return BST_OK without a launch; K == 0
  *    writes zeros.
  *  - The library holds no mutable host state except cached device properties,

@@ -203,8 +203,10 @@ class Workload:
         # enough copies that the bytes between two uses of one copy exceed L2
         self.copies = copies or max(1, min(4096, math.ceil(2 * L2_BYTES / per_set)))
         self.sched = bst.sched(1, 0)
-        self.launches_per_step = {"int8_per_token": 3, "grouped_int8_per_token": 3, "grouped_slice_k_bf16": 2,
-                                  "grouped_slice_k_int8": 4}.get(name, 1)
+        # kernels per call: int8 widens both operands in one bulk-copy launch
+        # before its GEMM; slice-K rewrites its per-group maps in a prep launch
+        self.launches_per_step = {"int8_per_token": 2, "grouped_int8_per_token": 2, "grouped_slice_k_bf16": 2,
+                                  "grouped_slice_k_int8": 3}.get(name, 1)
         self._alloc()
 
     def _alloc(self):

@@ -956,11 +956,10 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     if (tiles >= (1ull << 32)) return BST_ERR_INVALID_ARG;
     if ((pair ? smem_pair_dequant() : smem_dequant()) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
-    cudaError_t e = launch_widen_s8_bf16(A, lda, wa, kp, M, K, dev.sms, stream, 1, 0, 0, dev.err, timeout_ns());
-    if (e == cudaSuccess)
-        e = b_kmajor ? launch_widen_s8_bf16(B, ldb, wb, ldwb, N, K, dev.sms, stream, 1, 0, 0, dev.err, timeout_ns())
-                     : launch_widen_s8_bf16(B, ldb, wb, ldwb, K, N, dev.sms, stream, 1, 0, 0, dev.err, timeout_ns());
-    if (e != cudaSuccess) return BST_ERR_CUDA;
+    const WidenArgs wa_args{A, lda, wa, kp, M, K};
+    const WidenArgs wb_args = b_kmajor ? WidenArgs{B, ldb, wb, ldwb, N, K} : WidenArgs{B, ldb, wb, ldwb, K, N};
+    if (launch_widen2_s8_bf16(wa_args, wb_args, dev.sms, stream, dev.err, timeout_ns()) != cudaSuccess)
+        return BST_ERR_CUDA;
 
     OperandSpec a{wa, 2, static_cast<uint64_t>(M), static_cast<uint64_t>(K), kp, 0, 1, false};
     OperandSpec b{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(K), ldwb, 0, 1, !b_kmajor};
@@ -1055,11 +1054,10 @@ bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, i
     if (tiles_bound >= (1ull << 32)) return BST_ERR_INVALID_ARG;
     if (smem_pair_dequant() + 8 * (static_cast<uint32_t>(G) + 1) > dev.max_smem) return BST_ERR_UNSUPPORTED;
 
-    cudaError_t e = launch_widen_s8_bf16(A, lda, wa, kp, total_m, K, dev.sms, stream, 1, 0, 0, dev.err, timeout_ns());
-    if (e == cudaSuccess)
-        e = launch_widen_s8_bf16(B, ldb, wb, ldwb, b_rows, b_cols, dev.sms, stream, G, G > 1 ? stride_b : 0, per_group,
-                                 dev.err, timeout_ns());
-    if (e != cudaSuccess) return BST_ERR_CUDA;
+    const WidenArgs wa_args{A, lda, wa, kp, total_m, K};
+    const WidenArgs wb_args{B, ldb, wb, ldwb, b_rows, b_cols, G, G > 1 ? stride_b : 0, per_group};
+    if (launch_widen2_s8_bf16(wa_args, wb_args, dev.sms, stream, dev.err, timeout_ns()) != cudaSuccess)
+        return BST_ERR_CUDA;
 
     OperandSpec a{wa, 2, static_cast<uint64_t>(total_m), static_cast<uint64_t>(K), kp, 0, 1, false};
     OperandSpec b{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(K), ldwb, per_group,
@@ -1203,14 +1201,10 @@ bst_status bst_gemm_grouped_slice_k_quant_per_token(int32_t G, const int32_t* gr
     uint16_t* wa = reinterpret_cast<uint16_t*>(meta + meta_bytes);
     uint16_t* wb = reinterpret_cast<uint16_t*>(meta + meta_bytes + a_bytes);
     const int64_t ldwa = a_kmajor ? kp : mp, ldwb = b_kmajor ? kp : np;
-    cudaError_t e = a_kmajor ? launch_widen_s8_bf16(A, lda, wa, ldwa, M, total_k, dev.sms, stream, 1, 0, 0, dev.err,
-                                                    timeout_ns())
-                             : launch_widen_s8_bf16(A, lda, wa, ldwa, total_k, M, dev.sms, stream, 1, 0, 0, dev.err,
-                                                    timeout_ns());
-    if (e == cudaSuccess)
-        e = b_kmajor ? launch_widen_s8_bf16(B, ldb, wb, ldwb, N, total_k, dev.sms, stream, 1, 0, 0, dev.err, timeout_ns())
-                     : launch_widen_s8_bf16(B, ldb, wb, ldwb, total_k, N, dev.sms, stream, 1, 0, 0, dev.err, timeout_ns());
-    if (e != cudaSuccess) return BST_ERR_CUDA;
+    const WidenArgs wa_args = a_kmajor ? WidenArgs{A, lda, wa, ldwa, M, total_k} : WidenArgs{A, lda, wa, ldwa, total_k, M};
+    const WidenArgs wb_args = b_kmajor ? WidenArgs{B, ldb, wb, ldwb, N, total_k} : WidenArgs{B, ldb, wb, ldwb, total_k, N};
+    if (launch_widen2_s8_bf16(wa_args, wb_args, dev.sms, stream, dev.err, timeout_ns()) != cudaSuccess)
+        return BST_ERR_CUDA;
     SliceKRun r;
     r.a = OperandSpec{wa, 2, static_cast<uint64_t>(M), static_cast<uint64_t>(total_k), ldwa, 0, 1, !a_kmajor};
     r.b = OperandSpec{wb, 2, static_cast<uint64_t>(N), static_cast<uint64_t>(total_k), ldwb, 0, 1, !b_kmajor};

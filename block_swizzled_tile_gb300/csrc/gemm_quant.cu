@@ -131,14 +131,25 @@ constexpr uint32_t kWidenSlots = 4;
 constexpr uint32_t kWidenThreads = 256;
 constexpr uint32_t kWidenSmem = kWidenSlots * (kWidenChunk + 2 * kWidenChunk) + kWidenSlots * 8;
 
+struct WidenSeg {
+    const int8_t* src;
+    uint16_t* dst;
+    uint64_t n;                                         // elements, a multiple of 16
+};
+
+// Both operands of a GEMM in one launch: the chunks of segment 0, then those
+// of segment 1 (n = 0 for a single operand).
 __global__ void __launch_bounds__(kWidenThreads, 1)
-widen_s8_bf16_bulk_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__ dst, uint64_t n, uint32_t* err,
-                          uint64_t timeout_ns) {
+widen_s8_bf16_bulk_kernel(WidenSeg s0, WidenSeg s1, uint32_t* err, uint64_t timeout_ns) {
     extern __shared__ __align__(128) uint8_t sm[];
     uint8_t* const in = sm;
     uint8_t* const out = sm + kWidenSlots * kWidenChunk;
     uint64_t* const full = reinterpret_cast<uint64_t*>(out + kWidenSlots * 2 * kWidenChunk);
-    const uint64_t nchunks = n / kWidenChunk;
+    const uint64_t c0 = s0.n / kWidenChunk;
+    const uint64_t nchunks = c0 + s1.n / kWidenChunk;
+    // chunk c of the joint sequence: its source and destination
+    auto chunk_src = [&](uint64_t c) { return c < c0 ? s0.src + c * kWidenChunk : s1.src + (c - c0) * kWidenChunk; };
+    auto chunk_dst = [&](uint64_t c) { return c < c0 ? s0.dst + c * kWidenChunk : s1.dst + (c - c0) * kWidenChunk; };
     const uint64_t first = blockIdx.x, step = gridDim.x;
     const uint64_t mine = first < nchunks ? (nchunks - first + step - 1) / step : 0;
     if (threadIdx.x == 0) {
@@ -149,7 +160,7 @@ widen_s8_bf16_bulk_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__
     auto load = [&](uint64_t i) {                       // thread 0: chunk i of this CTA into slot i % 4
         const uint32_t s = static_cast<uint32_t>(i % kWidenSlots);
         mbar_arrive_expect_tx(&full[s], kWidenChunk);
-        bulk_load_global(in + s * kWidenChunk, src + (first + i * step) * kWidenChunk, kWidenChunk, &full[s]);
+        bulk_load_global(in + s * kWidenChunk, chunk_src(first + i * step), kWidenChunk, &full[s]);
     };
     if (threadIdx.x == 0)
         for (uint64_t i = 0; i < kWidenSlots && i < mine; ++i) load(i);
@@ -177,7 +188,7 @@ widen_s8_bf16_bulk_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__
         fence_proxy_async_smem();                       // generic writes -> the bulk store's reads
         __syncthreads();
         if (threadIdx.x == 0) {
-            bulk_store_global(dst + (first + i * step) * kWidenChunk, out + s * 2 * kWidenChunk, 2 * kWidenChunk);
+            bulk_store_global(chunk_dst(first + i * step), out + s * 2 * kWidenChunk, 2 * kWidenChunk);
             bulk_commit_group();
             if (i + kWidenSlots < mine) load(i + kWidenSlots);
         }
@@ -189,16 +200,50 @@ widen_s8_bf16_bulk_kernel(const int8_t* __restrict__ src, uint16_t* __restrict__
             mbar_wait_drain(&full[j % kWidenSlots], static_cast<uint32_t>((j / kWidenSlots) & 1u), timeout_ns);
     }
     if (blockIdx.x == gridDim.x - 1) {
-        // the tail: n - nchunks * 16 KB elements, a multiple of 16
-        const uint64_t t0 = nchunks * kWidenChunk / 16, t1 = n / 16;
-        const int4* s4 = reinterpret_cast<const int4*>(src);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-        for (uint64_t g = t0 + threadIdx.x; g < t1; g += kWidenThreads) {
-            const int4 r = __ldg(s4 + g);
-            d4[2 * g] = widen16_lo(r);
-            d4[2 * g + 1] = widen16_hi(r);
+        // the tails: past each segment's last whole chunk, a multiple of 16 elements
+        for (uint32_t k = 0; k < 2; ++k) {
+            const WidenSeg& sg = k ? s1 : s0;
+            const uint64_t t0 = sg.n / kWidenChunk * kWidenChunk / 16, t1 = sg.n / 16;
+            const int4* s4 = reinterpret_cast<const int4*>(sg.src);
+            uint4* d4 = reinterpret_cast<uint4*>(sg.dst);
+            for (uint64_t g = t0 + threadIdx.x; g < t1; g += kWidenThreads) {
+                const int4 r = __ldg(s4 + g);
+                d4[2 * g] = widen16_lo(r);
+                d4[2 * g + 1] = widen16_hi(r);
+            }
         }
     }
+}
+
+static cudaError_t launch_widen_bulk(WidenSeg s0, WidenSeg s1, uint32_t sms, cudaStream_t stream, uint32_t* err,
+                                     uint64_t timeout_ns) {
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(widen_s8_bf16_bulk_kernel), kWidenSmem, attr_done);
+    if (e != cudaSuccess) return e;
+    widen_s8_bf16_bulk_kernel<<<sms, kWidenThreads, kWidenSmem, stream>>>(s0, s1, err, timeout_ns);
+    return cudaGetLastError();
+}
+
+// A dense operand (rows and batches back to back in source and destination,
+// 16-byte aligned, whole 16-element groups): its element count, else 0.
+static uint64_t dense_elems(const WidenArgs& w) {
+    if (w.rows <= 0 || w.cols <= 0 || w.batch <= 0) return 0;
+    const bool ok = reinterpret_cast<uintptr_t>(w.src) % 16 == 0 && reinterpret_cast<uintptr_t>(w.dst) % 16 == 0 &&
+                    w.cols % 16 == 0 && w.ld_src == w.cols && w.ld_dst == w.cols &&
+                    (w.batch == 1 || (w.bs_src == w.rows * w.cols && w.bs_dst == w.rows * w.cols));
+    return ok ? static_cast<uint64_t>(w.rows) * w.cols * w.batch : 0u;
+}
+
+cudaError_t launch_widen2_s8_bf16(const WidenArgs& a, const WidenArgs& b, uint32_t sms, cudaStream_t stream,
+                                  uint32_t* err, uint64_t timeout_ns) {
+    const uint64_t na = dense_elems(a), nb = dense_elems(b);
+    if (na && nb && err && na + nb >= 2ull * sms * kWidenChunk && widen_bulk_enabled())
+        return launch_widen_bulk(WidenSeg{a.src, a.dst, na}, WidenSeg{b.src, b.dst, nb}, sms, stream, err, timeout_ns);
+    cudaError_t e = launch_widen_s8_bf16(a.src, a.ld_src, a.dst, a.ld_dst, a.rows, a.cols, sms, stream, a.batch,
+                                         a.bs_src, a.bs_dst, err, timeout_ns);
+    if (e != cudaSuccess) return e;
+    return launch_widen_s8_bf16(b.src, b.ld_src, b.dst, b.ld_dst, b.rows, b.cols, sms, stream, b.batch, b.bs_src,
+                                b.bs_dst, err, timeout_ns);
 }
 
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,
@@ -210,13 +255,8 @@ cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* ds
     const bool dense = vec && cols % 16 == 0 && ld_src == cols && ld_dst == cols &&
                        (batch == 1 || (bs_src == rows * cols && bs_dst == rows * cols));
     const uint64_t n = static_cast<uint64_t>(rows) * cols * batch;
-    if (dense && err && n >= 2ull * sms * kWidenChunk && widen_bulk_enabled()) {
-        static std::atomic<uint64_t> attr_done{0};
-        cudaError_t e = set_smem_once(reinterpret_cast<const void*>(widen_s8_bf16_bulk_kernel), kWidenSmem, attr_done);
-        if (e != cudaSuccess) return e;
-        widen_s8_bf16_bulk_kernel<<<sms, kWidenThreads, kWidenSmem, stream>>>(src, dst, n, err, timeout_ns);
-        return cudaGetLastError();
-    }
+    if (dense && err && n >= 2ull * sms * kWidenChunk && widen_bulk_enabled())
+        return launch_widen_bulk(WidenSeg{src, dst, n}, WidenSeg{src, dst, 0}, sms, stream, err, timeout_ns);
     if (dense) {
         widen_s8_bf16_flat_kernel<<<sms * 4, 256, 0, stream>>>(src, dst, n / 16);
         return cudaGetLastError();

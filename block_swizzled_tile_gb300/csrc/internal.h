@@ -155,6 +155,22 @@ uint32_t smem_dequant();
 uint32_t smem_pair(uint32_t bn, uint32_t groups);
 
 // int8 [rows, cols] (ld_src elements) -> bf16 [rows, cols] (ld_dst elements)
+// One int8 operand to widen into a bf16 copy (leading dimensions and batch
+// strides in elements).
+struct WidenArgs {
+    const int8_t* src;
+    int64_t ld_src;
+    uint16_t* dst;
+    int64_t ld_dst;
+    int64_t rows, cols;
+    int64_t batch = 1, bs_src = 0, bs_dst = 0;
+};
+
+// Both operands of an int8 GEMM: one bulk-copy launch when both are dense,
+// else one launch each.
+cudaError_t launch_widen2_s8_bf16(const WidenArgs& a, const WidenArgs& b, uint32_t sms, cudaStream_t stream,
+                                  uint32_t* err, uint64_t timeout_ns);
+
 // err / timeout_ns: the device error word and the wait limit of the bulk-copy
 // widening (large dense operands); without err the ordinary-load kernels run
 cudaError_t launch_widen_s8_bf16(const int8_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst, int64_t rows,

@@ -1,5 +1,6 @@
 """GPU parity of the fp16/bf16 path (bst_gemm, bst_gemm_batched) and of the
 device scheduler (bst_swizzle_map) against the CPU oracle."""
+import functools
 import itertools
 
 import numpy as np
@@ -311,6 +312,23 @@ def test_pair_fp16_square_workload(S, d):
     assert_close_f16(got, oracle_dense(w, "f16"))
     tr = trace.cpu().numpy().view(np.uint32).reshape(-1, 5)
     assert np.array_equal(tr, np.array(osw.swizzle_map(1024, 1024, 256, 256, S, d), dtype=np.uint32))
+
+
+@functools.lru_cache(maxsize=1)
+def _large_bf16():
+    w = wl.dense16(8192, 2048, 8192, "bf16", b_col_major=True, seed=81)
+    return w, oracle_dense(w, "bf16")
+
+
+@pytest.mark.parametrize("S,d", [(1, 1), (8, 1), (4, 0)])
+def test_pair_large_operands_l2_priority_and_alternating_k(S, d):
+    """bf16 8192 x 2048 x 8192 on CTA-pair tiles.  Under Nz the window streams
+    A (134 MB, more than half of L2): its loads are marked evict_first, B's
+    evict_last, and odd waves of tiles run their K loop from the last k-block
+    down.  Under Zn the streamed operand is B (33.5 MB) and neither applies.
+    Every element within the tolerance of the oracle."""
+    w, ref = _large_bf16()
+    assert_close_f16(run_dense(w, "bf16", bst.sched(S, d)), ref)
 
 
 def test_pair_needs_tma_operands():

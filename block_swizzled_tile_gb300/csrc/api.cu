@@ -108,33 +108,6 @@ struct Sched {
     uint64_t* timeline = nullptr;
 };
 
-// L2 priority and K direction of the CTA-pair kernels' operand loads.  Under
-// the Zn order the tiles of one window share A's row panels over several
-// waves of tiles and read each B column panel in one wave (Nz: the other way
-// round).  When the operand read once per window (per batch) is larger than
-// half of L2, it pushes the shared panels out before the next wave reads them
-// again.  Then the shared operand's loads are marked evict_last and the
-// other's evict_first, and odd waves run their K loop backwards, so that they
-// start on the k-blocks the previous wave read last.  BST_L2_HINT (0 none,
-// 1 both hints, 2 evict_last only, 3 evict_first only) and BST_K_ALT (0 / 1)
-// override the choice.
-int env_choice(const char* name) {
-    const char* e = std::getenv(name);
-    return (e && e[0] >= '0' && e[0] <= '9') ? static_cast<int>(std::strtol(e, nullptr, 10)) : -1;
-}
-
-void set_l2_policy(GemmArgs& g, const Sched& sch, uint64_t a_bytes, uint64_t b_bytes) {
-    static const int hint_env = env_choice("BST_L2_HINT");
-    static const int alt_env = env_choice("BST_K_ALT");
-    const uint64_t streamed = sch.dir == 0 ? b_bytes : a_bytes;
-    const bool big = streamed > (64ull << 20);
-    const int mode = hint_env >= 0 ? hint_env : (big ? 1 : 0);
-    const uint32_t shared = (mode == 1 || mode == 2) ? 1u : 0u;
-    const uint32_t other = (mode == 1 || mode == 3) ? 2u : 0u;
-    g.l2_hint = sch.dir == 0 ? (shared | other << 2) : (other | shared << 2);
-    g.k_alt = (alt_env >= 0 ? alt_env != 0 : big) ? 1u : 0u;
-}
-
 bst_status read_sched(const bst_sched* s, Sched& out) {
     if (!s) return BST_OK;
     if (s->swizzle_offset < 1 || s->swizzle_direction > 1) return BST_ERR_INVALID_ARG;
@@ -565,7 +538,6 @@ bst_status run_dense(uint32_t mode, int64_t M, int64_t N, int64_t K, const void*
     p.g.timeout_ns = timeout_ns();
     p.g.dynamic = sch.dynamic;
     p.g.shuffle_k = sch.shuffle_k;
-    set_l2_policy(p.g, sch, a.mn * a.k * a.esize, b.mn * b.k * b.esize);
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (copy_split) return cuda_status(launch_dense_split(p, bn, splits, static_cast<uint32_t>(tiles), stream));
@@ -729,7 +701,6 @@ bst_status run_mxf8(int64_t M, int64_t N, int64_t K, const void* A, bst_layout l
     p.g.timeout_ns = timeout_ns();
     p.g.dynamic = sch.dynamic;
     p.g.shuffle_k = sch.shuffle_k;
-    set_l2_policy(p.g, sch, 0, 0);
     set_prefetch(p.g, a, b, sfa, static_cast<uint64_t>(M) * (K / 32), sfb, static_cast<uint64_t>(N) * (K / 32));
     if (splits > 1) return cuda_status(launch_mxf8_split(p, bn, splits, static_cast<uint32_t>(tiles), stream));
     if (pair) return cuda_status(launch_mxf8_pair(p, bn, pair_grid(sch, tiles, dev.sms), stream));
@@ -827,7 +798,6 @@ bst_status run_slice_k(const SliceKRun& r, int32_t G, const int32_t* group_k, in
     p.g.timeout_ns = timeout_ns();
     p.g.dynamic = sch.dynamic;
     p.g.shuffle_k = sch.shuffle_k;
-    set_l2_policy(p.g, sch, 0, 0);   // per group the operands are small
     const uint32_t pairs = pair_grid(sch, tiles, dev.sms);
     return cuda_status(r.dequant ? launch_pair_dequant(p, pairs, stream) : launch_pair(p, bn, pairs, stream));
 }
@@ -923,7 +893,6 @@ bst_status bst_gemm_grouped(int32_t G, const int32_t* group_m, int64_t total_m, 
     p.g.timeout_ns = timeout_ns();
     p.g.dynamic = sch.dynamic;
     p.g.shuffle_k = sch.shuffle_k;
-    set_l2_policy(p.g, sch, 0, 0);   // per group the operands are small
     set_prefetch(p.g, a, b, nullptr, 0, nullptr, 0);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (pair)
@@ -1024,7 +993,6 @@ bst_status bst_gemm_quant_per_token(int64_t M, int64_t N, int64_t K, const int8_
     p.g.timeout_ns = timeout_ns();
     p.g.dynamic = sch.dynamic;
     p.g.shuffle_k = sch.shuffle_k;
-    set_l2_policy(p.g, sch, static_cast<uint64_t>(M) * K * 2, static_cast<uint64_t>(N) * K * 2);
     const uint32_t ctas = sch.num_ctas ? sch.num_ctas : dev.sms;
     if (pair)
         return cuda_status(launch_pair_dequant(p, pair_grid(sch, tiles, dev.sms),
@@ -1126,7 +1094,6 @@ bst_status bst_gemm_grouped_quant_per_token(int32_t G, const int32_t* group_m, i
     p.g.timeout_ns = timeout_ns();
     p.g.dynamic = sch.dynamic;
     p.g.shuffle_k = sch.shuffle_k;
-    set_l2_policy(p.g, sch, 0, 0);   // per group the operands are small
     return cuda_status(launch_pair_dequant(p, pair_grid(sch, tiles_bound, dev.sms), stream));
 }
 

@@ -110,10 +110,6 @@ struct GemmArgs {
     const uint32_t* group_kb;  // slice-K: k-blocks of each group, then a status word (non-zero: bad sizes)
     uint32_t dynamic;          // CTA-pair kernels: tasks claimed through cluster launch control
     uint32_t shuffle_k;        // each tile starts its K loop at k-block (task % k-blocks)
-    uint32_t k_alt;            // CTA-pair kernels: tasks of odd waves (task / clusters odd) run their K
-                               // loop from the last k-block down
-    uint32_t l2_hint;          // CTA-pair kernels: L2 priority of the TMA loads, A in bits 0-1 and B in
-                               // bits 2-3 (0 normal, 1 evict_last, 2 evict_first)
     int32_t* acc_out;
     const uint8_t* sfa;
     const uint8_t* sfb;

@@ -236,16 +236,6 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
         // single threads issue the loads (cheaper per k-block than a
         // warp-wide loop with one active lane)
         const uint32_t role = (rank == 0 && is_a) ? 0u : 1u;
-        const uint32_t hint = (prm.g.l2_hint >> (is_a ? 0u : 2u)) & 3u;
-        const uint64_t pol = hint ? l2_policy(hint) : 0ull;
-        auto load2 = [&](void* dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y) {
-            if (hint) tma_load_2d_pair_hint(dst, m, bar, x, y, pol);
-            else tma_load_2d_pair(dst, m, bar, x, y);
-        };
-        auto load3 = [&](void* dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y, int32_t z) {
-            if (hint) tma_load_3d_pair_hint(dst, m, bar, x, y, z, pol);
-            else tma_load_3d_pair(dst, m, bar, x, y, z);
-        };
         if (lane == 0 && dyn && role == 0 && cid < total_tiles) ok = tasks.request(ctl);
         for (uint32_t t = cid; lane == 0 && ok && t < total_tiles; t = tasks.next(t, ok, role, ctl)) {
             const TileInfo ti = tile_info(sa, t, TM, BN, gt);
@@ -264,33 +254,32 @@ __global__ void __launch_bounds__(pair_threads<EPI>(), 1) gemm_pair_kernel(const
             }
             // ShuffleK: the K loop of task t starts at k-block t % tkb
             const uint32_t rot = (prm.g.shuffle_k && tkb) ? t % tkb : 0u;
-            const bool down = prm.g.k_alt && ((t / nclusters) & 1u);
             for (uint32_t kb = 0; kb < tkb; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, ctl, 1)) { ok = false; break; }
                 {
                     uint8_t* sa_s = smem + stage * Lay::kStageBytes;
                     uint8_t* sb_s = sa_s + Lay::kABytes;
                     const uint32_t bar = full_leader + stage * 8;
-                    const uint32_t kx = (down ? tkb - 1u - kb : kb) + rot;
+                    const uint32_t kx = kb + rot;
                     const int32_t k0 = (kx < tkb ? kx : kx - tkb) * bk_elems;
                     if (is_a) {
                         if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                         if (!a_mn) {
-                            if (a_rank3) load3(sa_s, map_a, bar, k0, a_row, zc);
-                            else load2(sa_s, map_a, bar, k0, a_row);
+                            if (a_rank3) tma_load_3d_pair(sa_s, map_a, bar, k0, a_row, zc);
+                            else tma_load_2d_pair(sa_s, map_a, bar, k0, a_row);
                         } else {
                             for (uint32_t j = 0; j < kBM / bk_elems; ++j) {
-                                if (a_rank3) load3(sa_s + j * bk_elems * kLine, map_a, bar, a_row + j * bk_elems, k0, zc);
-                                else load2(sa_s + j * bk_elems * kLine, map_a, bar, a_row + j * bk_elems, k0);
+                                if (a_rank3) tma_load_3d_pair(sa_s + j * bk_elems * kLine, map_a, bar, a_row + j * bk_elems, k0, zc);
+                                else tma_load_2d_pair(sa_s + j * bk_elems * kLine, map_a, bar, a_row + j * bk_elems, k0);
                             }
                         }
                     } else if (!b_mn) {
-                        if (b_rank3) load3(sb_s, map_b, bar, k0, b_col, zc);
-                        else load2(sb_s, map_b, bar, k0, b_col);
+                        if (b_rank3) tma_load_3d_pair(sb_s, map_b, bar, k0, b_col, zc);
+                        else tma_load_2d_pair(sb_s, map_b, bar, k0, b_col);
                     } else {
                         for (uint32_t j = 0; j < BH / bk_elems; ++j) {
-                            if (b_rank3) load3(sb_s + j * bk_elems * kLine, map_b, bar, b_col + j * bk_elems, k0, zc);
-                            else load2(sb_s + j * bk_elems * kLine, map_b, bar, b_col + j * bk_elems, k0);
+                            if (b_rank3) tma_load_3d_pair(sb_s + j * bk_elems * kLine, map_b, bar, b_col + j * bk_elems, k0, zc);
+                            else tma_load_2d_pair(sb_s + j * bk_elems * kLine, map_b, bar, b_col + j * bk_elems, k0);
                         }
                     }
                     if (tl && is_a && issued < 15) tl[1 + issued] = globaltimer_ns();

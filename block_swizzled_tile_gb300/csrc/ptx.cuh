@@ -535,34 +535,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z));
 }
 
-// L2 eviction priority for the bulk tensor loads below: 1 = evict_last (an
-// operand panel the next wave of tiles reads again), 2 = evict_first (a panel
-// read by one wave only); 0 is never passed (the plain loads are used)
-__device__ __forceinline__ uint64_t l2_policy(uint32_t code) {
-    uint64_t pol;
-    if (code == 1u)
-        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    else
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                                      int32_t x, int32_t y, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "l"(pol));
-}
-
-__device__ __forceinline__ void tma_load_3d_pair_hint(void* dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                                      int32_t x, int32_t y, int32_t z, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "l"(pol));
-}
-
 // collective over the pair: executed by one warp in each of the two CTAs
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

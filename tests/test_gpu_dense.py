@@ -321,12 +321,10 @@ def _large_bf16():
 
 
 @pytest.mark.parametrize("S,d", [(1, 1), (8, 1), (4, 0)])
-def test_pair_large_operands_l2_priority_and_alternating_k(S, d):
-    """bf16 8192 x 2048 x 8192 on CTA-pair tiles.  Under Nz the window streams
-    A (134 MB, more than half of L2): its loads are marked evict_first, B's
-    evict_last, and odd waves of tiles run their K loop from the last k-block
-    down.  Under Zn the streamed operand is B (33.5 MB) and neither applies.
-    Every element within the tolerance of the oracle."""
+def test_pair_large_operands_several_waves(S, d):
+    """bf16 8192 x 2048 x 8192 on CTA-pair tiles: 256 tiles over the 76 pairs of
+    the persistent grid (several waves), operands of 134 and 33.5 MB, both
+    window directions.  Every element within the tolerance of the oracle."""
     w, ref = _large_bf16()
     assert_close_f16(run_dense(w, "bf16", bst.sched(S, d)), ref)
 

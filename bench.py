@@ -679,6 +679,60 @@ def roofline_of(work, per_step_ms, clocks, peaks, src, setting=None):
     return entry
 
 
+TIMELINE_CTAS = 8192          # rows of 64 stamps in the --timeline buffer
+
+
+def timeline_rows(stamps):
+    """Per stamp slot that any CTA wrote: (slot, min, median, max) in us from
+    the first CTA's entry (slot 0), over the CTAs that wrote it.  `stamps` is
+    [CTAs, 64] of %globaltimer ns, 0 where nothing was written."""
+    t = np.asarray(stamps, dtype=np.int64)
+    t = t[t[:, 0] > 0]
+    if not len(t):
+        return []
+    t0 = t[:, 0].min()
+    rows = []
+    for c in range(t.shape[1]):
+        v = t[:, c]
+        v = v[v > 0]
+        if len(v):
+            us = (v - t0) / 1e3
+            rows.append((c, float(us.min()), float(np.median(us)), float(us.max())))
+    return rows
+
+
+def timeline_report(args):
+    """--timeline N: N launches of the workload back to back (schedule from
+    --swizzle, default Zn1), then one more whose kernel writes its
+    %globaltimer stamps (the `timeline` field of bst_sched; the slots are
+    listed in include/bst.h); three rounds.  Prints the CUDA-event time of
+    the stamped launch and, per slot, min / median / max over the CTAs."""
+    torch.cuda.set_device(0)
+    work = Workload(args.workload)
+    opts = sched_opts(args)
+    S, d = (int(args.swizzle[2:]), 0 if args.swizzle.startswith("Zn") else 1) if args.swizzle else (1, 0)
+    buf = torch.zeros(TIMELINE_CTAS * 64, dtype=torch.int64, device="cuda")
+    plain = work.bst.sched(S, d, **opts)
+    stamped = work.bst.sched(S, d, timeline=buf, **opts)
+    for _ in range(3):
+        for i in range(args.timeline):
+            work.step(i, plain)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        work.step(args.timeline, stamped)
+        e1.record()
+        torch.cuda.synchronize()
+    work.bst.check_async()
+    rows = timeline_rows(buf.view(TIMELINE_CTAS, 64).cpu().numpy())
+    ctas = int((buf.view(TIMELINE_CTAS, 64)[:, 0] > 0).sum())
+    print("%s %s%d, after %d launches: stamped launch %.2f us (CUDA events), %d CTAs"
+          % (args.workload, "Zn" if d == 0 else "Nz", S, args.timeline, e0.elapsed_time(e1) * 1e3, ctas))
+    print("slot      min   median      max  (us from the first CTA's entry)")
+    for c, lo, med, hi in rows:
+        print("%4d %8.2f %8.2f %8.2f" % (c, lo, med, hi))
+
+
 def measure(name, args, world, rank, stream, sampler, cpu_budget, steps):
     """One workload: swizzle choice, warm-up, clock-sampled soak and exactly
     `steps` timed steps, the end-to-end leg and the oracle on the host.
@@ -785,12 +839,17 @@ def main():
     ap.add_argument("--dynamic", type=int, default=0, choices=[0, 1],
                     help="1: tasks claimed at run time through cluster launch control (CTA-pair tiles)")
     ap.add_argument("--shuffle-k", type=int, default=0, choices=[0, 1], help="1: ShuffleK (rotated K start per task)")
+    ap.add_argument("--timeline", type=int, default=0,
+                    help="N > 0: print the kernel's pipeline stamps of one launch after N plain launches, no JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     if args.impl == "reference":
         reference_arm(args, args.workload)
+        return
+    if args.timeline > 0:
+        timeline_report(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -79,5 +79,17 @@ def assert_close_fro(got, ref, fro):
     assert e <= fro, "relative Frobenius error %.3g > %.3g" % (e, fro)
 
 
+def assert_special_equal(got, ref, fro):
+    """NaN positions, and infinity positions with their signs, equal the
+    reference's; the finite rest is within the relative Frobenius bound."""
+    assert got.shape == ref.shape
+    nan_r, inf_r = np.isnan(ref), np.isinf(ref)
+    assert np.array_equal(np.isnan(got), nan_r), "NaN positions differ"
+    assert np.array_equal(np.isinf(got), inf_r), "infinity positions differ"
+    assert np.array_equal(got[inf_r], ref[inf_r]), "infinity signs differ"
+    ok = ~(nan_r | inf_r)
+    assert_close_fro(got[ok], ref[ok], fro)
+
+
 DT = {"f16": bst.F16, "bf16": bst.BF16, "f32": bst.F32}
 OUT_BYTES = {"f16": 2, "bf16": 2, "f32": 4}

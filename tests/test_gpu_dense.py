@@ -10,7 +10,8 @@ import torch
 import block_swizzled_tile_gb300 as bst
 from block_swizzled_tile_gb300 import workloads as wl
 from oracle import gemm as og, swizzle as osw
-from tests.gpu_util import (DT, OUT_BYTES, assert_close_f16, canary_intact, decode_out, dev, empty_bytes, host)
+from tests.gpu_util import (DT, FRO_F16, OUT_BYTES, assert_close_f16, assert_special_equal, canary_intact,
+                            decode_out, dev, empty_bytes, host)
 from tests.swizzle_checks import check_map
 
 pytestmark = pytest.mark.gpu
@@ -231,6 +232,32 @@ def test_special_values_identity_and_zero():
     assert np.array_equal(got, decode_out(w["a"].copy(), "f16"))   # A.I == A exactly
     w_zero = dict(w, b=np.zeros_like(eye))
     assert not run_dense(w_zero, "f32").any()
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_special_values_inf_nan_and_overflow(dt):
+    """IEEE special values through the fp32 accumulation and the output cast:
+    an infinity in row 3 of A makes that row +-inf, with NaN where it meets a
+    zero of B (inf x 0); a NaN makes row 7 NaN; for fp16, a row of 65504s
+    makes sums past the fp16 range round to +-inf.  NaN and infinity positions
+    (with signs) equal the oracle's; the finite rest is within the tolerance."""
+    M, N, K = 256, 256, 128
+    w = wl.dense16(M, N, K, dt, seed=9)
+    inf, nan, big = (0x7C00, 0x7E00, 0x7BFF) if dt == "f16" else (0x7F80, 0x7FC0, None)
+    a, b = w["a"].copy(), w["b"].copy()          # row-major [M, K] and [K, N] bit patterns
+    a[3, 10] = inf
+    a[7, 20] = nan
+    b[10, 9] = 0
+    if big is not None:
+        a[11, :] = big
+        b[:, 5] = big
+    got = run_dense(dict(w, a=a, b=b), dt)
+    # the plain definition summed without BLAS (whose kernels need not keep
+    # IEEE infinities and NaNs), rounded once by the oracle
+    acc = np.einsum("ik,kj->ij", og.decode(a, dt), og.decode(b, dt))
+    ref = decode_out(og.round_out(acc, dt), dt)
+    assert np.isnan(ref[7]).all() and np.isnan(ref[3, 9]) and np.isinf(ref[3, 0])
+    assert_special_equal(got, ref, FRO_F16)
 
 
 # ------------------------------------------------------------- batched -----

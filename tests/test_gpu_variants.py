@@ -10,8 +10,8 @@ import torch
 import block_swizzled_tile_gb300 as bst
 from block_swizzled_tile_gb300 import workloads as wl
 from oracle import formats, gemm as og, swizzle as osw
-from tests.gpu_util import (FRO_MX, assert_close_f16, assert_close_fro, canary_intact, decode_out, dev,
-                            empty_bytes, host)
+from tests.gpu_util import (FRO_MX, assert_close_f16, assert_close_fro, assert_special_equal, canary_intact,
+                            decode_out, dev, empty_bytes, host)
 
 pytestmark = pytest.mark.gpu
 CANARY = 256
@@ -126,6 +126,25 @@ def test_mxfp8_unit_scales_and_single_block():
     got = run_mx(w, bst.sched(1, 0, tile_n=128), out="f32")
     ref = decode_out(og.gemm_mxfp8(w["a"], w["sa"], w["b"], w["sb"], "f32"), "f32")
     assert_close_fro(got, ref, 1e-5)
+
+
+@pytest.mark.parametrize("K", [256, 1024])
+def test_mxfp8_nan_code_and_nan_scale(K):
+    """The NaN encodings of the MX formats: e4m3 S.1111.111 in row 5 of A makes
+    output row 5 NaN; the E8M0 scale 0xFF on a 32-element block of column 200
+    of B makes output column 200 NaN.  K = 256 runs one-CTA tiles, K = 1024
+    the CTA pair.  NaN positions equal the oracle's; the rest is within the
+    tolerance."""
+    M, N = 256, 256
+    w = wl.mxfp8(M, N, K, seed=11)
+    w["a"][5, 77] = 0x7F
+    w["sb"][200, 3] = 0xFF
+    got = run_mx(w, bst.sched(1, 0, tile_n=128))
+    # the oracle's operands, summed without BLAS, rounded once by the oracle
+    acc = np.einsum("ik,jk->ij", og.mx_dequant_operand(w["a"], w["sa"]), og.mx_dequant_operand(w["b"], w["sb"]))
+    ref = decode_out(og.round_out(acc, "bf16"), "bf16")
+    assert np.isnan(ref[5]).all() and np.isnan(ref[:, 200]).all() and np.isnan(ref).sum() == M + N - 1
+    assert_special_equal(got, ref, FRO_MX)
 
 
 @pytest.mark.parametrize("tn", [128, 256])

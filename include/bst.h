@@ -104,16 +104,27 @@ typedef struct {
                                    nActual}.  For grouped calls it must hold
                                    (ceil(total_m/128) + G) * ceil(N/tile_n) tasks.
                                    Debug only.                                        */
-    uint64_t* timeline;         /* optional DEVICE buffer of 64 uint64 per CTA; when
-                                   non-NULL the GEMM kernels write %globaltimer stamps
-                                   (ns) of their pipeline events: [0] start, [1..15]
-                                   producer k-block issues, [16..31] MMA k-block starts,
-                                   [32..39] epilogue tile starts, [40..47] epilogue tile
-                                   ends, [48..50] producer/MMA/epilogue exit.  Split-K
-                                   kernels instead use [32] accumulator ready, [34] / [33]
-                                   partials sent / received, [36..39] exit steps, and per
-                                   epilogue warp [48..51] partials received, [40..43]
-                                   stores done.  Profiling only.                       */
+    uint64_t* timeline;         /* optional DEVICE buffer of 64 uint64 per CTA (row =
+                                   block index); when non-NULL the GEMM kernels write
+                                   %globaltimer stamps (ns) of their pipeline events.
+                                   Persistent kernels: [0] set-up done (after the
+                                   grid-dependency wait), [1..15] A-load issues of the
+                                   first k-blocks, [8..14] copy or two-row-view B
+                                   batches, [16..31] MMA k-block starts, [32..39] /
+                                   [40..47] epilogue tile starts / ends, [48..50] exit
+                                   of warps 0, 1, 2; one-CTA kernels also [55] entry and
+                                   [56] / [57] before / after the first tile's
+                                   coordinates; the MXFP8 pair kernel instead has [0]
+                                   entry, [53] / [52] after the wait / the dependent-
+                                   launch trigger, [54] first load, [56..61] scale
+                                   groups rewritten.  Split-K pair kernels: [0] entry,
+                                   [44] after the wait, [1] after the trigger, [2..15]
+                                   A-load issues, [16..31] MMA k-block starts, [32]
+                                   accumulator ready, [34] / [33] partials sent /
+                                   received, per epilogue warp [48..51] partials
+                                   received and [40..43] stores done, [36] epilogue done,
+                                   [39] / [37] cluster barrier passed / TMEM freed.
+                                   Profiling only (bench.py --timeline prints them).   */
     uint32_t shuffle_k;         /* 1: ShuffleK ("Block Dispatch Policies",
                                    ENABLE_SHUFFLE_K): the K loop of task t starts at
                                    k-block t % (k-blocks of the tile) and wraps, so
